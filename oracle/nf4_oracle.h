@@ -1,0 +1,86 @@
+/*
+ * nf4_oracle.h -- CPU oracle for the NF4-dequant-fused backward-A GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path includes, links or
+ * calls this code: only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or helper with the
+ * CUDA library; the NF4 codebook in nf4_oracle.c is typed a second time on
+ * purpose.
+ *
+ * What it computes (page "aprender-gpu 0.32.0 -- src/kernels/backward/
+ * nf4_tensor_core.rs", struct doc comment):
+ *
+ *     grad_A[M x K] = grad_out[M x N] @ dequant(B_nf4[K x N])^T
+ *
+ * in plain loops, with the operands rounded the way that page's kernel rounds
+ * them (fp32 scale * codebook, then f32 -> f16; grad_out f32 -> f16) and the
+ * sum taken in fp64 (double), sequentially over n.
+ *
+ * Layouts (same page, build_ptx, "PHASE 2: Dequant B_nf4"):
+ *   scales  fp32 [N][K/64]              scale of (column n, 64-element K-block b)
+ *   data    u8   [N][K/2]               byte of element (k, n) at n*(K/2) + k/2,
+ *                                       low nibble = even k, high nibble = odd k
+ *   B       fp32 [K][N] row-major       the dense weight that nf4o_quantize reads
+ *   go      [M][N] row-major            fp32, or bf16 given as raw uint16 bits
+ *   result  fp64 [rows][K]
+ *
+ * Every function returns 0 on success and a negative value on bad arguments.
+ */
+#ifndef NF4_ORACLE_H
+#define NF4_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { NF4O_F32 = 0, NF4O_BF16 = 1 };
+
+/* The 16-value NormalFloat4 codebook, ascending. */
+void nf4o_codebook(float out[16]);
+
+/* IEEE 754 binary32 -> binary16, round to nearest even, gradual underflow,
+ * overflow to infinity, NaN kept quiet.  Integer bit operations only. */
+uint16_t nf4o_f32_to_f16(float x);
+void nf4o_f32_to_f16_array(const float* x, long long count, uint16_t* out);
+double nf4o_f16_to_f64(uint16_t h);
+float nf4o_bf16_to_f32(uint16_t b);
+
+/* Quantise B fp32 [K][N] (row-major) into packed NF4 codes and absmax scales.
+ * K must be a positive multiple of 64, N positive. */
+int nf4o_quantize(const float* B, int K, int N, uint8_t* data, float* scales);
+
+/* The code of element (k, n), read back from the packed data. */
+int nf4o_code_at(const uint8_t* data, int K, int k, int n);
+
+/* deq(B)[k, n] = f16( fp32(scale[n][k/64] * codebook[code(k, n)]) ), written
+ * transposed as raw f16 bits bt[n*K + k]. */
+int nf4o_dequantize_f16(const float* scales, const uint8_t* data, int K, int N,
+                        uint16_t* bt);
+
+/* Round grad_out to the f16 operand the GEMM multiplies: f32 -> f16 (RNE), or
+ * bf16 -> f32 (exact) -> f16 (RNE). */
+int nf4o_round_operand(const void* go, int dtype, long long count, uint16_t* out);
+
+/* ref[i][k] = sum_n f16(go)[rows[i], n] * deq(B)[k, n], in fp64, n ascending;
+ * bound[i][k] = the same sum over absolute values of the products (may be
+ * NULL).  go16 is [M][N] f16 bits, bt is [N][K] f16 bits. */
+int nf4o_backward_a_rows(const uint16_t* go16, const uint16_t* bt,
+                         int M, int N, int K, const int* rows, int nrows,
+                         double* ref, double* bound);
+
+/* Whole problem from raw inputs: rounds go, dequantises B, and computes every
+ * row.  ref and bound are [M][K]; bound may be NULL. */
+int nf4o_backward_a(const void* go, int dtype, const float* scales,
+                    const uint8_t* data, int M, int N, int K,
+                    double* ref, double* bound);
+
+/* OpenMP thread control for the row loops (1 when built without OpenMP). */
+void nf4o_set_threads(int n);
+int nf4o_max_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
