@@ -1,0 +1,187 @@
+"""Python binding of libnf4bwd.so: the NF4-dequant-fused backward-A GEMM.
+
+    grad_A[M x K] = grad_out[M x N] @ dequant(B_nf4[K x N])^T
+
+(page "aprender-gpu 0.32.0 -- src/kernels/backward/nf4_tensor_core.rs", struct
+doc comment.)  Argument marshalling only: every step runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream; the functions
+enqueue work on ``torch.cuda.current_stream()`` and return without waiting.
+
+There is no fallback: if the compiled library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libnf4bwd.so")
+
+NF4_OK = 0
+NF4_ERR_INVALID = 1
+NF4_ERR_ALIGN = 2
+NF4_ERR_CUDA = 3
+NF4_ERR_TIMEOUT = 4
+NF4_ERR_WORKSPACE = 5
+NF4_F32 = 0
+NF4_BF16 = 1
+
+# Every function the header declares, with (restype, argtypes).
+_vp, _i, _sz = C.c_void_p, C.c_int, C.c_size_t
+
+
+class Nf4Problem(C.Structure):
+    """Mirror of ``nf4_problem``."""
+    _fields_ = [("grad_out", _vp), ("go_dtype", _i), ("scales", _vp), ("data", _vp),
+                ("grad_A", _vp), ("M", _i), ("N", _i), ("K", _i)]
+
+
+SIGNATURES = {
+    "nf4_abi_version": (_i, []),
+    "nf4_status_string": (C.c_char_p, [_i]),
+    "nf4_quantize": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
+    "nf4_dequantize_f16": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
+    "nf4_backward_a": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "nf4_backward_a_ex": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "nf4_backward_a_batched_workspace": (_sz, [_i]),
+    "nf4_backward_a_batched": (_i, [C.POINTER(Nf4Problem), _i, _vp, _sz, _vp]),
+    "nf4_check_error": (_i, [_vp]),
+}
+
+_lib = None
+
+
+class Nf4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def lib() -> C.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m backward_gemm_gb300.build` (or __graft_entry__.build())")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().nf4_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != NF4_OK:
+        raise Nf4Error(rc, what)
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return NF4_F32
+    if t.dtype == torch.bfloat16:
+        return NF4_BF16
+    raise TypeError(f"grad_out must be float32 or bfloat16, got {t.dtype}")
+
+
+def _require_cuda_contig(name: str, t: torch.Tensor) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class NF4Weight:
+    """A frozen weight B [K x N] in NF4: ``data`` u8 [N, K/2], ``scales`` f32 [N, K/64]."""
+
+    def __init__(self, data: torch.Tensor, scales: torch.Tensor, K: int, N: int):
+        self.data, self.scales, self.K, self.N = data, scales, int(K), int(N)
+
+    @property
+    def nbytes(self) -> int:
+        return self.data.numel() + 4 * self.scales.numel()
+
+
+def quantize(B: torch.Tensor) -> NF4Weight:
+    """Quantise a dense fp32 weight B [K, N] (row-major, on the GPU) to NF4."""
+    _require_cuda_contig("B", B)
+    if B.dtype != torch.float32 or B.dim() != 2:
+        raise ValueError("B must be a 2-D float32 tensor [K, N]")
+    K, N = B.shape
+    data = torch.empty((N, K // 2), dtype=torch.uint8, device=B.device)
+    scales = torch.empty((N, max(K // 64, 1)), dtype=torch.float32, device=B.device)
+    _check(lib().nf4_quantize(_ptr(B), K, N, _ptr(data), _ptr(scales), _stream()), "nf4_quantize")
+    return NF4Weight(data, scales, K, N)
+
+
+def dequantize_f16(w: NF4Weight) -> torch.Tensor:
+    """deq(B)^T as float16 [N, K] (the GEMM's B^T operand values)."""
+    bt = torch.empty((w.N, w.K), dtype=torch.float16, device=w.data.device)
+    _check(lib().nf4_dequantize_f16(_ptr(w.scales), _ptr(w.data), w.K, w.N, _ptr(bt), _stream()),
+           "nf4_dequantize_f16")
+    return bt
+
+
+def backward_a(grad_out: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = None):
+    """grad_A [M, K] fp32 = grad_out [M, N] (fp32 or bf16) @ deq(B)^T."""
+    _require_cuda_contig("grad_out", grad_out)
+    M, N = grad_out.shape
+    if N != w.N:
+        raise ValueError(f"grad_out has N={N}, weight has N={w.N}")
+    if out is None:
+        out = torch.empty((M, w.K), dtype=torch.float32, device=grad_out.device)
+    _require_cuda_contig("out", out)
+    if out.dtype != torch.float32 or tuple(out.shape) != (M, w.K):
+        raise ValueError("out must be float32 [M, K]")
+    _check(lib().nf4_backward_a_ex(_ptr(grad_out), _dtype_code(grad_out), _ptr(w.scales),
+                                   _ptr(w.data), _ptr(out), M, N, w.K, _stream()),
+           "nf4_backward_a_ex")
+    return out
+
+
+def batched_workspace(count: int, device=None) -> torch.Tensor:
+    n = int(lib().nf4_backward_a_batched_workspace(count))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def backward_a_batched(items, workspace: torch.Tensor | None = None):
+    """Grouped launch.  ``items``: sequence of (grad_out, NF4Weight, out-or-None).
+    Returns the list of outputs."""
+    items = list(items)
+    arr = (Nf4Problem * max(len(items), 1))()
+    outs = []
+    for i, (go, w, out) in enumerate(items):
+        _require_cuda_contig("grad_out", go)
+        M, N = go.shape
+        if out is None:
+            out = torch.empty((M, w.K), dtype=torch.float32, device=go.device)
+        _require_cuda_contig("out", out)
+        outs.append(out)
+        arr[i] = Nf4Problem(go.data_ptr(), _dtype_code(go), w.scales.data_ptr(), w.data.data_ptr(),
+                            out.data_ptr(), M, N, w.K)
+    if workspace is None:
+        workspace = batched_workspace(len(items), items[0][0].device if items else None)
+    _check(lib().nf4_backward_a_batched(arr, len(items), _ptr(workspace), workspace.numel(),
+                                        _stream()), "nf4_backward_a_batched")
+    return outs
+
+
+def check_error() -> None:
+    """Synchronise the current stream and raise if a kernel's bounded wait gave up."""
+    _check(lib().nf4_check_error(_stream()), "nf4_check_error")

@@ -1,0 +1,594 @@
+// nf4_gemm.cu -- the NF4-dequant-fused backward-A GEMM on tcgen05 tensor cores.
+//
+//     grad_A[M x K] = grad_out[M x N] @ dequant(B_nf4[K x N])^T
+//
+// (page "aprender-gpu 0.32.0 -- src/kernels/backward/nf4_tensor_core.rs",
+// struct doc comment and build_ptx phases 1-4.)  That page's kernel gives one
+// warp a 16x16 output tile and runs WMMA 16x16x16 over N; here the same
+// arithmetic runs as a persistent, warp-specialised sm_103a kernel:
+//
+//   tile        128 tokens (MMA M) x 256 output columns k (MMA N); the shared
+//               dimension N is consumed 64 at a time (4 MMAs of K=16 each)
+//   warp 4      TMA producer: grad_out tile (fp32 as two 32-column boxes, or one
+//               bf16 box) and the NF4 byte tile (64 rows n x 128 bytes = 256 k),
+//               both 128-byte swizzled, into a 3-stage raw ring
+//   warps 6-13  converters: grad_out -> f16 into the K-major A operand; NF4 codes
+//               x block scale -> f16 into the MN-major B^T operand (one 64-k NF4
+//               block is exactly one 128-byte swizzle row); 2-stage operand ring
+//   warp 5      allocates 512 TMEM columns; one thread issues tcgen05.mma into a
+//               double-buffered fp32 accumulator (2 x 256 columns)
+//   warps 0-3   epilogue: tcgen05.ld of their 32-lane quarter, masked fp32
+//               stores of grad_A (rows >= M and columns >= K are not written),
+//               overlapping the next tile's main loop
+//
+// Out-of-range operands contribute 0 (page above, "PHASE 1"/"PHASE 2": zero the
+// out-of-bounds elements): TMA fills rows >= M and columns >= N of grad_out with
+// zeros, and the scale of every column n >= N is taken as 0.
+//
+// The same kernel serves one problem (descriptor passed as a kernel parameter)
+// and a grouped launch over many projections (descriptors in a caller-owned
+// device workspace, tiles of all problems flattened into one list).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "nf4_common.h"
+#include "nf4_dequant.cuh"
+#include "ptx.cuh"
+
+namespace nf4 {
+
+// ------------------------------------------------------------------ geometry
+constexpr int BM = 128;  // tokens per tile (MMA M)
+constexpr int BK = 256;  // output columns k per tile (MMA N)
+constexpr int BN = 64;   // shared-dimension slice per stage (4 x MMA K=16)
+
+constexpr int kEpiWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kConvWarp0 = 6;
+constexpr int kConvWarps = 8;
+constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;  // 448
+
+constexpr int kRawStages = 3;
+constexpr int kOpStages = 2;
+constexpr int kGoBoxBytes = BM * 128;                  // one 128-byte-wide box of 128 rows
+constexpr int kGoBytes = 2 * kGoBoxBytes;              // fp32: 64 columns = two boxes
+constexpr int kNf4Bytes = BN * (BK / 2);               // 64 rows n x 128 bytes
+constexpr int kRawBytes = kGoBytes + kNf4Bytes;        // 40 KB
+constexpr int kABytes = BM * BN * 2;                   // 16 KB f16
+constexpr int kBBytes = BK * BN * 2;                   // 32 KB f16
+constexpr int kOpBytes = kABytes + kBBytes;            // 48 KB
+constexpr int kRawOff = 0;
+constexpr int kOpOff = kRawOff + kRawStages * kRawBytes;
+constexpr int kBarOff = kOpOff + kOpStages * kOpBytes;
+constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 + 2 + 1;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kTmemCols = 2 * BK;
+
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
+
+// B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
+// 8 rows n per 1024-byte atom; atoms along k are kBLbo apart, atoms along n 1 KB.
+constexpr uint32_t kBLbo = BN * 128;  // 8 KB: all 8 n-groups of one 64-k chunk
+constexpr uint32_t kSbo = 1024;
+
+// ------------------------------------------------------------------ problems
+struct ProblemDesc {
+  CUtensorMap tm_go;   // grad_out [M][N], box 128 rows x 128 bytes, 128B swizzle
+  CUtensorMap tm_nf4;  // codes [N][K/2] bytes, box 64 rows x 128 bytes, 128B swizzle
+  const float* scales;
+  float* grad_A;
+  int M, N, K, dtype;
+  int tiles_m, tiles_k, n_stages, tile_begin;
+};
+
+struct Tile {
+  const ProblemDesc* p;
+  int mt, kt, ns;
+};
+
+__device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int t) {
+  int lo = 0, hi = count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (descs[mid].tile_begin <= t) lo = mid; else hi = mid - 1;
+  }
+  Tile r;
+  r.p = descs + lo;
+  const int local = t - r.p->tile_begin;
+  r.mt = local % r.p->tiles_m;
+  r.kt = local / r.p->tiles_m;
+  r.ns = r.p->n_stages;
+  return r;
+}
+
+// Scale of (column n, K-block kt*4 + j); 0 outside the weight, so padded
+// columns dequantise to zero.
+__device__ __forceinline__ float load_scale(const ProblemDesc* p, int kt, int s, int j, int nl) {
+  const int n = s * BN + nl;
+  const int KB = p->K >> 6;
+  const int b = kt * 4 + j;
+  if (n >= p->N || b >= KB) return 0.0f;
+  return __ldg(p->scales + static_cast<int64_t>(n) * KB + b);
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_a_kernel(const __grid_constant__ ProblemDesc single, const ProblemDesc* __restrict__ batch,
+                 int count, int total_tiles) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_addr(smem);
+  const ProblemDesc* descs = batch != nullptr ? batch : &single;
+
+  const uint32_t bar0 = sbase + kBarOff;
+  auto full_raw = [&](uint32_t i) { return bar0 + 8u * i; };
+  auto empty_raw = [&](uint32_t i) { return bar0 + 8u * (kRawStages + i); };
+  auto full_op = [&](uint32_t i) { return bar0 + 8u * (2 * kRawStages + i); };
+  auto empty_op = [&](uint32_t i) { return bar0 + 8u * (2 * kRawStages + kOpStages + i); };
+  auto tmem_full = [&](uint32_t i) { return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + i); };
+  auto tmem_empty = [&](uint32_t i) {
+    return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 2 + i);
+  };
+  const uint32_t mma_done = bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(full_raw(i), 1);
+      mbar_init(empty_raw(i), kConvWarps);
+    }
+    for (int i = 0; i < kOpStages; ++i) {
+      mbar_init(full_op(i), kConvWarps);
+      mbar_init(empty_op(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tmem_full(i), 1);
+      mbar_init(tmem_empty(i), kEpiWarps);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      if (count == 1) {
+        tma_prefetch_desc(&descs[0].tm_go);
+        tma_prefetch_desc(&descs[0].tm_nf4);
+      }
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        const Tile tl = tile_at(descs, count, t);
+        const bool f32 = tl.p->dtype == NF4_F32;
+        const uint32_t bytes = (f32 ? kGoBytes : kGoBoxBytes) + kNf4Bytes;
+        for (int s = 0; s < tl.ns; ++s, ++it) {
+          const uint32_t slot = it % kRawStages;
+          const uint32_t ph = (it / kRawStages) & 1u;
+          if (!mbar_wait(empty_raw(slot), ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_raw(slot);
+          mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t dst = sbase + kRawOff + slot * kRawBytes;
+          tma_load_2d(dst, &tl.p->tm_go, s * BN, tl.mt * BM, fb);
+          if (f32) tma_load_2d(dst + kGoBoxBytes, &tl.p->tm_go, s * BN + 32, tl.mt * BM, fb);
+          tma_load_2d(dst + kGoBytes, &tl.p->tm_nf4, tl.kt * (BK / 2), s * BN, fb);
+        }
+      }
+      // Every issued copy must land before the CTA may exit.
+      for (uint32_t i = (it > kRawStages ? it - kRawStages : 0u); i < it; ++i)
+        mbar_wait(full_raw(i % kRawStages), (i / kRawStages) & 1u, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BM, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
+      uint32_t it = 0, lt = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++lt) {
+        const Tile tl = tile_at(descs, count, t);
+        const uint32_t acc = lt & 1u;
+        if (!mbar_wait(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BK;
+        for (int s = 0; s < tl.ns; ++s, ++it) {
+          const uint32_t slot = it % kOpStages;
+          if (!mbar_wait(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + kOpOff + slot * kOpBytes;
+          const uint64_t a_desc = smem_desc_sw128(a_addr, 16, kSbo);
+          const uint64_t b_desc = smem_desc_sw128(a_addr + kABytes, kBLbo, kSbo);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
+            tc_mma_f16(d_tmem, a_desc + 2u * kk, b_desc + (2u * kSbo >> 4) * kk, idesc,
+                       (s | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_op(slot));
+        }
+        if (!ok) break;
+        tc_commit(tmem_full(acc));
+      }
+      // No MMA may still be writing TMEM when it is released.
+      tc_commit(mma_done);
+      mbar_wait(mma_done, 0, nullptr);
+    }
+    __syncwarp();
+  } else if (warp >= kConvWarp0) {
+    // ---------------------------------------------------------------- converters
+    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..255
+    const int ar = ct & (BM - 1);                   // A: row of the tile
+    const int ahalf = ct >> 7;                      // A: 16-byte chunks 4*ahalf .. +3
+    const int bj = ct >> 6;                         // B: 64-k chunk (NF4 block) 0..3
+    const int bn = ct & 63;                         // B: row n of the stage
+    const uint32_t aswz = static_cast<uint32_t>(ar & 7);
+    const uint32_t bswz = static_cast<uint32_t>(bn & 7);
+
+    int t = blockIdx.x;
+    float scale_next = 0.0f;
+    if (t < total_tiles) {
+      const Tile tl = tile_at(descs, count, t);
+      scale_next = load_scale(tl.p, tl.kt, 0, bj, bn);
+    }
+    uint32_t it = 0;
+    bool ok = true;
+    for (; ok && t < total_tiles; t += gridDim.x) {
+      const Tile tl = tile_at(descs, count, t);
+      const bool f32 = tl.p->dtype == NF4_F32;
+      for (int s = 0; s < tl.ns; ++s, ++it) {
+        const float scale = scale_next;
+        if (s + 1 < tl.ns) {
+          scale_next = load_scale(tl.p, tl.kt, s + 1, bj, bn);
+        } else if (t + static_cast<int>(gridDim.x) < total_tiles) {
+          const Tile nx = tile_at(descs, count, t + gridDim.x);
+          scale_next = load_scale(nx.p, nx.kt, 0, bj, bn);
+        }
+        const uint32_t rslot = it % kRawStages;
+        const uint32_t oslot = it % kOpStages;
+        // All lanes wait; the warp goes on only if every lane saw the phase
+        // complete, so a timeout never leaves the warp divergent.
+        const bool got = mbar_wait(full_raw(rslot), (it / kRawStages) & 1u, abort_flag) &&
+                         mbar_wait(empty_op(oslot), ((it / kOpStages) & 1u) ^ 1u, abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t raw = sbase + kRawOff + rslot * kRawBytes;
+        const uint32_t a_op = sbase + kOpOff + oslot * kOpBytes;
+        const uint32_t b_op = a_op + kABytes;
+
+        // grad_out -> f16 A operand (K-major, 128B swizzle: chunk c of row r at c ^ (r % 8)).
+        const uint32_t a_row = a_op + ar * 128;
+        if (f32) {
+          const uint32_t src = raw + ahalf * kGoBoxBytes + ar * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 x0 = lds128(src + (((2u * i) ^ aswz) << 4));
+            const uint4 x1 = lds128(src + (((2u * i + 1u) ^ aswz) << 4));
+            uint4 h;
+            h.x = pack_f16x2(__uint_as_float(x0.x), __uint_as_float(x0.y));
+            h.y = pack_f16x2(__uint_as_float(x0.z), __uint_as_float(x0.w));
+            h.z = pack_f16x2(__uint_as_float(x1.x), __uint_as_float(x1.y));
+            h.w = pack_f16x2(__uint_as_float(x1.z), __uint_as_float(x1.w));
+            sts128(a_row + (((4u * ahalf + i) ^ aswz) << 4), h);
+          }
+        } else {
+          const uint32_t src = raw + ar * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t c = (4u * ahalf + i) ^ aswz;
+            const uint4 w = lds128(src + (c << 4));
+            uint4 h;
+            h.x = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+            h.y = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+            h.z = pack_f16x2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+            h.w = pack_f16x2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+            sts128(a_row + (c << 4), h);
+          }
+        }
+
+        // NF4 block (row n = bn, k = 64*bj .. +63) -> one 128-byte swizzle row of B^T.
+        {
+          const uint32_t src = raw + kGoBytes + bn * 128;
+          const uint4 q0 = lds128(src + (((2u * bj) ^ bswz) << 4));
+          const uint4 q1 = lds128(src + (((2u * bj + 1u) ^ bswz) << 4));
+          const BlockTable tb = make_block_table(scale);
+          const uint32_t dst = b_op + bj * kBLbo + (bn >> 3) * kSbo + bswz * 128;
+          const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sts128(dst + ((static_cast<uint32_t>(e) ^ bswz) << 4),
+                                             dequant_word(words[e], tb));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(full_op(oslot));
+          mbar_arrive(empty_raw(rslot));
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    uint32_t lt = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++lt) {
+      const Tile tl = tile_at(descs, count, t);
+      const uint32_t acc = lt & 1u;
+      const bool got = mbar_wait(tmem_full(acc), (lt >> 1) & 1u, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
+      tc_fence_after();
+      const int row = tl.mt * BM + warp * 32 + lane;
+      const bool row_ok = row < tl.p->M;
+      float* out_row = tl.p->grad_A + static_cast<int64_t>(row_ok ? row : 0) * tl.p->K;
+      const uint32_t taddr = tmem_base + acc * BK + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BK / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_wait_ld();
+        const int col = tl.kt * BK + c * 32;
+        if (row_ok && col < tl.p->K) {
+          float4* dst = reinterpret_cast<float4*>(out_row + col);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty(acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+static bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base,
+                      uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                      uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Argument rules shared by the single and grouped entry points.
+static int check_problem(const void* go, int dtype, const float* scales, const uint8_t* data,
+                         const float* grad_A, int M, int N, int K) {
+  if (dtype != NF4_F32 && dtype != NF4_BF16) return NF4_ERR_INVALID;
+  if (M < 0 || N < 0 || K <= 0 || K % 64 != 0) return NF4_ERR_INVALID;
+  if (M == 0) return NF4_OK;
+  if (grad_A == nullptr) return NF4_ERR_INVALID;
+  if (!aligned(grad_A, 16)) return NF4_ERR_ALIGN;
+  if (N == 0) return NF4_OK;
+  if (go == nullptr || scales == nullptr || data == nullptr) return NF4_ERR_INVALID;
+  if (N % (dtype == NF4_F32 ? 4 : 8) != 0) return NF4_ERR_INVALID;
+  if (!aligned(go, 16) || !aligned(data, 16) || !aligned(scales, 4)) return NF4_ERR_ALIGN;
+  return NF4_OK;
+}
+
+static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* scales,
+                     const uint8_t* data, float* grad_A, int M, int N, int K) {
+  std::memset(d, 0, sizeof(*d));
+  const bool f32 = dtype == NF4_F32;
+  if (!encode_2d(&d->tm_go, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 go, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(N) * (f32 ? 4 : 2), f32 ? 32 : 64, BM))
+    return NF4_ERR_CUDA;
+  if (!encode_2d(&d->tm_nf4, CU_TENSOR_MAP_DATA_TYPE_UINT8, data, static_cast<uint64_t>(K / 2),
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), BK / 2, BN))
+    return NF4_ERR_CUDA;
+  d->scales = scales;
+  d->grad_A = grad_A;
+  d->M = M;
+  d->N = N;
+  d->K = K;
+  d->dtype = dtype;
+  d->tiles_m = (M + BM - 1) / BM;
+  d->tiles_k = (K + BK - 1) / BK;
+  d->n_stages = (N + BN - 1) / BN;
+  d->tile_begin = 0;
+  return NF4_OK;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool attr_set = false;
+};
+
+static int device_info(DeviceInfo** out) {
+  static DeviceInfo infos[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NF4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& di = infos[dev];
+  if (!di.attr_set) {
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NF4_ERR_CUDA;
+    if (cudaFuncSetAttribute(bwd_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return NF4_ERR_CUDA;
+    di.attr_set = true;
+  }
+  *out = &di;
+  return NF4_OK;
+}
+
+static int launch(const ProblemDesc& single, const ProblemDesc* batch, int count, int total_tiles,
+                  cudaStream_t stream) {
+  DeviceInfo* di = nullptr;
+  const int rc = device_info(&di);
+  if (rc != NF4_OK) return rc;
+  const int grid = std::min(total_tiles, di->sms);
+  bwd_a_kernel<<<grid, kThreads, kSmemBytes, stream>>>(single, batch, count, total_tiles);
+  return launch_status();
+}
+
+}  // namespace nf4
+
+using namespace nf4;
+
+extern "C" int nf4_abi_version(void) { return 1; }
+
+extern "C" const char* nf4_status_string(int status) {
+  switch (status) {
+    case NF4_OK: return "ok";
+    case NF4_ERR_INVALID: return "invalid argument";
+    case NF4_ERR_ALIGN: return "misaligned pointer";
+    case NF4_ERR_CUDA: return "CUDA error";
+    case NF4_ERR_TIMEOUT: return "kernel wait timed out";
+    case NF4_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float* scales,
+                                 const uint8_t* data, float* grad_A, int M, int N, int K,
+                                 void* stream) {
+  int rc = check_problem(grad_out, go_dtype, scales, data, grad_A, M, N, K);
+  if (rc != NF4_OK || M == 0) return rc;
+  if (N == 0) {
+    return cudaMemsetAsync(grad_A, 0, sizeof(float) * static_cast<size_t>(M) * K,
+                           as_stream(stream)) == cudaSuccess
+               ? NF4_OK
+               : NF4_ERR_CUDA;
+  }
+  ProblemDesc d;
+  rc = fill_desc(&d, grad_out, go_dtype, scales, data, grad_A, M, N, K);
+  if (rc != NF4_OK) return rc;
+  const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
+  if (tiles > INT_MAX) return NF4_ERR_INVALID;
+  return launch(d, nullptr, 1, static_cast<int>(tiles), as_stream(stream));
+}
+
+extern "C" int nf4_backward_a(const float* grad_out, const float* scales, const uint8_t* data,
+                              float* grad_A, int M, int N, int K, void* stream) {
+  return nf4_backward_a_ex(grad_out, NF4_F32, scales, data, grad_A, M, N, K, stream);
+}
+
+extern "C" size_t nf4_backward_a_batched_workspace(int count) {
+  if (count <= 0) return 0;
+  return sizeof(ProblemDesc) * static_cast<size_t>(count);
+}
+
+extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (count < 0 || (count > 0 && problems == nullptr)) return NF4_ERR_INVALID;
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    const int rc = check_problem(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
+    if (rc != NF4_OK) return rc;
+  }
+  cudaStream_t st = as_stream(stream);
+  std::vector<ProblemDesc> descs;
+  descs.reserve(count);
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    if (p.M == 0) continue;
+    if (p.N == 0) {
+      if (cudaMemsetAsync(p.grad_A, 0, sizeof(float) * static_cast<size_t>(p.M) * p.K, st) !=
+          cudaSuccess)
+        return NF4_ERR_CUDA;
+      continue;
+    }
+    descs.emplace_back();
+    const int rc = fill_desc(&descs.back(), p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A,
+                             p.M, p.N, p.K);
+    if (rc != NF4_OK) return rc;
+  }
+  if (descs.empty()) return NF4_OK;
+  if (workspace == nullptr || !aligned(workspace, 256) ||
+      workspace_bytes < sizeof(ProblemDesc) * descs.size())
+    return NF4_ERR_WORKSPACE;
+  // Longest tiles first, so that the static round-robin over the flattened
+  // tile list ends with the short ones.
+  std::stable_sort(descs.begin(), descs.end(), [](const ProblemDesc& a, const ProblemDesc& b) {
+    return a.n_stages > b.n_stages;
+  });
+  int64_t total = 0;
+  for (ProblemDesc& d : descs) {
+    d.tile_begin = static_cast<int>(total);
+    total += static_cast<int64_t>(d.tiles_m) * d.tiles_k;
+    if (total > INT_MAX) return NF4_ERR_INVALID;
+  }
+  if (cudaMemcpyAsync(workspace, descs.data(), sizeof(ProblemDesc) * descs.size(),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return NF4_ERR_CUDA;
+  ProblemDesc unused;
+  std::memset(&unused, 0, sizeof(unused));
+  return launch(unused, static_cast<const ProblemDesc*>(workspace), static_cast<int>(descs.size()),
+                static_cast<int>(total), st);
+}
+
+extern "C" int nf4_check_error(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return NF4_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return NF4_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+    return NF4_ERR_TIMEOUT;
+  }
+  return cudaGetLastError() == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+}

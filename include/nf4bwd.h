@@ -1,0 +1,143 @@
+/*
+ * nf4bwd.h -- C ABI of libnf4bwd.so, the NF4-dequant-fused backward-A GEMM
+ * for GB300 (sm_103a).
+ *
+ * The operation (page "aprender-gpu 0.32.0 -- src/kernels/backward/
+ * nf4_tensor_core.rs", struct doc comment of Nf4TensorCoreGemmBackwardAKernel):
+ *
+ *     grad_A[M x K] = grad_out[M x N] @ dequant(B_nf4[K x N])^T
+ *
+ * N is the shared (contraction) dimension, K the output dimension; B_nf4 is the
+ * frozen 4-bit NormalFloat weight of a linear layer with K inputs and N outputs.
+ *
+ * Conventions for every entry point below
+ *   - All array pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates nothing, keeps no reference after the call returns and never
+ *     frees caller memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued asynchronously on it; the call returns before the GPU
+ *     finishes.  Inputs must stay valid until the stream reaches the work.
+ *   - The return value is an nf4_status.  Argument errors are detected on the
+ *     host before anything is enqueued, and then nothing is written.
+ *   - Kernel faults are not detected by the call itself; a bounded wait inside
+ *     a kernel that gives up (no progress for 1 s) sets a device status word
+ *     that nf4_check_error() reports as NF4_ERR_TIMEOUT.
+ *
+ * Data layout (page above, build_ptx "PHASE 2: Dequant B_nf4"):
+ *   scales   fp32 [N][K/64]   absmax of the 64-element K-block b of column n
+ *   data     u8   [N][K/2]    codes of column n, K contiguous: element (k, n)
+ *                             is nibble (k % 2) of byte n*(K/2) + k/2, low
+ *                             nibble = even k
+ *   grad_out [M][N] row-major, fp32 or bf16
+ *   grad_A   fp32 [M][K] row-major, overwritten (not accumulated into)
+ *
+ * Arithmetic (same page, build_ptx phases 1-3): every dequantised weight is
+ * f16_rn(f32(scale * codebook[code])); grad_out is rounded to f16 (bf16 input:
+ * widened exactly to f32 first); products of the f16 operands are summed in
+ * fp32 by the tensor cores (tcgen05, accumulator in tensor memory).
+ */
+#ifndef NF4BWD_H
+#define NF4BWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nf4_status {
+  NF4_OK = 0,
+  NF4_ERR_INVALID = 1, /* null pointer, negative size, K % 64 != 0, N not a multiple of
+                          the row alignment (4 for fp32 grad_out, 8 for bf16), ... */
+  NF4_ERR_ALIGN = 2,   /* a pointer is not 16-byte aligned (scales: 4-byte) */
+  NF4_ERR_CUDA = 3,    /* a CUDA runtime call or a kernel launch failed */
+  NF4_ERR_TIMEOUT = 4, /* a kernel's bounded wait gave up (reported by nf4_check_error) */
+  NF4_ERR_WORKSPACE = 5 /* workspace missing, misaligned or too small */
+} nf4_status;
+
+typedef enum nf4_dtype { NF4_F32 = 0, NF4_BF16 = 1 } nf4_dtype;
+
+/* Version of this ABI (incremented on any incompatible change). */
+int nf4_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nf4_status_string(int status);
+
+/*
+ * Quantise a dense fp32 weight B [K][N] (row-major) to NF4: for every column n
+ * and 64-element K-block b, scales[n][b] = max |B[k][n]| over the block, and
+ * each element gets the code of the nearest codebook entry to B/scale (f32
+ * differences, ties to the lower code; an all-zero block gets scale 0 and code
+ * 7).  The pages fix the packed layout (page above, build_ptx "PHASE 2") but
+ * not the quantiser; this is blockwise absmax NormalFloat4 quantisation as in
+ * Dettmers et al., "QLoRA" (2023).
+ *   B       [K*N] fp32, 16-byte aligned not required (4-byte)
+ *   data    [N*K/2] bytes, 16-byte aligned; scales [N*K/64] fp32, 4-byte aligned
+ *   K       positive multiple of 64; N positive
+ */
+int nf4_quantize(const float* B, int K, int N, uint8_t* data, float* scales, void* stream);
+
+/*
+ * Dequantise to f16, transposed: bt[n*K + k] = f16 bits of
+ * f16_rn(f32(scales[n][k/64] * codebook[code(k, n)])) (page above, build_ptx
+ * "PHASE 2").  Runs the same device routine that the GEMM's producer warps use
+ * to build the B^T operand, so it exposes their values for bit-exact checks.
+ *   bt      [N*K] uint16 (f16 bits), 16-byte aligned
+ */
+int nf4_dequantize_f16(const float* scales, const uint8_t* data, int K, int N, uint16_t* bt,
+                       void* stream);
+
+/*
+ * grad_A = grad_out @ dequant(B_nf4)^T with fp32 grad_out (page above, the
+ * kernel's parameter list: grad_out_ptr, scales_ptr, data_ptr, grad_a_ptr, m, n,
+ * k).  M == 0 enqueues nothing; N == 0 writes zeros into grad_A.
+ *   grad_out [M*N] fp32, 16-byte aligned, N % 4 == 0
+ *   data     16-byte aligned; scales 4-byte aligned; grad_A [M*K] fp32, 16-byte aligned
+ *   K        positive multiple of 64
+ */
+int nf4_backward_a(const float* grad_out, const float* scales, const uint8_t* data,
+                   float* grad_A, int M, int N, int K, void* stream);
+
+/* As nf4_backward_a, with grad_out of type go_dtype (NF4_F32 or NF4_BF16;
+ * bf16 needs N % 8 == 0). */
+int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float* scales,
+                      const uint8_t* data, float* grad_A, int M, int N, int K, void* stream);
+
+/* One projection of a grouped launch. */
+typedef struct nf4_problem {
+  const void* grad_out; /* [M][N], type go_dtype */
+  int go_dtype;         /* NF4_F32 or NF4_BF16 */
+  const float* scales;  /* [N][K/64] */
+  const uint8_t* data;  /* [N][K/2] */
+  float* grad_A;        /* [M][K], overwritten */
+  int M, N, K;
+} nf4_problem;
+
+/* Bytes of device workspace nf4_backward_a_batched needs for `count` problems. */
+size_t nf4_backward_a_batched_workspace(int count);
+
+/*
+ * Grouped backward-A over `count` independent projections in one persistent
+ * launch (the page's doc comment counts 28 layers x 7 projections = 196
+ * backward projections per training step).  Every problem follows the rules of
+ * nf4_backward_a_ex.  `problems` is a HOST array, read before the call returns.
+ * `workspace` is caller-owned device memory of at least
+ * nf4_backward_a_batched_workspace(count) bytes, 256-byte aligned; the call
+ * writes per-problem descriptors into it with an asynchronous copy on `stream`,
+ * so it must not be reused by another call until this one has run.
+ */
+int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, then report and clear the library's device status word
+ * (NF4_ERR_TIMEOUT if any kernel's bounded wait gave up since the last check),
+ * or NF4_ERR_CUDA if the stream reports a CUDA error.
+ */
+int nf4_check_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NF4BWD_H */

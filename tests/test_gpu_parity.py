@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Ordered from the most diagnostic to the broadest: codes and dequantised
+operands bit for bit, GEMMs whose exact answer isolates one operand's layout
+(one-hot grad_out rows, an identity weight), then seeded problems that span
+several tiles with ragged tails, the grouped launch, and the full-size
+workloads on sampled rows.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import assert_close, run_problem, sample_rows, to_device_go
+from workloads import BF16, CONFIGS, F32, Problem, make_grad_out, make_weight
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from backward_gemm_gb300.build import build
+
+    build()
+    import backward_gemm_gb300 as nb
+
+    nb.lib()
+    yield
+
+
+def nb():
+    import backward_gemm_gb300
+
+    return backward_gemm_gb300
+
+
+# ---------------------------------------------------------------- quantise / dequantise
+@pytest.mark.parametrize("K,N,outliers,std", [(128, 64, False, 0.02), (1536, 256, True, 0.02),
+                                             (640, 72, False, 1.0), (64, 4, True, 0.015)])
+def test_quantize_codes_bit_exact(K, N, outliers, std):
+    B = make_weight(Problem(1, N, K, F32, 1.0, std, outliers, seed=K + N))
+    B[:64, :2] = 0.0  # all-zero blocks
+    w = nb().quantize(torch.from_numpy(B).cuda())
+    data_o, scales_o = oracle.quantize(B)
+    np.testing.assert_array_equal(w.scales.cpu().numpy(), scales_o)
+    np.testing.assert_array_equal(w.data.cpu().numpy(), data_o)
+
+
+@pytest.mark.parametrize("K,N", [(128, 64), (1536, 256), (640, 72)])
+def test_dequantize_bit_exact(K, N):
+    B = make_weight(Problem(1, N, K, F32, 1.0, 0.02, True, seed=3 * K + N))
+    data_o, scales_o = oracle.quantize(B)
+    w = nb().NF4Weight(torch.from_numpy(data_o).cuda(), torch.from_numpy(scales_o).cuda(), K, N)
+    bt = nb().dequantize_f16(w).cpu().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(bt, oracle.dequantize_f16(scales_o, data_o, K, N))
+
+
+# ---------------------------------------------------------------- exact-answer GEMMs
+def _weight_from_oracle(B):
+    data_o, scales_o = oracle.quantize(B)
+    w = nb().NF4Weight(torch.from_numpy(data_o).cuda(), torch.from_numpy(scales_o).cuda(),
+                       B.shape[0], B.shape[1])
+    return w, data_o, scales_o
+
+
+def test_one_hot_rows_give_dequantised_columns_exactly():
+    """go[m, :] = e_n  =>  grad_A[m, :] = deq(B)[:, n] exactly (one product by 1.0)."""
+    K, N = 640, 192
+    B = make_weight(Problem(1, N, K, F32, 1.0, 0.02, True, seed=5))
+    w, data_o, scales_o = _weight_from_oracle(B)
+    ns = [0, 1, 7, 8, 15, 16, 63, 64, 65, 127, 128, 191]
+    M = 2 * len(ns) + 130  # rows in two M tiles, the rest zero
+    go = np.zeros((M, N), dtype=np.float32)
+    for i, n in enumerate(ns):
+        go[i, n] = 1.0
+        go[129 + i, n] = 1.0
+    ga = nb().backward_a(torch.from_numpy(go).cuda(), w).cpu().numpy()
+    bt = oracle.dequantize_f16(scales_o, data_o, K, N).view(np.float16).astype(np.float32)
+    for i, n in enumerate(ns):
+        np.testing.assert_array_equal(ga[i], bt[n], err_msg=f"row {i} n={n}")
+        np.testing.assert_array_equal(ga[129 + i], bt[n], err_msg=f"row {129 + i} n={n}")
+    assert np.all(ga[len(ns):129] == 0) and np.all(ga[129 + len(ns):] == 0)
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_identity_weight_returns_rounded_grad_out(dtype):
+    """B = I (K = N): deq(B) is exactly I, so grad_A = f16(grad_out) exactly."""
+    K = N = 320
+    B = np.eye(K, N, dtype=np.float32)
+    w, _, _ = _weight_from_oracle(B)
+    p = Problem(200, N, K, dtype, 1.0, seed=9)
+    go = make_grad_out(p)
+    ga = nb().backward_a(to_device_go(go, dtype), w).cpu().numpy()
+    want = oracle.round_operand(go, dtype).view(np.float16).astype(np.float32)
+    np.testing.assert_array_equal(ga, want)
+
+
+# ---------------------------------------------------------------- seeded problems
+SMALL = [
+    Problem(32, 64, 128, F32, 1.0, 0.02, False, 0, "tiny"),
+    Problem(300, 192, 640, F32, 1.0, 0.02, True, 1, "ragged-3x3"),
+    Problem(129, 72, 64, F32, 1e-2, 0.02, False, 2, "n-tail"),
+    Problem(257, 136, 384, BF16, 1e-2, 0.02, True, 3, "bf16-ragged"),
+    Problem(17, 4, 256, F32, 1.0, 0.02, False, 4, "n4"),
+    Problem(5, 8, 192, BF16, 1.0, 0.02, False, 5, "n8-bf16"),
+    Problem(2048, 128, 4096, F32, 1.0, 0.015, False, 6, "persistent-256-tiles"),
+]
+
+
+@pytest.mark.parametrize("p", SMALL, ids=lambda p: p.name)
+def test_small_problems_full_check(p):
+    run_problem(p)
+
+
+def test_deterministic():
+    p = Problem(300, 192, 640, F32, 1.0, 0.02, True, 11)
+    go = to_device_go(make_grad_out(p), F32)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    a = nb().backward_a(go, w)
+    b = nb().backward_a(go, w)
+    assert torch.equal(a, b)
+
+
+def test_batched_matches_single_and_oracle():
+    probs = [Problem(300, 192, 640, F32, 1.0, 0.02, True, 21),
+             Problem(129, 256, 1536, BF16, 1e-2, 0.02, False, 22),
+             Problem(64, 72, 64, F32, 1e-2, 0.02, False, 23),
+             Problem(1000, 64, 256, F32, 1.0, 0.02, False, 24)]
+    items, gos, ws, Bs = [], [], [], []
+    for p in probs:
+        go = make_grad_out(p)
+        B = make_weight(p)
+        w = nb().quantize(torch.from_numpy(B).cuda())
+        items.append((to_device_go(go, p.go_dtype), w, None))
+        gos.append(go)
+        Bs.append(B)
+        ws.append(w)
+    outs = nb().backward_a_batched(items)
+    nb().check_error()
+    for p, go, B, (go_t, w, _), out in zip(probs, gos, Bs, items, outs):
+        single = nb().backward_a(go_t, w)
+        assert torch.equal(out, single), p
+        data_o, scales_o = oracle.quantize(B)
+        ref, bound = oracle.backward_a(go, p.go_dtype, scales_o, data_o, p.K)
+        assert_close(out.cpu().numpy(), ref, bound, str(p))
+
+
+def test_batched_full_step_shapes_one_layer():
+    """One layer's seven projections at a reduced token count, grouped."""
+    full = CONFIGS["full_step"][:7]
+    probs = [Problem(256, p.N, p.K, p.go_dtype, p.go_std, p.b_std, p.outliers, p.seed, p.name)
+             for p in full]
+    items, refs = [], []
+    for p in probs:
+        go = make_grad_out(p)
+        B = make_weight(p)
+        items.append((to_device_go(go, p.go_dtype), nb().quantize(torch.from_numpy(B).cuda()), None))
+        data_o, scales_o = oracle.quantize(B)
+        go16 = oracle.round_operand(go, p.go_dtype)
+        bt = oracle.dequantize_f16(scales_o, data_o, p.K, p.N)
+        rows = sample_rows(p.M, 6, p.seed)
+        refs.append((rows,) + oracle.backward_a_rows(go16, bt, rows))
+    outs = nb().backward_a_batched(items)
+    nb().check_error()
+    for p, out, (rows, ref, bound) in zip(probs, outs, refs):
+        assert_close(out.cpu().numpy()[rows], ref, bound, p.name)
+
+
+# ---------------------------------------------------------------- edge cases
+def test_empty_and_degenerate():
+    w = nb().quantize(torch.from_numpy(make_weight(Problem(1, 64, 128))).cuda())
+    out = nb().backward_a(torch.zeros((0, 64), device="cuda"), w)
+    assert out.shape == (0, 128)
+    # N == 0: empty sum, grad_A is zero.
+    w0 = nb().NF4Weight(torch.zeros((0, 64), dtype=torch.uint8, device="cuda"),
+                        torch.zeros((0, 2), device="cuda"), 128, 0)
+    out = torch.full((3, 128), 7.0, device="cuda")
+    nb().backward_a(torch.zeros((3, 0), device="cuda"), w0, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+    # grad_out all zero gives zeros.
+    out = nb().backward_a(torch.zeros((40, 64), device="cuda"), w)
+    assert torch.all(out == 0)
+
+
+def test_rejects_bad_arguments_without_launching():
+    L = nb().lib()
+    go = torch.zeros((16, 64), device="cuda")
+    w = nb().quantize(torch.from_numpy(make_weight(Problem(1, 64, 128))).cuda())
+    out = torch.zeros((16, 128), device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    args = lambda **kw: [kw.get("go", go.data_ptr()), w.scales.data_ptr(), w.data.data_ptr(),
+                         kw.get("out", out.data_ptr()), 16, kw.get("N", 64), kw.get("K", 128), s]
+    assert L.nf4_backward_a(*args(K=100)) == nb().NF4_ERR_INVALID
+    assert L.nf4_backward_a(*args(N=66)) == nb().NF4_ERR_INVALID
+    assert L.nf4_backward_a(*args(go=go.data_ptr() + 4)) == nb().NF4_ERR_ALIGN
+    assert L.nf4_backward_a(*args(out=out.data_ptr() + 8)) == nb().NF4_ERR_ALIGN
+    assert L.nf4_backward_a(*args(go=None)) == nb().NF4_ERR_INVALID
+    nb().check_error()
+
+
+# ---------------------------------------------------------------- full-size workloads
+FULL = [(name, p) for name in ("q_proj", "mlp", "large") for p in CONFIGS[name]]
+
+
+@pytest.mark.parametrize("name,p", FULL, ids=[p.name for _, p in FULL])
+def test_full_size_sampled_rows(name, p):
+    run_problem(p, rows=sample_rows(p.M, 10, p.seed))
