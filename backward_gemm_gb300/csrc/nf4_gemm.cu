@@ -82,7 +82,7 @@ constexpr uint32_t kBLbo = BN * 128;  // 8 KB: all 8 n-groups of one 64-k chunk
 constexpr uint32_t kSbo = 1024;
 
 // ------------------------------------------------------------------ problems
-struct ProblemDesc {
+struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
   CUtensorMap tm_go;   // grad_out [M][N], box 128 rows x 128 bytes, 128B swizzle
   CUtensorMap tm_nf4;  // codes [N][K/2] bytes, box 64 rows x 128 bytes, 128B swizzle
   const float* scales;
@@ -90,6 +90,8 @@ struct ProblemDesc {
   int M, N, K, dtype;
   int tiles_m, tiles_k, n_stages, tile_begin;
 };
+
+static_assert(sizeof(ProblemDesc) % 16 == 0, "descriptor copy granularity");
 
 struct Tile {
   const ProblemDesc* p;
@@ -378,6 +380,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ descriptor upload
+// Descriptors of a grouped launch travel to the workspace as kernel parameters
+// (copied by value at launch, also when the launch is captured in a CUDA graph),
+// kDescsPerUpload at a time.
+constexpr int kDescsPerUpload = 72;
+struct DescChunk {
+  ProblemDesc d[kDescsPerUpload];
+};
+static_assert(sizeof(DescChunk) <= 32000, "kernel parameter limit");
+
+__global__ void upload_descs_kernel(const __grid_constant__ DescChunk chunk, ProblemDesc* dst,
+                                    int n) {
+  const uint4* src = reinterpret_cast<const uint4*>(&chunk);
+  uint4* out = reinterpret_cast<uint4*>(dst);
+  const int words = n * static_cast<int>(sizeof(ProblemDesc) / sizeof(uint4));
+  for (int i = threadIdx.x; i < words; i += blockDim.x) out[i] = src[i];
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -572,9 +592,15 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
     total += static_cast<int64_t>(d.tiles_m) * d.tiles_k;
     if (total > INT_MAX) return NF4_ERR_INVALID;
   }
-  if (cudaMemcpyAsync(workspace, descs.data(), sizeof(ProblemDesc) * descs.size(),
-                      cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return NF4_ERR_CUDA;
+  ProblemDesc* ws = static_cast<ProblemDesc*>(workspace);
+  for (size_t i = 0; i < descs.size(); i += kDescsPerUpload) {
+    const int n = static_cast<int>(std::min<size_t>(kDescsPerUpload, descs.size() - i));
+    DescChunk chunk;
+    std::memset(&chunk, 0, sizeof(chunk));
+    std::memcpy(chunk.d, descs.data() + i, sizeof(ProblemDesc) * n);
+    upload_descs_kernel<<<1, 256, 0, st>>>(chunk, ws + i, n);
+    if (cudaGetLastError() != cudaSuccess) return NF4_ERR_CUDA;
+  }
   ProblemDesc unused;
   std::memset(&unused, 0, sizeof(unused));
   return launch(unused, static_cast<const ProblemDesc*>(workspace), static_cast<int>(descs.size()),

@@ -1,0 +1,432 @@
+"""Benchmark of the NF4-dequant-fused backward-A GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the hot path over one batch of synthetic input: one
+backward-A call on the workload's projection(s) (a grouped launch when the
+workload has several).  The default workload is the single Qwen2.5-1.5B q_proj
+backward (M=2048 tokens, N=K=1536, fp32 grad_out).
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and a device synchronise, timed with CUDA events on the launching stream.
+The K steps replay a CUDA graph of G steps that rotates through enough input
+sets (grad_out, NF4 weight, grad_A) to exceed the 129 MB L2, so no step reads
+another step's inputs from L2.  Under torchrun every rank runs its own copy of
+the workload (M-sharded data parallelism: independent token batches, no
+collective on the data path); the reported time is the maximum over ranks.
+
+The JSON line carries the device throughput (`value`), an end-to-end number
+through the public API with host buffers (`e2e`), the roofline of the GEMM
+kernel against MEASURED_PEAKS.json, the CPU oracle timed on a bounded sample
+(`cpu_baseline`), and SM clocks sampled during the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import BF16, CONFIGS, DTYPE_NAMES, F32, Problem, make_grad_out, make_weight  # noqa
+
+L2_BYTES = 129 * 2**20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workloads() -> dict[str, list[Problem]]:
+    w = {"q_proj": CONFIGS["q_proj"], "tiny": CONFIGS["tiny"],
+         "up_proj": [CONFIGS["mlp"][0]], "down_proj": [CONFIGS["mlp"][1]],
+         "mlp": CONFIGS["mlp"], "full_step": CONFIGS["full_step"]}
+    for p in CONFIGS["large"]:
+        w[p.name] = [p]
+    return w
+
+
+def describe(name: str, probs: list[Problem]) -> str:
+    if len(probs) == 1:
+        p = probs[0]
+        return f"{name}: M={p.M} N={p.N} K={p.K} grad_out {DTYPE_NAMES[p.go_dtype]}"
+    return f"{name}: {len(probs)} projections grouped, M={probs[0].M}"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML (ctypes) every ~2 ms."""
+
+    # clocks_event_reasons bits (nvml.h)
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index: int):
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._ok = False
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if (self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0 and
+                    self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0):
+                self.samples.append((clk.value, rs.value))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self._ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
+        reasons = sorted({name for _, r in busy for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in busy), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(busy)}
+
+
+# ---------------------------------------------------------------- our arm
+def make_input_sets(probs, copies, dev):
+    import backward_gemm_gb300 as nb
+
+    sets = []
+    base_go = [make_grad_out(p) for p in probs]
+    base_B = [make_weight(p) for p in probs]
+    for c in range(copies):
+        items = []
+        for p, go, B in zip(probs, base_go, base_B):
+            if p.go_dtype == F32:
+                go_t = torch.from_numpy(go).to(dev)
+            else:
+                go_t = torch.from_numpy(go.view(np.int16)).to(dev).view(torch.bfloat16)
+            w = nb.quantize(torch.from_numpy(B).to(dev))
+            out = torch.empty((p.M, p.K), dtype=torch.float32, device=dev)
+            items.append((go_t, w, out))
+        ws = nb.batched_workspace(len(items), dev) if len(items) > 1 else None
+        sets.append((items, ws))
+    torch.cuda.synchronize()
+    return sets, base_go
+
+
+def run_step(items, ws):
+    import backward_gemm_gb300 as nb
+
+    if len(items) == 1:
+        go, w, out = items[0]
+        nb.backward_a(go, w, out=out)
+    else:
+        nb.backward_a_batched(items, ws)
+
+
+def bench_ours(args, rank, world, dev):
+    import backward_gemm_gb300 as nb
+    from backward_gemm_gb300.build import build
+
+    if rank == 0:
+        build()
+    if world > 1:
+        torch.distributed.barrier()
+    build()
+    nb.lib()
+
+    probs = workloads()[args.workload]
+    flops = sum(p.flops for p in probs)
+    alg_bytes = sum(p.algorithmic_bytes for p in probs)
+    per_set = sum(p.go_bytes + 4 * p.M * p.K + p.K * p.N // 2 for p in probs)
+    copies = max(2, min(16, -(-2 * L2_BYTES // per_set)))
+    sets, host_go = make_input_sets(probs, copies, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            run_step(*sets[i % copies])
+        nb.check_error()
+        # Graph of `copies` steps, one per input set.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(copies):
+                run_step(*sets[i])
+        graph.replay()
+        stream.synchronize()
+
+        K = args.steps
+        full, rem = divmod(K, copies)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index) as clocks:
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                run_step(*sets[i])
+            ev1.record(stream)
+            ev1.synchronize()
+        torch.cuda.synchronize(dev)
+        ms = ev0.elapsed_time(ev1)
+        nb.check_error()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+
+    ms_per_step = ms / K
+    value = flops * K * world / (ms * 1e-3) / 1e12  # whole-job TFLOP/s
+
+    # End to end through the public API with host buffers: pinned grad_out in,
+    # grad_A out, copies inside the timed region.
+    e2e = None
+    if not args.no_e2e:
+        e2e = bench_e2e(args, probs, host_go, sets[0], stream, dev, flops, world)
+
+    peaks, peak_kind = load_peaks()
+    long_run = ms > 1000.0
+    peak_tf = peaks["bf16_tflops_sustained" if long_run else "bf16_tflops"]
+    t_tensor = flops / (peak_tf * 1e12)
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = flops / (ms_per_step * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf}
+    else:
+        achieved = alg_bytes / (ms_per_step * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    roof["traffic"] = traffic_for(args.workload)
+    roof["peak_source"] = (f"{peak_kind} {'sustained' if long_run else 'burst'} bf16 "
+                           "(f16 nominal rate = bf16)" if roof["bound"] == "tensor"
+                           else f"{peak_kind} HBM copy")
+    roof["kernel"] = "bwd_a_kernel"
+
+    line = {
+        "metric": "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 operands, f32 accumulate", "data": "synthetic",
+        "config": {"workload": describe(args.workload, probs), "problems": len(probs),
+                   "gflop_per_step": flops / 1e9, "algorithmic_mb_per_step": alg_bytes / 1e6,
+                   "l2": f"rotating {copies} input sets, {copies * per_set / 2**20:.0f} MiB > L2",
+                   "timing": f"CUDA graph of {copies} steps, CUDA events",
+                   "parallelism": f"dp{world} (M-sharded replicas, no collective)"},
+        "e2e": e2e,
+        "roofline": roof,
+        "gpu_launches": K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(probs, budget_s=args.cpu_seconds)
+    return line
+
+
+def bench_e2e(args, probs, host_go, set0, stream, dev, flops, world):
+    import backward_gemm_gb300 as nb
+
+    items, ws = set0
+    pinned_in = []
+    for p, go in zip(probs, host_go):
+        t = torch.from_numpy(go.view(np.int16) if p.go_dtype == BF16 else go)
+        pinned_in.append(t.pin_memory())
+    pinned_out = [torch.empty((p.M, p.K), dtype=torch.float32).pin_memory() for p in probs]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in)
+    d2h = sum(t.numel() * 4 for t in pinned_out)
+    steps = max(3, min(args.steps, 50))
+
+    def one():
+        for (go_d, w, out), hin, hout in zip(items, pinned_in, pinned_out):
+            dst = go_d.view(torch.int16) if go_d.dtype == torch.bfloat16 else go_d
+            dst.copy_(hin, non_blocking=True)
+        run_step(items, ws)
+        for (go_d, w, out), hout in zip(items, pinned_out):
+            hout.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        stream.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            one()
+        ev1.record(stream)
+        ev1.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    return {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "steps": steps}
+
+
+def traffic_for(workload: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary of
+    this workload, if one exists for the current kernel (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(workload)
+    except (OSError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+def cpu_baseline(probs, budget_s: float = 15.0, rows_per_problem: int | None = None):
+    """The CPU oracle as it stands, on a bounded sample: for each problem a slice
+    of its rows (quantise, dequantise and operand rounding included)."""
+    import oracle
+
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    done_flops = 0
+    rows_total = 0
+    sample_desc = []
+    for p in probs:
+        go = make_grad_out(p)
+        B = make_weight(p)
+        data, scales = oracle.quantize(B)
+        bt = oracle.dequantize_f16(scales, data, p.K, p.N)
+        rows = rows_per_problem or max(1, min(p.M, int(2e9 / (2 * p.N * p.K)) or 1))
+        go16 = oracle.round_operand(go[:rows], p.go_dtype)
+        oracle.backward_a_rows(go16, bt, np.arange(rows, dtype=np.int32), want_bound=False)
+        done_flops += 2 * rows * p.N * p.K
+        rows_total += rows
+        if len(sample_desc) < 3:
+            sample_desc.append(f"{rows} of {p.M} rows of {p.M}x{p.N}x{p.K}")
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": dt,
+            "sample": "; ".join(sample_desc) + (f" (+{len(probs) - 3} more problems, "
+                                                if len(probs) > 3 else "")
+                      + ("" if len(probs) <= 3 else f"{rows_total} rows total)")
+                      + "; fp64 sums, includes quantise/dequantise/rounding"}
+
+
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    from oracle.build import build_oracle
+
+    build_oracle()
+    probs = workloads()[args.workload]
+    p = probs[0]
+    go = make_grad_out(p)
+    data, scales = oracle.quantize(make_weight(p))
+    steps_done = 0
+    # A bounded per-step sample: probe the oracle's rate on a few rows, then size
+    # each step so that warm-up plus timed steps take about a minute in total.
+    probe = min(p.M, 8)
+    t0 = time.perf_counter()
+    bt = oracle.dequantize_f16(scales, data, p.K, p.N)
+    oracle.backward_a_rows(oracle.round_operand(go[:probe], p.go_dtype), bt,
+                           np.arange(probe, dtype=np.int32), want_bound=False)
+    rate = 2 * probe * p.N * p.K / max(time.perf_counter() - t0, 1e-6)
+    per_step_s = 60.0 / max(args.steps + args.warmup, 1)
+    rows = max(1, min(p.M, int(rate * per_step_s / (2 * p.N * p.K))))
+
+    def step():
+        bt = oracle.dequantize_f16(scales, data, p.K, p.N)
+        go16 = oracle.round_operand(go[:rows], p.go_dtype)
+        oracle.backward_a_rows(go16, bt, np.arange(rows, dtype=np.int32), want_bound=False)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+        steps_done += 1
+    dt = time.perf_counter() - t0
+    flops = 2 * rows * p.N * p.K * steps_done
+    value = flops / dt / 1e12
+    sample = f"{rows} of {p.M} rows of {p.M}x{p.N}x{p.K} per step (dequantise + rounding + fp64 rows)"
+    return {"metric": "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline",
+            "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(steps_done, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(args.workload, probs),
+                       "parallelism": "host cores (OpenMP), rank 0 only"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="q_proj", choices=sorted(workloads()))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    if args.impl == "reference":
+        line = bench_reference(args, rank, world)
+    else:
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        line = bench_ours(args, rank, world, dev)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -123,9 +123,12 @@ size_t nf4_backward_a_batched_workspace(int count);
  * backward projections per training step).  Every problem follows the rules of
  * nf4_backward_a_ex.  `problems` is a HOST array, read before the call returns.
  * `workspace` is caller-owned device memory of at least
- * nf4_backward_a_batched_workspace(count) bytes, 256-byte aligned; the call
- * writes per-problem descriptors into it with an asynchronous copy on `stream`,
- * so it must not be reused by another call until this one has run.
+ * nf4_backward_a_batched_workspace(count) bytes, 256-byte aligned.  The call
+ * enqueues, on `stream`, small kernels that write the per-problem descriptors
+ * (tensor maps, pointers, sizes) into it -- the descriptors travel as kernel
+ * parameters, so nothing on the host has to outlive the call -- and then the
+ * GEMM kernel that reads them.  The workspace must not be reused by another
+ * call until this one has run.
  */
 int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspace,
                            size_t workspace_bytes, void* stream);

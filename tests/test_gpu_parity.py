@@ -170,6 +170,32 @@ def test_batched_full_step_shapes_one_layer():
         assert_close(out.cpu().numpy()[rows], ref, bound, p.name)
 
 
+def test_batched_call_captured_in_cuda_graph():
+    """The grouped launch's descriptors travel by value, so a captured call replays
+    correctly after everything the host built for it is gone."""
+    import gc
+
+    probs = [Problem(300, 192, 640, F32, 1.0, 0.02, True, 31),
+             Problem(129, 256, 1536, BF16, 1e-2, 0.02, False, 32)]
+    items = [(to_device_go(make_grad_out(p), p.go_dtype),
+              nb().quantize(torch.from_numpy(make_weight(p)).cuda()), None) for p in probs]
+    eager = nb().backward_a_batched(items)
+    outs = [torch.zeros_like(e) for e in eager]
+    ws = nb().batched_workspace(len(items))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        nb().backward_a_batched([(go, w, o) for (go, w, _), o in zip(items, outs)], ws)
+    gc.collect()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    nb().check_error()
+    for e, o in zip(eager, outs):
+        assert torch.equal(e, o)
+
+
 # ---------------------------------------------------------------- edge cases
 def test_empty_and_degenerate():
     w = nb().quantize(torch.from_numpy(make_weight(Problem(1, 64, 128))).cuda())
