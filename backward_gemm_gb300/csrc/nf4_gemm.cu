@@ -93,8 +93,13 @@ struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
 
 static_assert(sizeof(ProblemDesc) % 16 == 0, "descriptor copy granularity");
 
+// One tile of one problem, with the problem's fields read once into registers
+// (the inline-asm memory clobbers would otherwise force reloads every stage).
 struct Tile {
   const ProblemDesc* p;
+  const float* scales;
+  float* grad_A;
+  int M, N, K, dtype;
   int mt, kt, ns;
 };
 
@@ -105,23 +110,45 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int
     if (descs[mid].tile_begin <= t) lo = mid; else hi = mid - 1;
   }
   Tile r;
-  r.p = descs + lo;
-  const int local = t - r.p->tile_begin;
-  r.mt = local % r.p->tiles_m;
-  r.kt = local / r.p->tiles_m;
-  r.ns = r.p->n_stages;
+  const ProblemDesc* p = descs + lo;
+  r.p = p;
+  r.scales = p->scales;
+  r.grad_A = p->grad_A;
+  r.M = p->M;
+  r.N = p->N;
+  r.K = p->K;
+  r.dtype = p->dtype;
+  const int local = t - p->tile_begin;
+  const int tm = p->tiles_m;
+  r.mt = local % tm;
+  r.kt = local / tm;
+  r.ns = p->n_stages;
   return r;
 }
 
-// Scale of (column n, K-block kt*4 + j); 0 outside the weight, so padded
-// columns dequantise to zero.
-__device__ __forceinline__ float load_scale(const ProblemDesc* p, int kt, int s, int j, int nl) {
+// Scale of (column n = stage s row nl, K-block kt*4 + j); 0 outside the weight,
+// so padded columns dequantise to zero.
+__device__ __forceinline__ float load_scale(const Tile& tl, int s, int j, int nl) {
   const int n = s * BN + nl;
-  const int KB = p->K >> 6;
-  const int b = kt * 4 + j;
-  if (n >= p->N || b >= KB) return 0.0f;
-  return __ldg(p->scales + static_cast<int64_t>(n) * KB + b);
+  const int KB = tl.K >> 6;
+  const int b = tl.kt * 4 + j;
+  if (n >= tl.N || b >= KB) return 0.0f;
+  return __ldg(tl.scales + static_cast<int64_t>(n) * KB + b);
 }
+
+// Optional timing probes (compiled in only with -DNF4_TRACE, for profiling):
+// CTA 0 records clock64() at fixed points of each role into a device buffer.
+#ifdef NF4_TRACE
+__device__ unsigned long long* g_trace = nullptr;
+constexpr int kTraceSlots = 2048;
+#define NF4_PROBE(ev, idx)                                                         \
+  do {                                                                             \
+    if (blockIdx.x == 0 && g_trace != nullptr && (idx) < kTraceSlots)              \
+      g_trace[(ev) * kTraceSlots + (idx)] = static_cast<unsigned long long>(clock64()); \
+  } while (0)
+#else
+#define NF4_PROBE(ev, idx) do { } while (0)
+#endif
 
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(kThreads, 1)
@@ -186,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         const Tile tl = tile_at(descs, count, t);
-        const bool f32 = tl.p->dtype == NF4_F32;
+        const bool f32 = tl.dtype == NF4_F32;
         const uint32_t bytes = (f32 ? kGoBytes : kGoBoxBytes) + kNf4Bytes;
         for (int s = 0; s < tl.ns; ++s, ++it) {
           const uint32_t slot = it % kRawStages;
@@ -195,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          NF4_PROBE(7, it);
           const uint32_t fb = full_raw(slot);
           mbar_arrive_expect_tx(fb, bytes);
           const uint32_t dst = sbase + kRawOff + slot * kRawBytes;
@@ -227,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          NF4_PROBE(5, it);
           const uint32_t a_addr = sbase + kOpOff + slot * kOpBytes;
           const uint64_t a_desc = smem_desc_sw128(a_addr, 16, kSbo);
           const uint64_t b_desc = smem_desc_sw128(a_addr + kABytes, kBLbo, kSbo);
@@ -237,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (s | kk) != 0 ? 1u : 0u);
           }
           tc_commit(empty_op(slot));
+          NF4_PROBE(6, it);
         }
         if (!ok) break;
         tc_commit(tmem_full(acc));
@@ -260,23 +290,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     float scale_next = 0.0f;
     if (t < total_tiles) {
       const Tile tl = tile_at(descs, count, t);
-      scale_next = load_scale(tl.p, tl.kt, 0, bj, bn);
+      scale_next = load_scale(tl, 0, bj, bn);
     }
     uint32_t it = 0;
     bool ok = true;
     for (; ok && t < total_tiles; t += gridDim.x) {
       const Tile tl = tile_at(descs, count, t);
-      const bool f32 = tl.p->dtype == NF4_F32;
+      const bool f32 = tl.dtype == NF4_F32;
       for (int s = 0; s < tl.ns; ++s, ++it) {
         const float scale = scale_next;
         if (s + 1 < tl.ns) {
-          scale_next = load_scale(tl.p, tl.kt, s + 1, bj, bn);
+          scale_next = load_scale(tl, s + 1, bj, bn);
         } else if (t + static_cast<int>(gridDim.x) < total_tiles) {
           const Tile nx = tile_at(descs, count, t + gridDim.x);
-          scale_next = load_scale(nx.p, nx.kt, 0, bj, bn);
+          scale_next = load_scale(nx, 0, bj, bn);
         }
         const uint32_t rslot = it % kRawStages;
         const uint32_t oslot = it % kOpStages;
+        const bool probe = (ct == 0);
+        if (probe) NF4_PROBE(0, it);
         // All lanes wait; the warp goes on only if every lane saw the phase
         // complete, so a timeout never leaves the warp divergent.
         const bool got = mbar_wait(full_raw(rslot), (it / kRawStages) & 1u, abort_flag) &&
@@ -285,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        if (probe) NF4_PROBE(1, it);
         const uint32_t raw = sbase + kRawOff + rslot * kRawBytes;
         const uint32_t a_op = sbase + kOpOff + oslot * kOpBytes;
         const uint32_t b_op = a_op + kABytes;
@@ -319,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
+        if (probe) NF4_PROBE(2, it);
         // NF4 block (row n = bn, k = 64*bj .. +63) -> one 128-byte swizzle row of B^T.
         {
           const uint32_t src = raw + kGoBytes + bn * 128;
@@ -331,12 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 8; ++e) sts128(dst + ((static_cast<uint32_t>(e) ^ bswz) << 4),
                                              dequant_word(words[e], tb));
         }
+        if (probe) NF4_PROBE(3, it);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(full_op(oslot));
           mbar_arrive(empty_raw(rslot));
         }
+        if (probe) NF4_PROBE(4, it);
       }
     }
   } else {
@@ -347,10 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc = lt & 1u;
       const bool got = mbar_wait(tmem_full(acc), (lt >> 1) & 1u, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
+      if (threadIdx.x == 0) NF4_PROBE(8, lt);
       tc_fence_after();
       const int row = tl.mt * BM + warp * 32 + lane;
-      const bool row_ok = row < tl.p->M;
-      float* out_row = tl.p->grad_A + static_cast<int64_t>(row_ok ? row : 0) * tl.p->K;
+      const bool row_ok = row < tl.M;
+      float* out_row = tl.grad_A + static_cast<int64_t>(row_ok ? row : 0) * tl.K;
       const uint32_t taddr = tmem_base + acc * BK + (static_cast<uint32_t>(warp * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < BK / 32; ++c) {
@@ -358,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_wait_ld();
         const int col = tl.kt * BK + c * 32;
-        if (row_ok && col < tl.p->K) {
+        if (row_ok && col < tl.K) {
           float4* dst = reinterpret_cast<float4*>(out_row + col);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -369,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty(acc));
+      if (threadIdx.x == 0) NF4_PROBE(9, lt);
     }
   }
 
@@ -606,6 +644,13 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
   return launch(unused, static_cast<const ProblemDesc*>(workspace), static_cast<int>(descs.size()),
                 static_cast<int>(total), st);
 }
+
+#ifdef NF4_TRACE
+extern "C" int nf4_debug_set_trace(void* buf) {
+  unsigned long long* p = static_cast<unsigned long long*>(buf);
+  return cudaMemcpyToSymbol(g_trace, &p, sizeof(p)) == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+}
+#endif
 
 extern "C" int nf4_check_error(void* stream) {
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return NF4_ERR_CUDA;

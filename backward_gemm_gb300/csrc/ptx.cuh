@@ -192,19 +192,18 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uin
 }
 
 // ---------------------------------------------------------------- shared memory
+// Volatile, so these stay in order with the barrier waits and proxy fences.
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
+               : "r"(addr));
   return v;
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
+               "r"(v.z), "r"(v.w));
 }
 
 // ---------------------------------------------------------------- byte permute
