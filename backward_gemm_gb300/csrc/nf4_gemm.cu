@@ -53,8 +53,10 @@ constexpr int kEpiWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kConvWarp0 = 6;
-constexpr int kConvWarps = 8;
-constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;  // 448
+constexpr int kConvGroups = 2;   // group g converts the stages it with it % 2 == g
+constexpr int kGroupWarps = 8;   // warps per group (256 threads)
+constexpr int kConvWarps = kConvGroups * kGroupWarps;
+constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;  // 704
 
 constexpr int kRawStages = 3;
 constexpr int kOpStages = 2;
@@ -74,6 +76,7 @@ constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base t
 constexpr uint32_t kTmemCols = 2 * BK;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOpStages == kConvGroups, "each converter group owns one operand slot");
 static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
@@ -126,14 +129,55 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int
   return r;
 }
 
-// Scale of (column n = stage s row nl, K-block kt*4 + j); 0 outside the weight,
-// so padded columns dequantise to zero.
-__device__ __forceinline__ float load_scale(const Tile& tl, int s, int j, int nl) {
-  const int n = s * BN + nl;
-  const int KB = tl.K >> 6;
-  const int b = tl.kt * 4 + j;
-  if (n >= tl.N || b >= KB) return 0.0f;
-  return __ldg(tl.scales + static_cast<int64_t>(n) * KB + b);
+// Stage cursor of a converter group: which tile and stage it converts next,
+// with the fields of that tile's problem needed for the scale loads.
+struct ConvCursor {
+  int t, s, ns, kt, N, KB;
+  bool f32;
+  const float* scales;
+};
+
+__device__ __forceinline__ void cc_load(ConvCursor& c, const ProblemDesc* descs, int count,
+                                        int total_tiles) {
+  if (c.t < total_tiles) {
+    const Tile tl = tile_at(descs, count, c.t);
+    c.ns = tl.ns;
+    c.kt = tl.kt;
+    c.N = tl.N;
+    c.KB = tl.K >> 6;
+    c.f32 = tl.dtype == NF4_F32;
+    c.scales = tl.scales;
+  }
+}
+
+__device__ __forceinline__ void cc_start(ConvCursor& c, const ProblemDesc* descs, int count,
+                                         int total_tiles) {
+  c.t = blockIdx.x;
+  c.s = 0;
+  c.ns = 1;
+  c.kt = 0;
+  c.N = 0;
+  c.KB = 0;
+  c.f32 = true;
+  c.scales = nullptr;
+  cc_load(c, descs, count, total_tiles);
+}
+
+__device__ __forceinline__ void cc_next(ConvCursor& c, const ProblemDesc* descs, int count,
+                                        int total_tiles) {
+  if (c.t >= total_tiles) return;
+  if (++c.s >= c.ns) {
+    c.s = 0;
+    c.t += gridDim.x;
+    cc_load(c, descs, count, total_tiles);
+  }
+}
+
+__device__ __forceinline__ float cc_scale(const ConvCursor& c, int j, int nl) {
+  const int n = c.s * BN + nl;
+  const int b = c.kt * 4 + j;
+  if (n >= c.N || b >= c.KB) return 0.0f;
+  return __ldg(c.scales + static_cast<int64_t>(n) * c.KB + b);
 }
 
 // Optional timing probes (compiled in only with -DNF4_TRACE, for profiling):
@@ -154,9 +198,10 @@ constexpr int kTraceSlots = 2048;
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_a_kernel(const __grid_constant__ ProblemDesc single, const ProblemDesc* __restrict__ batch,
                  int count, int total_tiles) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Pointer arithmetic on the shared array keeps the shared address space
+  // visible to the compiler, so plain loads and stores below are ld/st.shared.
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(smem);
   const ProblemDesc* descs = batch != nullptr ? batch : &single;
 
@@ -179,10 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
       mbar_init(full_raw(i), 1);
-      mbar_init(empty_raw(i), kConvWarps);
+      mbar_init(empty_raw(i), kGroupWarps);
     }
     for (int i = 0; i < kOpStages; ++i) {
-      mbar_init(full_op(i), kConvWarps);
+      mbar_init(full_op(i), kGroupWarps);
       mbar_init(empty_op(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -278,102 +323,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kConvWarp0) {
     // ---------------------------------------------------------------- converters
-    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..255
-    const int ar = ct & (BM - 1);                   // A: row of the tile
-    const int ahalf = ct >> 7;                      // A: 16-byte chunks 4*ahalf .. +3
-    const int bj = ct >> 6;                         // B: 64-k chunk (NF4 block) 0..3
-    const int bn = ct & 63;                         // B: row n of the stage
+    const int cg_thread = threadIdx.x - kConvWarp0 * 32;  // 0..511
+    const int group = cg_thread >> 8;                     // 0..1
+    const int ct = cg_thread & 255;                       // thread within the group
+    const int ar = ct & (BM - 1);                         // A: row of the tile
+    const int ahalf = ct >> 7;                            // A: 16-byte chunks 4*ahalf .. +3
+    const int bj = ct >> 6;                               // B: 64-k chunk (NF4 block) 0..3
+    const int bn = ct & 63;                               // B: row n of the stage
     const uint32_t aswz = static_cast<uint32_t>(ar & 7);
     const uint32_t bswz = static_cast<uint32_t>(bn & 7);
 
-    int t = blockIdx.x;
-    float scale_next = 0.0f;
-    if (t < total_tiles) {
-      const Tile tl = tile_at(descs, count, t);
-      scale_next = load_scale(tl, 0, bj, bn);
-    }
-    uint32_t it = 0;
-    bool ok = true;
-    for (; ok && t < total_tiles; t += gridDim.x) {
-      const Tile tl = tile_at(descs, count, t);
-      const bool f32 = tl.dtype == NF4_F32;
-      for (int s = 0; s < tl.ns; ++s, ++it) {
-        const float scale = scale_next;
-        if (s + 1 < tl.ns) {
-          scale_next = load_scale(tl, s + 1, bj, bn);
-        } else if (t + static_cast<int>(gridDim.x) < total_tiles) {
-          const Tile nx = tile_at(descs, count, t + gridDim.x);
-          scale_next = load_scale(nx, 0, bj, bn);
-        }
-        const uint32_t rslot = it % kRawStages;
-        const uint32_t oslot = it % kOpStages;
-        const bool probe = (ct == 0);
-        if (probe) NF4_PROBE(0, it);
-        // All lanes wait; the warp goes on only if every lane saw the phase
-        // complete, so a timeout never leaves the warp divergent.
-        const bool got = mbar_wait(full_raw(rslot), (it / kRawStages) & 1u, abort_flag) &&
-                         mbar_wait(empty_op(oslot), ((it / kOpStages) & 1u) ^ 1u, abort_flag);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
-          ok = false;
-          break;
-        }
-        if (probe) NF4_PROBE(1, it);
-        const uint32_t raw = sbase + kRawOff + rslot * kRawBytes;
-        const uint32_t a_op = sbase + kOpOff + oslot * kOpBytes;
-        const uint32_t b_op = a_op + kABytes;
+    // `nxt` runs two stages (one group turn) ahead of the stage being converted,
+    // so the block scale it needs is loaded a whole turn before its use.
+    ConvCursor nxt;
+    cc_start(nxt, descs, count, total_tiles);
+    for (int i = 0; i < group; ++i) cc_next(nxt, descs, count, total_tiles);
+    bool cur_valid = nxt.t < total_tiles;
+    bool cur_f32 = nxt.f32;
+    float scale_cur = cur_valid ? cc_scale(nxt, bj, bn) : 0.0f;
+    cc_next(nxt, descs, count, total_tiles);
+    cc_next(nxt, descs, count, total_tiles);
 
-        // grad_out -> f16 A operand (K-major, 128B swizzle: chunk c of row r at c ^ (r % 8)).
-        const uint32_t a_row = a_op + ar * 128;
-        if (f32) {
-          const uint32_t src = raw + ahalf * kGoBoxBytes + ar * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 x0 = lds128(src + (((2u * i) ^ aswz) << 4));
-            const uint4 x1 = lds128(src + (((2u * i + 1u) ^ aswz) << 4));
-            uint4 h;
-            h.x = pack_f16x2(__uint_as_float(x0.x), __uint_as_float(x0.y));
-            h.y = pack_f16x2(__uint_as_float(x0.z), __uint_as_float(x0.w));
-            h.z = pack_f16x2(__uint_as_float(x1.x), __uint_as_float(x1.y));
-            h.w = pack_f16x2(__uint_as_float(x1.z), __uint_as_float(x1.w));
-            sts128(a_row + (((4u * ahalf + i) ^ aswz) << 4), h);
-          }
-        } else {
-          const uint32_t src = raw + ar * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t c = (4u * ahalf + i) ^ aswz;
-            const uint4 w = lds128(src + (c << 4));
-            uint4 h;
-            h.x = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
-            h.y = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
-            h.z = pack_f16x2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
-            h.w = pack_f16x2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
-            sts128(a_row + (c << 4), h);
-          }
-        }
+    uint32_t it = static_cast<uint32_t>(group);
+    while (cur_valid) {
+      const float scale = scale_cur;
+      const bool f32 = cur_f32;
+      cur_valid = nxt.t < total_tiles;
+      cur_f32 = nxt.f32;
+      scale_cur = cur_valid ? cc_scale(nxt, bj, bn) : 0.0f;
+      cc_next(nxt, descs, count, total_tiles);
+      cc_next(nxt, descs, count, total_tiles);
 
-        if (probe) NF4_PROBE(2, it);
-        // NF4 block (row n = bn, k = 64*bj .. +63) -> one 128-byte swizzle row of B^T.
-        {
-          const uint32_t src = raw + kGoBytes + bn * 128;
-          const uint4 q0 = lds128(src + (((2u * bj) ^ bswz) << 4));
-          const uint4 q1 = lds128(src + (((2u * bj + 1u) ^ bswz) << 4));
-          const BlockTable tb = make_block_table(scale);
-          const uint32_t dst = b_op + bj * kBLbo + (bn >> 3) * kSbo + bswz * 128;
-          const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      const uint32_t rslot = it % kRawStages;
+      const uint32_t oslot = it % kOpStages;
+      const bool probe = (cg_thread == 0);
+      if (probe) NF4_PROBE(0, it);
+      // All lanes wait; the warp goes on only if every lane saw the phase
+      // complete, so a timeout never leaves the warp divergent.
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_raw(rslot), (it / kRawStages) & 1u, abort_flag)))
+        break;
+      if (probe) NF4_PROBE(1, it);
+
+      // Raw inputs of this thread -> registers; then the raw slot is released.
+      const uint8_t* raw = smem + kRawOff + rslot * kRawBytes;
+      uint4 g[8];
+      if (f32) {
+        const uint8_t* src = raw + ahalf * kGoBoxBytes + ar * 128;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sts128(dst + ((static_cast<uint32_t>(e) ^ bswz) << 4),
-                                             dequant_word(words[e], tb));
-        }
-        if (probe) NF4_PROBE(3, it);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(full_op(oslot));
-          mbar_arrive(empty_raw(rslot));
-        }
-        if (probe) NF4_PROBE(4, it);
+        for (int i = 0; i < 8; ++i)
+          g[i] = *reinterpret_cast<const uint4*>(src + ((static_cast<uint32_t>(i) ^ aswz) << 4));
+      } else {
+        const uint8_t* src = raw + ar * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          g[i] = *reinterpret_cast<const uint4*>(src + (((4u * ahalf + i) ^ aswz) << 4));
       }
+      const uint8_t* qsrc = raw + kGoBytes + bn * 128;
+      const uint4 q0 = *reinterpret_cast<const uint4*>(qsrc + (((2u * bj) ^ bswz) << 4));
+      const uint4 q1 = *reinterpret_cast<const uint4*>(qsrc + (((2u * bj + 1u) ^ bswz) << 4));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_raw(rslot));
+
+      if (!__all_sync(0xFFFFFFFFu,
+                      mbar_wait(empty_op(oslot), ((it / kOpStages) & 1u) ^ 1u, abort_flag)))
+        break;
+      if (probe) NF4_PROBE(2, it);
+      uint8_t* a_op = smem + kOpOff + oslot * kOpBytes;
+      uint8_t* b_op = a_op + kABytes;
+
+      // grad_out -> f16 A operand (K-major, 128B swizzle: chunk c of row r at c ^ (r % 8)).
+      uint8_t* a_row = a_op + ar * 128;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 h;
+        if (f32) {
+          const uint4 x0 = g[2 * i], x1 = g[2 * i + 1];
+          h.x = pack_f16x2(__uint_as_float(x0.x), __uint_as_float(x0.y));
+          h.y = pack_f16x2(__uint_as_float(x0.z), __uint_as_float(x0.w));
+          h.z = pack_f16x2(__uint_as_float(x1.x), __uint_as_float(x1.y));
+          h.w = pack_f16x2(__uint_as_float(x1.z), __uint_as_float(x1.w));
+        } else {
+          const uint4 w = g[i];
+          h.x = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+          h.y = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+          h.z = pack_f16x2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+          h.w = pack_f16x2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+        }
+        *reinterpret_cast<uint4*>(a_row + (((4u * ahalf + i) ^ aswz) << 4)) = h;
+      }
+      if (probe) NF4_PROBE(3, it);
+
+      // NF4 block (row n = bn, k = 64*bj .. +63) -> one 128-byte swizzle row of B^T.
+      {
+        const BlockTable tb = make_block_table(scale);
+        uint8_t* dst = b_op + bj * kBLbo + (bn >> 3) * kSbo + bswz * 128;
+        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<uint4*>(dst + ((static_cast<uint32_t>(e) ^ bswz) << 4)) =
+              dequant_word(words[e], tb);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_op(oslot));
+      if (probe) NF4_PROBE(4, it);
+      it += kConvGroups;
     }
   } else {
     // ---------------------------------------------------------------- epilogue
