@@ -5,25 +5,32 @@
 // (page "aprender-gpu 0.32.0 -- src/kernels/backward/nf4_tensor_core.rs",
 // struct doc comment and build_ptx phases 1-4.)  That page's kernel gives one
 // warp a 16x16 output tile and runs WMMA 16x16x16 over N; here the same
-// arithmetic runs as a persistent, warp-specialised sm_103a kernel:
+// arithmetic runs as a persistent, warp-specialised kernel on pairs of SMs:
 //
-//   tile        128 tokens (MMA M) x 256 output columns k (MMA N); the shared
-//               dimension N is consumed 64 at a time (4 MMAs of K=16 each)
-//   warp 4      TMA producer: grad_out tile (fp32 as two 32-column boxes, or one
-//               bf16 box) and the NF4 byte tile (64 rows n x 128 bytes = 256 k),
-//               both 128-byte swizzled, into a 3-stage raw ring
-//   warps 6-13  converters: grad_out -> f16 into the K-major A operand; NF4 codes
-//               x block scale -> f16 into the MN-major B^T operand (one 64-k NF4
-//               block is exactly one 128-byte swizzle row); 2-stage operand ring
-//   warp 5      allocates 512 TMEM columns; one thread issues tcgen05.mma into a
-//               double-buffered fp32 accumulator (2 x 256 columns)
-//   warps 0-3   epilogue: tcgen05.ld of their 32-lane quarter, masked fp32
-//               stores of grad_A (rows >= M and columns >= K are not written),
-//               overlapping the next tile's main loop
+//   pair tile   256 tokens x 256 output columns k, computed by a cluster of two
+//               CTAs with tcgen05.mma.cta_group::2 (M=256, N=256, K=16).  CTA r
+//               of the pair holds grad_out rows 128r..128r+127 of the tile (the A
+//               operand) and dequantises B^T for output columns 128r..128r+127
+//               (its half of the B operand); the MMA reads both halves, so each
+//               SM dequantises only half of what a single-CTA tile would need.
+//               The shared dimension N is consumed 64 at a time (4 MMAs).
+//   warp 4      TMA producer (each CTA): grad_out (fp32 as two 32-column boxes,
+//               or one bf16 box, 128-byte swizzle) and the CTA's NF4 bytes (64
+//               rows n x 64 bytes = 128 k, 64-byte swizzle) into a 3-stage ring
+//   warps 6-21  converters, two groups of 8 warps that take alternate stages:
+//               grad_out -> f16 into the K-major A operand; NF4 codes x block
+//               scale -> f16 into the MN-major B^T operand (one 64-k NF4 block
+//               is one 128-byte swizzle row); each group owns one operand slot
+//   warp 5      allocates 512 TMEM columns in both CTAs; in CTA 0 one thread
+//               issues the pair MMAs into a double-buffered fp32 accumulator
+//               (2 x 256 columns) and commits to barriers of both CTAs
+//   warps 0-3   epilogue (each CTA): tcgen05.ld of a 32-lane quarter, staged
+//               through shared memory and written with TMA stores, which clip
+//               rows >= M and columns >= K; overlaps the next tile's main loop
 //
 // Out-of-range operands contribute 0 (page above, "PHASE 1"/"PHASE 2": zero the
-// out-of-bounds elements): TMA fills rows >= M and columns >= N of grad_out with
-// zeros, and the scale of every column n >= N is taken as 0.
+// out-of-bounds elements): TMA fills rows >= M and columns >= N of grad_out
+// with zeros, and the scale of every column n >= N is taken as 0.
 //
 // The same kernel serves one problem (descriptor passed as a kernel parameter)
 // and a grouped launch over many projections (descriptors in a caller-owned
@@ -45,9 +52,11 @@
 namespace nf4 {
 
 // ------------------------------------------------------------------ geometry
-constexpr int BM = 128;  // tokens per tile (MMA M)
-constexpr int BK = 256;  // output columns k per tile (MMA N)
-constexpr int BN = 64;   // shared-dimension slice per stage (4 x MMA K=16)
+constexpr int BM = 128;        // tokens per CTA (half of the pair's MMA M = 256)
+constexpr int BMP = 2 * BM;    // tokens per pair tile
+constexpr int BK = 256;        // output columns k per pair tile (MMA N)
+constexpr int BKC = BK / 2;    // output columns whose B^T one CTA dequantises
+constexpr int BN = 64;         // shared-dimension slice per stage (4 x MMA K=16)
 
 constexpr int kEpiWarps = 4;
 constexpr int kProducerWarp = 4;
@@ -62,14 +71,16 @@ constexpr int kRawStages = 3;
 constexpr int kOpStages = 2;
 constexpr int kGoBoxBytes = BM * 128;                  // one 128-byte-wide box of 128 rows
 constexpr int kGoBytes = 2 * kGoBoxBytes;              // fp32: 64 columns = two boxes
-constexpr int kNf4Bytes = BN * (BK / 2);               // 64 rows n x 128 bytes
-constexpr int kRawBytes = kGoBytes + kNf4Bytes;        // 40 KB
+constexpr int kNf4Bytes = BN * (BKC / 2);              // 64 rows n x 64 bytes
+constexpr int kRawBytes = kGoBytes + kNf4Bytes;        // 36 KB
 constexpr int kABytes = BM * BN * 2;                   // 16 KB f16
-constexpr int kBBytes = BK * BN * 2;                   // 32 KB f16
-constexpr int kOpBytes = kABytes + kBBytes;            // 48 KB
+constexpr int kBBytes = BKC * BN * 2;                  // 16 KB f16
+constexpr int kOpBytes = kABytes + kBBytes;            // 32 KB
+constexpr int kEpiBufBytes = 32 * 128;                 // 32 rows x 32 fp32
 constexpr int kRawOff = 0;
 constexpr int kOpOff = kRawOff + kRawStages * kRawBytes;
-constexpr int kBarOff = kOpOff + kOpStages * kOpBytes;
+constexpr int kEpiOff = kOpOff + kOpStages * kOpBytes;
+constexpr int kBarOff = kEpiOff + kEpiWarps * 2 * kEpiBufBytes;
 constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 + 2 + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
@@ -87,21 +98,20 @@ constexpr uint32_t kSbo = 1024;
 // ------------------------------------------------------------------ problems
 struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
   CUtensorMap tm_go;   // grad_out [M][N], box 128 rows x 128 bytes, 128B swizzle
-  CUtensorMap tm_nf4;  // codes [N][K/2] bytes, box 64 rows x 128 bytes, 128B swizzle
+  CUtensorMap tm_nf4;  // codes [N][K/2] bytes, box 64 rows x 64 bytes, 64B swizzle
+  CUtensorMap tm_out;  // grad_A [M][K] fp32, box 32 rows x 32 columns, 128B swizzle
   const float* scales;
   float* grad_A;
   int M, N, K, dtype;
-  int tiles_m, tiles_k, n_stages, tile_begin;
+  int tiles_m, tiles_k, n_stages, tile_begin;  // tiles_m counts 256-row pair tiles
 };
 
 static_assert(sizeof(ProblemDesc) % 16 == 0, "descriptor copy granularity");
 
-// One tile of one problem, with the problem's fields read once into registers
-// (the inline-asm memory clobbers would otherwise force reloads every stage).
+// One pair tile of one problem, with the problem's fields read once into
+// registers (the inline-asm memory clobbers would otherwise force reloads).
 struct Tile {
   const ProblemDesc* p;
-  const float* scales;
-  float* grad_A;
   int M, N, K, dtype;
   int mt, kt, ns;
 };
@@ -115,8 +125,6 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int
   Tile r;
   const ProblemDesc* p = descs + lo;
   r.p = p;
-  r.scales = p->scales;
-  r.grad_A = p->grad_A;
   r.M = p->M;
   r.N = p->N;
   r.K = p->K;
@@ -129,8 +137,8 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int
   return r;
 }
 
-// Stage cursor of a converter group: which tile and stage it converts next,
-// with the fields of that tile's problem needed for the scale loads.
+// Stage cursor of a converter group: which pair tile and stage it converts
+// next, with the fields of that tile's problem needed for the scale loads.
 struct ConvCursor {
   int t, s, ns, kt, N, KB;
   bool f32;
@@ -146,13 +154,13 @@ __device__ __forceinline__ void cc_load(ConvCursor& c, const ProblemDesc* descs,
     c.N = tl.N;
     c.KB = tl.K >> 6;
     c.f32 = tl.dtype == NF4_F32;
-    c.scales = tl.scales;
+    c.scales = tl.p->scales;
   }
 }
 
-__device__ __forceinline__ void cc_start(ConvCursor& c, const ProblemDesc* descs, int count,
-                                         int total_tiles) {
-  c.t = blockIdx.x;
+__device__ __forceinline__ void cc_start(ConvCursor& c, int t0, const ProblemDesc* descs,
+                                         int count, int total_tiles) {
+  c.t = t0;
   c.s = 0;
   c.ns = 1;
   c.kt = 0;
@@ -163,19 +171,21 @@ __device__ __forceinline__ void cc_start(ConvCursor& c, const ProblemDesc* descs
   cc_load(c, descs, count, total_tiles);
 }
 
-__device__ __forceinline__ void cc_next(ConvCursor& c, const ProblemDesc* descs, int count,
-                                        int total_tiles) {
+__device__ __forceinline__ void cc_next(ConvCursor& c, int stride, const ProblemDesc* descs,
+                                        int count, int total_tiles) {
   if (c.t >= total_tiles) return;
   if (++c.s >= c.ns) {
     c.s = 0;
-    c.t += gridDim.x;
+    c.t += stride;
     cc_load(c, descs, count, total_tiles);
   }
 }
 
-__device__ __forceinline__ float cc_scale(const ConvCursor& c, int j, int nl) {
+// Scale of column n = (stage row nl) and global K-block kt*4 + 2*rank + j; 0
+// outside the weight, so padded columns dequantise to zero.
+__device__ __forceinline__ float cc_scale(const ConvCursor& c, uint32_t rank, int j, int nl) {
   const int n = c.s * BN + nl;
-  const int b = c.kt * 4 + j;
+  const int b = c.kt * 4 + 2 * static_cast<int>(rank) + j;
   if (n >= c.N || b >= c.KB) return 0.0f;
   return __ldg(c.scales + static_cast<int64_t>(n) * c.KB + b);
 }
@@ -201,9 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // Pointer arithmetic on the shared array keeps the shared address space
   // visible to the compiler, so plain loads and stores below are ld/st.shared.
+  // Both CTAs of a pair get the same offsets (the pair MMA relies on that).
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(smem);
   const ProblemDesc* descs = batch != nullptr ? batch : &single;
+  const uint32_t rank = cluster_ctarank();          // 0 = leader (issues the MMAs)
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
 
   const uint32_t bar0 = sbase + kBarOff;
   auto full_raw = [&](uint32_t i) { return bar0 + 8u * i; };
@@ -227,23 +241,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_raw(i), kGroupWarps);
     }
     for (int i = 0; i < kOpStages; ++i) {
-      mbar_init(full_op(i), kGroupWarps);
+      mbar_init(full_op(i), 2 * kGroupWarps);  // converters of both CTAs (used in CTA 0)
       mbar_init(empty_op(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tmem_full(i), 1);
-      mbar_init(tmem_empty(i), kEpiWarps);
+      mbar_init(tmem_empty(i), 2 * kEpiWarps);  // epilogues of both CTAs (used in CTA 0)
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -256,10 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      for (int t = cluster; ok && t < total_tiles; t += nclusters) {
         const Tile tl = tile_at(descs, count, t);
         const bool f32 = tl.dtype == NF4_F32;
         const uint32_t bytes = (f32 ? kGoBytes : kGoBoxBytes) + kNf4Bytes;
+        const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
+        const int x_nf4 = tl.kt * (BK / 2) + static_cast<int>(rank) * (BKC / 2);
         for (int s = 0; s < tl.ns; ++s, ++it) {
           const uint32_t slot = it % kRawStages;
           const uint32_t ph = (it / kRawStages) & 1u;
@@ -271,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_raw(slot);
           mbar_arrive_expect_tx(fb, bytes);
           const uint32_t dst = sbase + kRawOff + slot * kRawBytes;
-          tma_load_2d(dst, &tl.p->tm_go, s * BN, tl.mt * BM, fb);
-          if (f32) tma_load_2d(dst + kGoBoxBytes, &tl.p->tm_go, s * BN + 32, tl.mt * BM, fb);
-          tma_load_2d(dst + kGoBytes, &tl.p->tm_nf4, tl.kt * (BK / 2), s * BN, fb);
+          tma_load_2d(dst, &tl.p->tm_go, s * BN, row0, fb);
+          if (f32) tma_load_2d(dst + kGoBoxBytes, &tl.p->tm_go, s * BN + 32, row0, fb);
+          tma_load_2d(dst + kGoBytes, &tl.p->tm_nf4, x_nf4, s * BN, fb);
         }
       }
       // Every issued copy must land before the CTA may exit.
@@ -282,20 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(BM, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
+    // ---------------------------------------------------------------- MMA issuer (CTA 0)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BMP, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
       uint32_t it = 0, lt = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++lt) {
+      for (int t = cluster; ok && t < total_tiles; t += nclusters, ++lt) {
         const Tile tl = tile_at(descs, count, t);
         const uint32_t acc = lt & 1u;
-        if (!mbar_wait(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u, abort_flag)) break;
+        if (!mbar_wait_cluster(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BK;
         for (int s = 0; s < tl.ns; ++s, ++it) {
           const uint32_t slot = it % kOpStages;
-          if (!mbar_wait(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
+          if (!mbar_wait_cluster(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -307,17 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
-            tc_mma_f16(d_tmem, a_desc + 2u * kk, b_desc + (2u * kSbo >> 4) * kk, idesc,
-                       (s | kk) != 0 ? 1u : 0u);
+            tc_mma_f16_pair(d_tmem, a_desc + 2u * kk, b_desc + (2u * kSbo >> 4) * kk, idesc,
+                            (s | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(empty_op(slot));
+          tc_commit_pair(empty_op(slot), 0x3);
           NF4_PROBE(6, it);
         }
         if (!ok) break;
-        tc_commit(tmem_full(acc));
+        tc_commit_pair(tmem_full(acc), 0x3);
       }
-      // No MMA may still be writing TMEM when it is released.
-      tc_commit(mma_done);
+      // No MMA may still be writing TMEM (of either CTA) when it is released.
+      tc_commit_pair(mma_done, 0x1);
       mbar_wait(mma_done, 0, nullptr);
     }
     __syncwarp();
@@ -326,23 +343,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cg_thread = threadIdx.x - kConvWarp0 * 32;  // 0..511
     const int group = cg_thread >> 8;                     // 0..1
     const int ct = cg_thread & 255;                       // thread within the group
-    const int ar = ct & (BM - 1);                         // A: row of the tile
+    const int ar = ct & (BM - 1);                         // A: row of the CTA's tile
     const int ahalf = ct >> 7;                            // A: 16-byte chunks 4*ahalf .. +3
-    const int bj = ct >> 6;                               // B: 64-k chunk (NF4 block) 0..3
     const int bn = ct & 63;                               // B: row n of the stage
+    const int bj = (ct >> 6) & 1;                         // B: NF4 block of the CTA's half
+    const int bh = ct >> 7;                               // B: words 4*bh .. +3 of the block
     const uint32_t aswz = static_cast<uint32_t>(ar & 7);
     const uint32_t bswz = static_cast<uint32_t>(bn & 7);
+    const uint32_t qchunk = ((2u * bj + bh) ^ ((static_cast<uint32_t>(bn) >> 1) & 3u)) << 4;
+    const uint32_t full_op_leader0 = mapa_shared(full_op(0), 0);
 
     // `nxt` runs two stages (one group turn) ahead of the stage being converted,
     // so the block scale it needs is loaded a whole turn before its use.
     ConvCursor nxt;
-    cc_start(nxt, descs, count, total_tiles);
-    for (int i = 0; i < group; ++i) cc_next(nxt, descs, count, total_tiles);
+    cc_start(nxt, cluster, descs, count, total_tiles);
+    for (int i = 0; i < group; ++i) cc_next(nxt, nclusters, descs, count, total_tiles);
     bool cur_valid = nxt.t < total_tiles;
     bool cur_f32 = nxt.f32;
-    float scale_cur = cur_valid ? cc_scale(nxt, bj, bn) : 0.0f;
-    cc_next(nxt, descs, count, total_tiles);
-    cc_next(nxt, descs, count, total_tiles);
+    float scale_cur = cur_valid ? cc_scale(nxt, rank, bj, bn) : 0.0f;
+    cc_next(nxt, nclusters, descs, count, total_tiles);
+    cc_next(nxt, nclusters, descs, count, total_tiles);
 
     uint32_t it = static_cast<uint32_t>(group);
     while (cur_valid) {
@@ -350,9 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool f32 = cur_f32;
       cur_valid = nxt.t < total_tiles;
       cur_f32 = nxt.f32;
-      scale_cur = cur_valid ? cc_scale(nxt, bj, bn) : 0.0f;
-      cc_next(nxt, descs, count, total_tiles);
-      cc_next(nxt, descs, count, total_tiles);
+      scale_cur = cur_valid ? cc_scale(nxt, rank, bj, bn) : 0.0f;
+      cc_next(nxt, nclusters, descs, count, total_tiles);
+      cc_next(nxt, nclusters, descs, count, total_tiles);
 
       const uint32_t rslot = it % kRawStages;
       const uint32_t oslot = it % kOpStages;
@@ -378,14 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 4; ++i)
           g[i] = *reinterpret_cast<const uint4*>(src + (((4u * ahalf + i) ^ aswz) << 4));
       }
-      const uint8_t* qsrc = raw + kGoBytes + bn * 128;
-      const uint4 q0 = *reinterpret_cast<const uint4*>(qsrc + (((2u * bj) ^ bswz) << 4));
-      const uint4 q1 = *reinterpret_cast<const uint4*>(qsrc + (((2u * bj + 1u) ^ bswz) << 4));
+      const uint4 q = *reinterpret_cast<const uint4*>(raw + kGoBytes + bn * (BKC / 2) + qchunk);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_raw(rslot));
 
-      if (!__all_sync(0xFFFFFFFFu,
-                      mbar_wait(empty_op(oslot), ((it / kOpStages) & 1u) ^ 1u, abort_flag)))
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(empty_op(oslot),
+                                                     ((it / kOpStages) & 1u) ^ 1u, abort_flag)))
         break;
       if (probe) NF4_PROBE(2, it);
       uint8_t* a_op = smem + kOpOff + oslot * kOpBytes;
@@ -413,62 +431,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (probe) NF4_PROBE(3, it);
 
-      // NF4 block (row n = bn, k = 64*bj .. +63) -> one 128-byte swizzle row of B^T.
+      // Half an NF4 block (row n = bn, k = 64*bj + 32*bh .. +31) -> four 16-byte
+      // chunks of one 128-byte swizzle row of B^T.
       {
         const BlockTable tb = make_block_table(scale);
         uint8_t* dst = b_op + bj * kBLbo + (bn >> 3) * kSbo + bswz * 128;
-        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<uint4*>(dst + ((static_cast<uint32_t>(e) ^ bswz) << 4)) =
+        for (int e = 0; e < 4; ++e)
+          *reinterpret_cast<uint4*>(dst + (((4u * bh + e) ^ bswz) << 4)) =
               dequant_word(words[e], tb);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(full_op(oslot));
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(full_op(oslot));
+        else mbar_arrive_remote(full_op_leader0 + 8u * oslot);
+      }
       if (probe) NF4_PROBE(4, it);
       it += kConvGroups;
     }
   } else {
     // ---------------------------------------------------------------- epilogue
+    const uint32_t tmem_empty_leader0 = mapa_shared(tmem_empty(0), 0);
+    uint8_t* stage_buf = smem + kEpiOff + warp * 2 * kEpiBufBytes;
     uint32_t lt = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++lt) {
+    for (int t = cluster; t < total_tiles; t += nclusters, ++lt) {
       const Tile tl = tile_at(descs, count, t);
       const uint32_t acc = lt & 1u;
-      const bool got = mbar_wait(tmem_full(acc), (lt >> 1) & 1u, abort_flag);
+      const bool got = mbar_wait_cluster(tmem_full(acc), (lt >> 1) & 1u, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       if (threadIdx.x == 0) NF4_PROBE(8, lt);
       tc_fence_after();
-      const int row = tl.mt * BM + warp * 32 + lane;
-      const bool row_ok = row < tl.M;
-      float* out_row = tl.grad_A + static_cast<int64_t>(row_ok ? row : 0) * tl.K;
+      const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM + warp * 32;
       const uint32_t taddr = tmem_base + acc * BK + (static_cast<uint32_t>(warp * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < BK / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_wait_ld();
-        const int col = tl.kt * BK + c * 32;
-        if (row_ok && col < tl.K) {
-          float4* dst = reinterpret_cast<float4*>(out_row + col);
+        uint8_t* buf = stage_buf + (c & 1) * kEpiBufBytes;
+        if (c >= 2) {
+          if (lane == 0) bulk_wait_read<1>();  // the store that last read `buf` is done
+          __syncwarp();
+        }
+        // Row `lane` of the 32 x 32 fp32 block, 128-byte swizzled.
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        for (int q4 = 0; q4 < 8; ++q4)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((static_cast<uint32_t>(q4) ^ (lane & 7)) << 4)) =
+              make_uint4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * 32, row0, smem_addr(buf));
+          bulk_commit();
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty(acc));
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(tmem_empty(acc));
+        else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
+      }
       if (threadIdx.x == 0) NF4_PROBE(9, lt);
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
     }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the leader's MMAs are done and no remote arrive is in flight
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -476,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Descriptors of a grouped launch travel to the workspace as kernel parameters
 // (copied by value at launch, also when the launch is captured in a CUDA graph),
 // kDescsPerUpload at a time.
-constexpr int kDescsPerUpload = 72;
+constexpr int kDescsPerUpload = 60;
 struct DescChunk {
   ProblemDesc d[kDescsPerUpload];
 };
@@ -512,7 +550,7 @@ static EncodeTiledFn encode_fn() {
 
 static bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base,
                       uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                      uint32_t box_outer) {
+                      uint32_t box_outer, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -520,7 +558,7 @@ static bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* ba
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -545,10 +583,16 @@ static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* sca
   const bool f32 = dtype == NF4_F32;
   if (!encode_2d(&d->tm_go, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                  go, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
-                 static_cast<uint64_t>(N) * (f32 ? 4 : 2), f32 ? 32 : 64, BM))
+                 static_cast<uint64_t>(N) * (f32 ? 4 : 2), f32 ? 32 : 64, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   if (!encode_2d(&d->tm_nf4, CU_TENSOR_MAP_DATA_TYPE_UINT8, data, static_cast<uint64_t>(K / 2),
-                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), BK / 2, BN))
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), BKC / 2, BN,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
+    return NF4_ERR_CUDA;
+  if (!encode_2d(&d->tm_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, grad_A, static_cast<uint64_t>(K),
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 4, 32, 32,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   d->scales = scales;
   d->grad_A = grad_A;
@@ -556,7 +600,7 @@ static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* sca
   d->N = N;
   d->K = K;
   d->dtype = dtype;
-  d->tiles_m = (M + BM - 1) / BM;
+  d->tiles_m = (M + BMP - 1) / BMP;
   d->tiles_k = (K + BK - 1) / BK;
   d->n_stages = (N + BN - 1) / BN;
   d->tile_begin = 0;
@@ -564,8 +608,8 @@ static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* sca
 }
 
 struct DeviceInfo {
-  int sms = 0;
-  bool attr_set = false;
+  int max_clusters = 0;  // pairs of CTAs that fit on the device at once
+  bool ready = false;
 };
 
 static int device_info(DeviceInfo** out) {
@@ -575,13 +619,30 @@ static int device_info(DeviceInfo** out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NF4_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
   DeviceInfo& di = infos[dev];
-  if (!di.attr_set) {
-    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return NF4_ERR_CUDA;
+  if (!di.ready) {
     if (cudaFuncSetAttribute(bwd_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return NF4_ERR_CUDA;
-    di.attr_set = true;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NF4_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, bwd_a_kernel, &cfg) != cudaSuccess ||
+        clusters <= 0)
+      clusters = sms / 2;
+    di.max_clusters = clusters;
+    di.ready = true;
   }
   *out = &di;
   return NF4_OK;
@@ -592,8 +653,21 @@ static int launch(const ProblemDesc& single, const ProblemDesc* batch, int count
   DeviceInfo* di = nullptr;
   const int rc = device_info(&di);
   if (rc != NF4_OK) return rc;
-  const int grid = std::min(total_tiles, di->sms);
-  bwd_a_kernel<<<grid, kThreads, kSmemBytes, stream>>>(single, batch, count, total_tiles);
+  const int clusters = std::min(total_tiles, di->max_clusters);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, bwd_a_kernel, single, batch, count, total_tiles) != cudaSuccess)
+    return NF4_ERR_CUDA;
   return launch_status();
 }
 
