@@ -20,7 +20,8 @@
 //   warps 6-21  converters, two groups of 8 warps that take alternate stages:
 //               grad_out -> f16 into the K-major A operand; NF4 codes x block
 //               scale -> f16 into the MN-major B^T operand (one 64-k NF4 block
-//               is one 128-byte swizzle row); each group owns one operand slot
+//               is one 128-byte swizzle row); stage i goes to operand slot
+//               i % 3, so a group can start as soon as MMA i-3 is done
 //   warp 5      allocates 512 TMEM columns in both CTAs; in CTA 0 one thread
 //               issues the pair MMAs into a double-buffered fp32 accumulator
 //               (2 x 256 columns) and commits to barriers of both CTAs
@@ -68,7 +69,7 @@ constexpr int kConvWarps = kConvGroups * kGroupWarps;
 constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;  // 704
 
 constexpr int kRawStages = 3;
-constexpr int kOpStages = 2;
+constexpr int kOpStages = 3;
 constexpr int kGoBoxBytes = BM * 128;                  // one 128-byte-wide box of 128 rows
 constexpr int kGoBytes = 2 * kGoBoxBytes;              // fp32: 64 columns = two boxes
 constexpr int kNf4Bytes = BN * (BKC / 2);              // 64 rows n x 64 bytes
@@ -80,14 +81,13 @@ constexpr int kEpiBufBytes = 32 * 128;                 // 32 rows x 32 fp32
 constexpr int kRawOff = 0;
 constexpr int kOpOff = kRawOff + kRawStages * kRawBytes;
 constexpr int kEpiOff = kOpOff + kOpStages * kOpBytes;
-constexpr int kBarOff = kEpiOff + kEpiWarps * 2 * kEpiBufBytes;
+constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
 constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 + 2 + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 2 * BK;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOpStages == kConvGroups, "each converter group owns one operand slot");
 static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     const uint32_t tmem_empty_leader0 = mapa_shared(tmem_empty(0), 0);
-    uint8_t* stage_buf = smem + kEpiOff + warp * 2 * kEpiBufBytes;
+    uint8_t* buf = smem + kEpiOff + warp * kEpiBufBytes;
     uint32_t lt = 0;
     for (int t = cluster; t < total_tiles; t += nclusters, ++lt) {
       const Tile tl = tile_at(descs, count, t);
@@ -470,11 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_wait_ld();
-        uint8_t* buf = stage_buf + (c & 1) * kEpiBufBytes;
-        if (c >= 2) {
-          if (lane == 0) bulk_wait_read<1>();  // the store that last read `buf` is done
-          __syncwarp();
-        }
+        if (lane == 0) bulk_wait_read<0>();  // the previous store has read `buf`
+        __syncwarp();
         // Row `lane` of the 32 x 32 fp32 block, 128-byte swizzled.
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
