@@ -191,14 +191,18 @@ __device__ __forceinline__ float cc_scale(const ConvCursor& c, uint32_t rank, in
 }
 
 // Optional timing probes (compiled in only with -DNF4_TRACE, for profiling):
-// CTA 0 records clock64() at fixed points of each role into a device buffer.
+// the two CTAs of cluster 0 record clock64() at fixed points of each role into
+// a device buffer [cta][event][slot]; event kTraceEvents-1 slot 0 is the clock
+// right after the start-up cluster barrier, the common reference of both CTAs.
 #ifdef NF4_TRACE
 __device__ unsigned long long* g_trace = nullptr;
-constexpr int kTraceSlots = 2048;
-#define NF4_PROBE(ev, idx)                                                         \
-  do {                                                                             \
-    if (blockIdx.x == 0 && g_trace != nullptr && (idx) < kTraceSlots)              \
-      g_trace[(ev) * kTraceSlots + (idx)] = static_cast<unsigned long long>(clock64()); \
+constexpr int kTraceSlots = 512;
+constexpr int kTraceEvents = 40;
+#define NF4_PROBE(ev, idx)                                                               \
+  do {                                                                                   \
+    if (blockIdx.x < 2 && g_trace != nullptr && (idx) < kTraceSlots)                     \
+      g_trace[(blockIdx.x * kTraceEvents + (ev)) * kTraceSlots + (idx)] =                 \
+          static_cast<unsigned long long>(clock64());                                    \
   } while (0)
 #else
 #define NF4_PROBE(ev, idx) do { } while (0)
@@ -259,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+  if (threadIdx.x == 0) NF4_PROBE(39, 0);
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          NF4_PROBE(7, it);
+          NF4_PROBE(34, it);
           const uint32_t fb = full_raw(slot);
           mbar_arrive_expect_tx(fb, bytes);
           const uint32_t dst = sbase + kRawOff + slot * kRawBytes;
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          NF4_PROBE(5, it);
+          NF4_PROBE(32, it);
           const uint32_t a_addr = sbase + kOpOff + slot * kOpBytes;
           const uint64_t a_desc = smem_desc_sw128(a_addr, 16, kSbo);
           const uint64_t b_desc = smem_desc_sw128(a_addr + kABytes, kBLbo, kSbo);
@@ -328,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (s | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair(empty_op(slot), 0x3);
-          NF4_PROBE(6, it);
+          NF4_PROBE(33, it);
         }
         if (!ok) break;
         tc_commit_pair(tmem_full(acc), 0x3);
@@ -376,13 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const uint32_t rslot = it % kRawStages;
       const uint32_t oslot = it % kOpStages;
-      const bool probe = (cg_thread == 0);
-      if (probe) NF4_PROBE(0, it);
+      const bool probe = (lane == 0);
+      const int cw = cg_thread >> 5;  // converter warp 0..15
       // All lanes wait; the warp goes on only if every lane saw the phase
       // complete, so a timeout never leaves the warp divergent.
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_raw(rslot), (it / kRawStages) & 1u, abort_flag)))
         break;
-      if (probe) NF4_PROBE(1, it);
 
       // Raw inputs of this thread -> registers; then the raw slot is released.
       const uint8_t* raw = smem + kRawOff + rslot * kRawBytes;
@@ -405,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(empty_op(oslot),
                                                      ((it / kOpStages) & 1u) ^ 1u, abort_flag)))
         break;
-      if (probe) NF4_PROBE(2, it);
+      if (probe) NF4_PROBE(cw, it);
       uint8_t* a_op = smem + kOpOff + oslot * kOpBytes;
       uint8_t* b_op = a_op + kABytes;
 
@@ -429,7 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *reinterpret_cast<uint4*>(a_row + (((4u * ahalf + i) ^ aswz) << 4)) = h;
       }
-      if (probe) NF4_PROBE(3, it);
 
       // Half an NF4 block (row n = bn, k = 64*bj + 32*bh .. +31) -> four 16-byte
       // chunks of one 128-byte swizzle row of B^T.
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rank == 0) mbar_arrive(full_op(oslot));
         else mbar_arrive_remote(full_op_leader0 + 8u * oslot);
       }
-      if (probe) NF4_PROBE(4, it);
+      if (probe) NF4_PROBE(16 + cw, it);
       it += kConvGroups;
     }
   } else {
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc = lt & 1u;
       const bool got = mbar_wait_cluster(tmem_full(acc), (lt >> 1) & 1u, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
-      if (threadIdx.x == 0) NF4_PROBE(8, lt);
+      if (threadIdx.x == 0) NF4_PROBE(35, lt);
       tc_fence_after();
       const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM + warp * 32;
       const uint32_t taddr = tmem_base + acc * BK + (static_cast<uint32_t>(warp * 32) << 16);
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rank == 0) mbar_arrive(tmem_empty(acc));
         else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
       }
-      if (threadIdx.x == 0) NF4_PROBE(9, lt);
+      if (threadIdx.x == 0) NF4_PROBE(36, lt);
       if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
     }
