@@ -80,12 +80,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 }
 
 // Wait variant for barriers that receive arrivals from the other CTA of the
-// cluster (acquire at cluster scope).
+// cluster or from the pair's tensor-core commits (default semantics).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -124,10 +124,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared).
+// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared),
+// with the default (release, CTA-scope) semantics: the data the arrival
+// publishes is shared memory of the arriving CTA, handed to the async proxy by
+// fence.proxy.async before the arrive.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
