@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          NF4_PROBE(34, it);
+          NF4_PROBE(30, it);
           const uint32_t fb = full_raw(slot);
           mbar_arrive_expect_tx(fb, bytes);
           const uint32_t dst = sbase + kRawOff + slot * kRawBytes;
@@ -317,12 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * BK;
         for (int s = 0; s < tl.ns; ++s, ++it) {
           const uint32_t slot = it % kOpStages;
+          NF4_PROBE(32, it);
           if (!mbar_wait_cluster(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          NF4_PROBE(32, it);
+          NF4_PROBE(33, it);
           const uint32_t a_addr = sbase + kOpOff + slot * kOpBytes;
           const uint64_t a_desc = smem_desc_sw128(a_addr, 16, kSbo);
           const uint64_t b_desc = smem_desc_sw128(a_addr + kABytes, kBLbo, kSbo);
@@ -331,9 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
             tc_mma_f16_pair(d_tmem, a_desc + 2u * kk, b_desc + (2u * kSbo >> 4) * kk, idesc,
                             (s | kk) != 0 ? 1u : 0u);
+            NF4_PROBE(34 + kk, it);
           }
           tc_commit_pair(empty_op(slot), 0x3);
-          NF4_PROBE(33, it);
+          NF4_PROBE(38, it);
         }
         if (!ok) break;
         tc_commit_pair(tmem_full(acc), 0x3);
