@@ -312,13 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = cluster; ok && t < total_tiles; t += nclusters, ++lt) {
         const Tile tl = tile_at(descs, count, t);
         const uint32_t acc = lt & 1u;
-        if (!mbar_wait_cluster(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u, abort_flag)) break;
+        if (!mbar_spin(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BK;
         for (int s = 0; s < tl.ns; ++s, ++it) {
           const uint32_t slot = it % kOpStages;
           NF4_PROBE(32, it);
-          if (!mbar_wait_cluster(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
+          if (!mbar_spin(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -332,7 +332,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
             tc_mma_f16_pair(d_tmem, a_desc + 2u * kk, b_desc + (2u * kSbo >> 4) * kk, idesc,
                             (s | kk) != 0 ? 1u : 0u);
-            NF4_PROBE(34 + kk, it);
           }
           tc_commit_pair(empty_op(slot), 0x3);
           NF4_PROBE(38, it);
