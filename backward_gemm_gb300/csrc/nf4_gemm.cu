@@ -301,6 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every issued copy must land before the CTA may exit.
       for (uint32_t i = (it > kRawStages ? it - kRawStages : 0u); i < it; ++i)
         mbar_wait(full_raw(i % kRawStages), (i / kRawStages) & 1u, nullptr);
+      // So must every commit the leader multicasts into this CTA's operand-slot
+      // barriers (nobody else waits for the last ones): wait for the last phase
+      // of each slot.  Both CTAs run the same stage sequence.
+      if (ok) {
+        for (uint32_t i = (it > kOpStages ? it - kOpStages : 0u); i < it; ++i)
+          mbar_wait_cluster(empty_op(i % kOpStages), (i / kOpStages) & 1u, nullptr);
+      }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -312,7 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = cluster; ok && t < total_tiles; t += nclusters, ++lt) {
         const Tile tl = tile_at(descs, count, t);
         const uint32_t acc = lt & 1u;
-        if (!mbar_spin(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u, abort_flag)) break;
+        if (!mbar_spin(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BK;
         for (int s = 0; s < tl.ns; ++s, ++it) {
@@ -342,6 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // No MMA may still be writing TMEM (of either CTA) when it is released.
       tc_commit_pair(mma_done, 0x1);
       mbar_wait(mma_done, 0, nullptr);
+      // The epilogues' arrivals for the last two tiles are not needed by any MMA,
+      // but the CTA may not exit while one from the other CTA is still in flight.
+      if (ok) {
+        for (uint32_t l = (lt > 2 ? lt - 2 : 0u); l < lt; ++l)
+          mbar_spin(tmem_empty(l & 1u), (l >> 1) & 1u, nullptr);
+      }
     }
     __syncwarp();
   } else if (warp >= kConvWarp0) {
