@@ -80,12 +80,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 }
 
 // Wait variant for barriers that receive arrivals from the other CTA of the
-// cluster or from the pair's tensor-core commits (default semantics).
+// cluster or from the pair's tensor-core commits (acquire at cluster scope).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -110,37 +110,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
-// Non-suspending poll of a barrier phase (for the single MMA-issuing thread,
-// whose every idle cycle is an idle tensor-core cycle).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Spin until the phase completes; bounded like mbar_wait.
-__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
-    if (abort_flag != nullptr && *abort_flag != 0) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicExch(&g_status, kStatusTimeout);
-      if (abort_flag != nullptr) *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -156,11 +125,10 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 }
 
 // Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared),
-// with the default (release, CTA-scope) semantics: the data the arrival
-// publishes is shared memory of the arriving CTA, handed to the async proxy by
-// fence.proxy.async before the arrive.
+// releasing at cluster scope what this thread has observed.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
