@@ -1,0 +1,100 @@
+"""The C ABI (no GPU needed): the library builds, loads, exports every function
+that include/nf4bwd.h declares, and rejects bad arguments on the host before
+touching the device."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nf4bwd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from backward_gemm_gb300.build import build
+
+    build()
+    import backward_gemm_gb300 as nb
+
+    return nb.lib()
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nf4_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_calls():
+    names = declared_functions()
+    for n in ("nf4_quantize", "nf4_dequantize_f16", "nf4_backward_a", "nf4_backward_a_ex",
+              "nf4_backward_a_batched", "nf4_backward_a_batched_workspace", "nf4_check_error",
+              "nf4_status_string", "nf4_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (nf4_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert getattr(lib, n) is not None
+
+
+def test_binding_covers_every_declared_symbol():
+    import backward_gemm_gb300 as nb
+
+    assert set(declared_functions()) <= set(nb.SIGNATURES)
+
+
+def test_status_strings(lib):
+    import backward_gemm_gb300 as nb
+
+    assert lib.nf4_abi_version() == 1
+    assert nb.status_string(nb.NF4_OK) == "ok"
+    assert "timed out" in nb.status_string(nb.NF4_ERR_TIMEOUT)
+    assert nb.status_string(99) == "unknown status"
+
+
+def test_host_validation_rejects_before_any_device_work(lib):
+    import backward_gemm_gb300 as nb
+
+    fake = C.c_void_p(0x100000)  # never dereferenced: every call below fails validation
+    # K not a multiple of 64, negative sizes, unknown dtype, null pointers.
+    assert lib.nf4_backward_a(fake, fake, fake, fake, 16, 64, 100, None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_backward_a(fake, fake, fake, fake, -1, 64, 128, None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_backward_a_ex(fake, 7, fake, fake, fake, 16, 64, 128, None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_backward_a(None, fake, fake, fake, 16, 64, 128, None) == nb.NF4_ERR_INVALID
+    # N not a multiple of the TMA row alignment (4 fp32 / 8 bf16 elements).
+    assert lib.nf4_backward_a(fake, fake, fake, fake, 16, 66, 128, None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_backward_a_ex(fake, nb.NF4_BF16, fake, fake, fake, 16, 68, 128,
+                                 None) == nb.NF4_ERR_INVALID
+    # Misaligned pointers.
+    odd = C.c_void_p(0x100004)
+    assert lib.nf4_backward_a(odd, fake, fake, fake, 16, 64, 128, None) == nb.NF4_ERR_ALIGN
+    assert lib.nf4_backward_a(fake, fake, fake, odd, 16, 64, 128, None) == nb.NF4_ERR_ALIGN
+    assert lib.nf4_quantize(fake, 100, 8, fake, fake, None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_dequantize_f16(fake, fake, 96, 8, fake, None) == nb.NF4_ERR_INVALID
+    # Grouped launch: a bad count or a bad problem is rejected.
+    assert lib.nf4_backward_a_batched(None, -1, None, 0, None) == nb.NF4_ERR_INVALID
+    probs = (nb.Nf4Problem * 1)(nb.Nf4Problem(0x100000, 0, 0x100000, 0x100000, 0x100000,
+                                              16, 64, 100))
+    assert lib.nf4_backward_a_batched(probs, 1, None, 0, None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_backward_a_batched_workspace(196) >= 196 * 384
+    assert lib.nf4_backward_a_batched_workspace(0) == 0
+
+
+def test_empty_problems_enqueue_nothing(lib):
+    import backward_gemm_gb300 as nb
+
+    fake = C.c_void_p(0x100000)
+    # M == 0 is a no-op that needs no valid pointers (nothing is read or written).
+    assert lib.nf4_backward_a(None, None, None, None, 0, 64, 128, None) == nb.NF4_OK
+    assert lib.nf4_backward_a_batched(None, 0, None, 0, None) == nb.NF4_OK

@@ -226,6 +226,12 @@ def test_rejects_bad_arguments_without_launching():
     assert L.nf4_backward_a(*args(go=go.data_ptr() + 4)) == nb().NF4_ERR_ALIGN
     assert L.nf4_backward_a(*args(out=out.data_ptr() + 8)) == nb().NF4_ERR_ALIGN
     assert L.nf4_backward_a(*args(go=None)) == nb().NF4_ERR_INVALID
+    # Grouped launch without (or with too small) a workspace.
+    probs = (nb().Nf4Problem * 1)(nb().Nf4Problem(go.data_ptr(), 0, w.scales.data_ptr(),
+                                                  w.data.data_ptr(), out.data_ptr(), 16, 64, 128))
+    assert L.nf4_backward_a_batched(probs, 1, None, 0, s) == nb().NF4_ERR_WORKSPACE
+    ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    assert L.nf4_backward_a_batched(probs, 1, ws.data_ptr(), 64, s) == nb().NF4_ERR_WORKSPACE
     nb().check_error()
 
 
