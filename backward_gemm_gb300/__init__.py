@@ -48,6 +48,7 @@ SIGNATURES = {
     "nf4_backward_a_batched_workspace": (_sz, [_i]),
     "nf4_backward_a_batched": (_i, [C.POINTER(Nf4Problem), _i, _vp, _sz, _vp]),
     "nf4_check_error": (_i, [_vp]),
+    "nf4_backward_a_batched_noalloc": (_i, [C.POINTER(Nf4Problem), _i, _vp]),
 }
 
 _lib = None
@@ -180,6 +181,23 @@ def backward_a_batched(items, workspace: torch.Tensor | None = None):
     _check(lib().nf4_backward_a_batched(arr, len(items), _ptr(workspace), workspace.numel(),
                                         _stream()), "nf4_backward_a_batched")
     return outs
+
+
+def backward_a_batched_noalloc(items):
+    """Grouped launch that allocates nothing on the device (descriptors kept in a
+    fixed array inside the library, at most 256 problems).  ``items`` as for
+    backward_a_batched, but every output must be given (no tensor is created)."""
+    items = list(items)
+    arr = (Nf4Problem * max(len(items), 1))()
+    for i, (go, w, out) in enumerate(items):
+        _require_cuda_contig("grad_out", go)
+        _require_cuda_contig("out", out)
+        M, N = go.shape
+        arr[i] = Nf4Problem(go.data_ptr(), _dtype_code(go), w.scales.data_ptr(), w.data.data_ptr(),
+                            out.data_ptr(), M, N, w.K)
+    _check(lib().nf4_backward_a_batched_noalloc(arr, len(items), _stream()),
+           "nf4_backward_a_batched_noalloc")
+    return [out for _, _, out in items]
 
 
 def check_error() -> None:

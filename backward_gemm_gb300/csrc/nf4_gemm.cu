@@ -826,3 +826,98 @@ extern "C" int nf4_check_error(void* stream) {
   }
   return cudaGetLastError() == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
+
+// ------------------------------------------------------------------ grouped launch without allocation
+// Some callers cannot allocate device memory for the grouped launch's
+// workspace: code that runs under a caching allocator it must not re-enter, in a
+// stream-ordered region where cudaMalloc would synchronise the device, or in a
+// process whose memory is fully reserved up front.  For them the descriptors
+// live in this file-scope device array instead.  It is reserved on every GPU
+// that loads the library, for the life of the process, and shared by every
+// call of nf4_backward_a_batched_noalloc on that GPU.
+namespace nf4 {
+constexpr int kNoAllocMaxProblems = 256;
+constexpr size_t kNoAllocBytes = kNoAllocMaxProblems * sizeof(ProblemDesc);  // 128 KiB
+static __device__ __align__(256) unsigned char g_noalloc_descs[kNoAllocBytes];
+
+// Device address of g_noalloc_descs on the current device, looked up once per
+// device.  In host code the array's name is only a host-side stand-in for the
+// symbol; cudaGetSymbolAddress gives the address a kernel may use.
+static int noalloc_descs(ProblemDesc** out) {
+  static ProblemDesc* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NF4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_descs) != cudaSuccess || p == nullptr)
+      return NF4_ERR_CUDA;
+    addr[dev] = static_cast<ProblemDesc*>(p);
+  }
+  *out = addr[dev];
+  return NF4_OK;
+}
+}  // namespace nf4
+
+extern "C" int nf4_backward_a_batched_noalloc(const nf4_problem* problems, int count,
+                                              void* stream) {
+  if (count < 0 || (count > 0 && problems == nullptr)) return NF4_ERR_INVALID;
+  if (count > kNoAllocMaxProblems) return NF4_ERR_WORKSPACE;
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    const int rc = check_problem(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
+    if (rc != NF4_OK) return rc;
+  }
+  cudaStream_t st = as_stream(stream);
+  // Problems that need the GEMM, longest tiles first (stable), as the grouped
+  // entry point orders them; no heap memory is used on the host either.
+  int order[kNoAllocMaxProblems];
+  int stages[kNoAllocMaxProblems];
+  int n = 0;
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    if (p.M == 0) continue;
+    if (p.N == 0) {
+      if (cudaMemsetAsync(p.grad_A, 0, sizeof(float) * static_cast<size_t>(p.M) * p.K, st) !=
+          cudaSuccess)
+        return NF4_ERR_CUDA;
+      continue;
+    }
+    const int ns = (p.N + BN - 1) / BN;
+    int j = n++;
+    while (j > 0 && stages[j - 1] < ns) {
+      order[j] = order[j - 1];
+      stages[j] = stages[j - 1];
+      --j;
+    }
+    order[j] = i;
+    stages[j] = ns;
+  }
+  if (n == 0) return NF4_OK;
+  ProblemDesc* ws = nullptr;
+  int rc = noalloc_descs(&ws);
+  if (rc != NF4_OK) return rc;
+  // Every descriptor the GEMM reads is written here, in stream order before it,
+  // so nothing left in the array by an earlier call is ever used.
+  DescChunk chunk;
+  int64_t total = 0;
+  for (int i = 0; i < n; i += kDescsPerUpload) {
+    const int m = std::min(kDescsPerUpload, n - i);
+    std::memset(&chunk, 0, sizeof(chunk));
+    for (int j = 0; j < m; ++j) {
+      const nf4_problem& p = problems[order[i + j]];
+      ProblemDesc& d = chunk.d[j];
+      rc = fill_desc(&d, p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
+      if (rc != NF4_OK) return rc;
+      d.tile_begin = static_cast<int>(total);
+      total += static_cast<int64_t>(d.tiles_m) * d.tiles_k;
+      if (total > INT_MAX) return NF4_ERR_INVALID;
+    }
+    upload_descs_kernel<<<1, 256, 0, st>>>(chunk, ws + i, m);
+    if (cudaGetLastError() != cudaSuccess) return NF4_ERR_CUDA;
+  }
+  ProblemDesc unused;
+  std::memset(&unused, 0, sizeof(unused));
+  return launch(unused, ws, n, static_cast<int>(total), st);
+}

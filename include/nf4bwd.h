@@ -134,6 +134,32 @@ int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspa
                            size_t workspace_bytes, void* stream);
 
 /*
+ * Grouped backward-A that allocates nothing.  The pages have no counterpart of
+ * this entry point: it exists for callers that cannot allocate device memory
+ * for the workspace of nf4_backward_a_batched -- code running inside a caching
+ * allocator it must not re-enter, inside a stream-ordered region where
+ * cudaMalloc would synchronise the device, or in a process whose device memory
+ * is all reserved up front.
+ *
+ * Same problems, rules and results as nf4_backward_a_batched, but the
+ * per-problem descriptors go to a fixed array inside the library (a
+ * file-scope device array of 128 KiB, reserved on every GPU that loads the
+ * library until the process exits), so the call takes no workspace.
+ *   count      at most 256 problems; more returns NF4_ERR_WORKSPACE and
+ *              enqueues nothing
+ *   set-up     the first call on a device looks up the array's device address
+ *              (cudaGetSymbolAddress) with that device current; make that first
+ *              call before any stream capture
+ *   sharing    every call on a device uses the same array, which keeps the last
+ *              call's descriptors; each call rewrites every descriptor its
+ *              kernel reads before the kernel runs, so nothing needs clearing,
+ *              but calls that overlap on the GPU (different streams, no ordering
+ *              between them) race on the array and must be serialised
+ * It calls no cudaMalloc or cudaFree and uses no heap memory on the host.
+ */
+int nf4_backward_a_batched_noalloc(const nf4_problem* problems, int count, void* stream);
+
+/*
  * Synchronise `stream`, then report and clear the library's device status word
  * (NF4_ERR_TIMEOUT if any kernel's bounded wait gave up since the last check),
  * or NF4_ERR_CUDA if the stream reports a CUDA error.
