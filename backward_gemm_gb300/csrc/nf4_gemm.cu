@@ -24,7 +24,9 @@
 //               i % 3, so a group can start as soon as MMA i-3 is done
 //   warp 5      allocates 512 TMEM columns in both CTAs; in CTA 0 one thread
 //               issues the pair MMAs into a double-buffered fp32 accumulator
-//               (2 x 256 columns) and commits to barriers of both CTAs
+//               (2 x 256 columns) and commits to barriers of both CTAs; in CTA 1
+//               one thread relays the converters' per-stage completion to CTA 0
+//               with a single cluster-scope arrive
 //   warps 0-3   epilogue (each CTA): tcgen05.ld of a 32-lane quarter, staged
 //               through shared memory and written with TMA stores, which clip
 //               rows >= M and columns >= K; overlaps the next tile's main loop
@@ -82,7 +84,7 @@ constexpr int kRawOff = 0;
 constexpr int kOpOff = kRawOff + kRawStages * kRawBytes;
 constexpr int kEpiOff = kOpOff + kOpStages * kOpBytes;
 constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
-constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 + 2 + 1;
+constexpr int kNumBars = 2 * kRawStages + 3 * kOpStages + 2 + 2 + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 2 * BK;
@@ -233,6 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 2 + i);
   };
   const uint32_t mma_done = bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 4);
+  // CTA 1 only: its converters' arrivals per operand slot, relayed to CTA 0.
+  auto conv_done = [&](uint32_t i) { return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -245,8 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_raw(i), kGroupWarps);
     }
     for (int i = 0; i < kOpStages; ++i) {
-      mbar_init(full_op(i), 2 * kGroupWarps);  // converters of both CTAs (used in CTA 0)
+      mbar_init(full_op(i), kGroupWarps + 1);  // CTA 0's converters + CTA 1's relay
       mbar_init(empty_op(i), 1);
+      mbar_init(conv_done(i), kGroupWarps);    // CTA 1's converters
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tmem_full(i), 1);
@@ -358,6 +363,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t l = (lt > 2 ? lt - 2 : 0u); l < lt; ++l)
           mbar_wait_cluster(tmem_empty(l & 1u), (l >> 1) & 1u, nullptr);
       }
+    } else if (rank == 1 && lane == 0) {
+      // Relay: one cluster-scope arrival on CTA 0's operand barrier per stage,
+      // once all of this CTA's converters of that stage have arrived locally.
+      const uint32_t full_op_leader0 = mapa_shared(full_op(0), 0);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = cluster; ok && t < total_tiles; t += nclusters) {
+        const Tile tl = tile_at(descs, count, t);
+        for (int s = 0; s < tl.ns; ++s, ++it) {
+          const uint32_t slot = it % kOpStages;
+          if (!mbar_wait(conv_done(slot), (it / kOpStages) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(full_op_leader0 + 8u * slot);
+        }
+      }
     }
     __syncwarp();
   } else if (warp >= kConvWarp0) {
@@ -373,7 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t aswz = static_cast<uint32_t>(ar & 7);
     const uint32_t bswz = static_cast<uint32_t>(bn & 7);
     const uint32_t qchunk = ((2u * bj + bh) ^ ((static_cast<uint32_t>(bn) >> 1) & 3u)) << 4;
-    const uint32_t full_op_leader0 = mapa_shared(full_op(0), 0);
 
     // `nxt` runs two stages (one group turn) ahead of the stage being converted,
     // so the block scale it needs is loaded a whole turn before its use.
@@ -464,10 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        if (rank == 0) mbar_arrive(full_op(oslot));
-        else mbar_arrive_remote(full_op_leader0 + 8u * oslot);
-      }
+      if (lane == 0) mbar_arrive(rank == 0 ? full_op(oslot) : conv_done(oslot));
       if (probe) NF4_PROBE(16 + cw, it);
       it += kConvGroups;
     }

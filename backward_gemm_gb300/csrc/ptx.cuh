@@ -124,12 +124,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared).
-// Default (release, CTA-scope) semantics: what the arrival publishes is this
-// CTA's own shared memory, already handed to the async proxy by
-// fence.proxy.async; a cluster-scope release costs thousands of cycles here.
+// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared),
+// releasing at cluster scope what this thread has observed.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
