@@ -25,8 +25,8 @@
 //   warp 5      allocates 512 TMEM columns in both CTAs; in CTA 0 one thread
 //               issues the pair MMAs into a double-buffered fp32 accumulator
 //               (2 x 256 columns) and commits to barriers of both CTAs; in CTA 1
-//               one thread relays the converters' per-stage completion to CTA 0
-//               with a single cluster-scope arrive
+//               one thread signals each converted stage to CTA 0 with a 16-byte
+//               bulk copy that completes on CTA 0's operand barrier
 //   warps 0-3   epilogue (each CTA): tcgen05.ld of a 32-lane quarter, staged
 //               through shared memory and written with TMA stores, which clip
 //               rows >= M and columns >= K; overlaps the next tile's main loop
@@ -86,7 +86,11 @@ constexpr int kEpiOff = kOpOff + kOpStages * kOpBytes;
 constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
 constexpr int kNumBars = 2 * kRawStages + 3 * kOpStages + 2 + 2 + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
+// misc: TMEM address, abort flag, then 16-byte signal words (one per operand
+// slot as destinations in CTA 0, one source in CTA 1)
+constexpr int kSigOff = kMiscOff + 16;
+constexpr uint32_t kSigBytes = 16;
+constexpr int kSmemBytes = kSigOff + (kOpStages + 1) * kSigBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 2 * BK;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -249,7 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_raw(i), kGroupWarps);
     }
     for (int i = 0; i < kOpStages; ++i) {
-      mbar_init(full_op(i), kGroupWarps + 1);  // CTA 0's converters + CTA 1's relay
+      // CTA 0's converters + the kSigBytes of CTA 1's completion copy, which
+      // are registered before they can arrive: here for each slot's first
+      // phase, by the MMA thread for every later one.
+      mbar_init(full_op(i), kGroupWarps);
       mbar_init(empty_op(i), 1);
       mbar_init(conv_done(i), kGroupWarps);    // CTA 1's converters
     }
@@ -258,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tmem_empty(i), 2 * kEpiWarps);  // epilogues of both CTAs (used in CTA 0)
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < kOpStages; ++i) mbar_expect_tx(full_op(i), kSigBytes);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -337,6 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // The slot's next phase (stage it + 3) expects CTA 1's signal bytes; it
+          // cannot be sent before the MMAs below complete.
+          mbar_expect_tx(full_op(slot), kSigBytes);
           tc_fence_after();
           NF4_PROBE(33, it);
           const uint32_t a_addr = sbase + kOpOff + slot * kOpBytes;
@@ -364,9 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_cluster(tmem_empty(l & 1u), (l >> 1) & 1u, nullptr);
       }
     } else if (rank == 1 && lane == 0) {
-      // Relay: one cluster-scope arrival on CTA 0's operand barrier per stage,
-      // once all of this CTA's converters of that stage have arrived locally.
+      // Relay: once all of this CTA's converters of a stage have arrived
+      // locally, a 16-byte bulk copy into CTA 0 completes (in bytes) on CTA 0's
+      // operand barrier of that stage.  The copy is asynchronous: this thread
+      // never waits for it, and CTA 0 cannot see the stage complete before the
+      // copy (issued after this CTA's operands were written) has landed.
       const uint32_t full_op_leader0 = mapa_shared(full_op(0), 0);
+      const uint32_t sig_leader0 = mapa_shared(sbase + kSigOff, 0);
+      const uint32_t sig_src = sbase + kSigOff + kOpStages * kSigBytes;
       uint32_t it = 0;
       bool ok = true;
       for (int t = cluster; ok && t < total_tiles; t += nclusters) {
@@ -377,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_remote(full_op_leader0 + 8u * slot);
+          bulk_copy_to_peer(sig_leader0 + slot * kSigBytes, sig_src, kSigBytes,
+                            full_op_leader0 + 8u * slot);
         }
       }
     }
