@@ -253,9 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_raw(i), kGroupWarps);
     }
     for (int i = 0; i < kOpStages; ++i) {
-      // CTA 0's converters + the kSigBytes of CTA 1's completion copy, which
-      // are registered before they can arrive: here for each slot's first
-      // phase, by the MMA thread for every later one.
+      // CTA 0's converters, one of which registers the kSigBytes of CTA 1's
+      // completion copy with its arrival (the copy may land before or after
+      // that arrival; the phase completes only when both are in).
       mbar_init(full_op(i), kGroupWarps);
       mbar_init(empty_op(i), 1);
       mbar_init(conv_done(i), kGroupWarps);    // CTA 1's converters
@@ -265,7 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tmem_empty(i), 2 * kEpiWarps);  // epilogues of both CTAs (used in CTA 0)
     }
     mbar_init(mma_done, 1);
-    for (int i = 0; i < kOpStages; ++i) mbar_expect_tx(full_op(i), kSigBytes);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -345,9 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // The slot's next phase (stage it + 3) expects CTA 1's signal bytes; it
-          // cannot be sent before the MMAs below complete.
-          mbar_expect_tx(full_op(slot), kSigBytes);
           tc_fence_after();
           NF4_PROBE(33, it);
           const uint32_t a_addr = sbase + kOpOff + slot * kOpBytes;
@@ -502,7 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(rank == 0 ? full_op(oslot) : conv_done(oslot));
+      if (lane == 0) {
+        if (rank == 1) mbar_arrive(conv_done(oslot));
+        else if ((cg_thread >> 5) % kGroupWarps == 0) mbar_arrive_expect_tx(full_op(oslot), kSigBytes);
+        else mbar_arrive(full_op(oslot));
+      }
       if (probe) NF4_PROBE(16 + cw, it);
       it += kConvGroups;
     }
