@@ -454,6 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           g[i] = *reinterpret_cast<const uint4*>(src + (((4u * ahalf + i) ^ aswz) << 4));
       }
       const uint4 q = *reinterpret_cast<const uint4*>(raw + kGoBytes + bn * (BKC / 2) + qchunk);
+      // The slot is refilled by TMA (async proxy) once released: order these
+      // generic-proxy reads before that write.
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_raw(rslot));
 
