@@ -24,9 +24,9 @@
 //               i % 3, so a group can start as soon as MMA i-3 is done
 //   warp 5      allocates 512 TMEM columns in both CTAs; in CTA 0 one thread
 //               issues the pair MMAs into a double-buffered fp32 accumulator
-//               (2 x 256 columns) and commits to barriers of both CTAs; in CTA 1
-//               one thread signals each converted stage to CTA 0 with a 16-byte
-//               bulk copy that completes on CTA 0's operand barrier
+//               (2 x 256 columns) and commits to barriers of both CTAs.  CTA 1's
+//               converter warps signal a finished stage to CTA 0 with 16-byte
+//               bulk copies that complete on CTA 0's operand barrier
 //   warps 0-3   epilogue (each CTA): tcgen05.ld of a 32-lane quarter, staged
 //               through shared memory and written with TMA stores, which clip
 //               rows >= M and columns >= K; overlaps the next tile's main loop
@@ -84,13 +84,14 @@ constexpr int kRawOff = 0;
 constexpr int kOpOff = kRawOff + kRawStages * kRawBytes;
 constexpr int kEpiOff = kOpOff + kOpStages * kOpBytes;
 constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
-constexpr int kNumBars = 2 * kRawStages + 3 * kOpStages + 2 + 2 + 1;
+constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 + 2 + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
-// misc: TMEM address, abort flag, then 16-byte signal words (one per operand
-// slot as destinations in CTA 0, one source in CTA 1)
+// misc: TMEM address, abort flag, then the 16-byte signal words: in CTA 0 one
+// destination per (operand slot, converter warp of a group), and one source.
 constexpr int kSigOff = kMiscOff + 16;
 constexpr uint32_t kSigBytes = 16;
-constexpr int kSmemBytes = kSigOff + (kOpStages + 1) * kSigBytes + 1024;  // + alignment slack
+constexpr uint32_t kSigSrcOff = kSigOff + kOpStages * kGroupWarps * kSigBytes;
+constexpr int kSmemBytes = kSigSrcOff + kSigBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 2 * BK;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -239,8 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 2 + i);
   };
   const uint32_t mma_done = bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 4);
-  // CTA 1 only: its converters' arrivals per operand slot, relayed to CTA 0.
-  auto conv_done = [&](uint32_t i) { return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -253,12 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_raw(i), kGroupWarps);
     }
     for (int i = 0; i < kOpStages; ++i) {
-      // CTA 0's converters, one of which registers the kSigBytes of CTA 1's
-      // completion copy with its arrival (the copy may land before or after
-      // that arrival; the phase completes only when both are in).
+      // CTA 0's converters, one of which registers with its arrival the bytes
+      // of the completion copies of CTA 1's converters (one 16-byte copy per
+      // warp; they may land before or after that arrival: the phase completes
+      // only when all arrivals and all bytes are in).
       mbar_init(full_op(i), kGroupWarps);
       mbar_init(empty_op(i), 1);
-      mbar_init(conv_done(i), kGroupWarps);    // CTA 1's converters
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tmem_full(i), 1);
@@ -370,29 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t l = (lt > 2 ? lt - 2 : 0u); l < lt; ++l)
           mbar_wait_cluster(tmem_empty(l & 1u), (l >> 1) & 1u, nullptr);
       }
-    } else if (rank == 1 && lane == 0) {
-      // Relay: once all of this CTA's converters of a stage have arrived
-      // locally, a 16-byte bulk copy into CTA 0 completes (in bytes) on CTA 0's
-      // operand barrier of that stage.  The copy is asynchronous: this thread
-      // never waits for it, and CTA 0 cannot see the stage complete before the
-      // copy (issued after this CTA's operands were written) has landed.
-      const uint32_t full_op_leader0 = mapa_shared(full_op(0), 0);
-      const uint32_t sig_leader0 = mapa_shared(sbase + kSigOff, 0);
-      const uint32_t sig_src = sbase + kSigOff + kOpStages * kSigBytes;
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = cluster; ok && t < total_tiles; t += nclusters) {
-        const Tile tl = tile_at(descs, count, t);
-        for (int s = 0; s < tl.ns; ++s, ++it) {
-          const uint32_t slot = it % kOpStages;
-          if (!mbar_wait(conv_done(slot), (it / kOpStages) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          bulk_copy_to_peer(sig_leader0 + slot * kSigBytes, sig_src, kSigBytes,
-                            full_op_leader0 + 8u * slot);
-        }
-      }
     }
     __syncwarp();
   } else if (warp >= kConvWarp0) {
@@ -408,6 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t aswz = static_cast<uint32_t>(ar & 7);
     const uint32_t bswz = static_cast<uint32_t>(bn & 7);
     const uint32_t qchunk = ((2u * bj + bh) ^ ((static_cast<uint32_t>(bn) >> 1) & 3u)) << 4;
+    // CTA 1: where this warp's stage-completion copy goes in CTA 0.
+    const uint32_t gw = static_cast<uint32_t>(ct >> 5);  // warp within the group
+    const uint32_t full_op_leader0 = mapa_shared(full_op(0), 0);
+    const uint32_t sig_leader0 = mapa_shared(sbase + kSigOff + gw * kSigBytes, 0);
 
     // `nxt` runs two stages (one group turn) ahead of the stage being converted,
     // so the block scale it needs is loaded a whole turn before its use.
@@ -502,9 +482,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        if (rank == 1) mbar_arrive(conv_done(oslot));
-        else if ((cg_thread >> 5) % kGroupWarps == 0) mbar_arrive_expect_tx(full_op(oslot), kSigBytes);
-        else mbar_arrive(full_op(oslot));
+        if (rank == 1) {
+          // A 16-byte copy into CTA 0 that completes on CTA 0's operand barrier;
+          // issued after this warp's operand writes were handed to the async
+          // proxy, never waited for here.
+          bulk_copy_to_peer(sig_leader0 + oslot * kGroupWarps * kSigBytes, sbase + kSigSrcOff,
+                            kSigBytes, full_op_leader0 + 8u * oslot);
+        } else if (gw == 0) {
+          mbar_arrive_expect_tx(full_op(oslot), kGroupWarps * kSigBytes);
+        } else {
+          mbar_arrive(full_op(oslot));
+        }
       }
       if (probe) NF4_PROBE(16 + cw, it);
       it += kConvGroups;
