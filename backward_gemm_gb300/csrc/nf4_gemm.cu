@@ -85,7 +85,7 @@ constexpr int kOpOff = kRawOff + kRawStages * kRawBytes;
 constexpr int kEpiOff = kOpOff + kOpStages * kOpBytes;
 constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
 constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 + 2 + 1;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;  // 16-byte aligned (bulk copies)
 // misc: TMEM address, abort flag, then the 16-byte signal words: in CTA 0 one
 // destination per (operand slot, converter warp of a group), and one source.
 constexpr int kSigOff = kMiscOff + 16;
@@ -95,6 +95,7 @@ constexpr int kSmemBytes = kSigSrcOff + kSigBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 2 * BK;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
 static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
