@@ -27,6 +27,8 @@
 //               (2 x 256 columns) and commits to barriers of both CTAs.  CTA 1's
 //               converter warps signal a finished stage to CTA 0 with 16-byte
 //               bulk copies that complete on CTA 0's operand barrier
+//   warp 22     CTA 0: waits on the operand barriers and publishes each ready
+//               stage in a shared-memory word the MMA thread polls
 //   warps 0-3   epilogue (each CTA): tcgen05.ld of a 32-lane quarter, staged
 //               through shared memory and written with TMA stores, which clip
 //               rows >= M and columns >= K; overlaps the next tile's main loop
@@ -68,7 +70,8 @@ constexpr int kConvWarp0 = 6;
 constexpr int kConvGroups = 2;   // group g converts the stages it with it % 2 == g
 constexpr int kGroupWarps = 8;   // warps per group (256 threads)
 constexpr int kConvWarps = kConvGroups * kGroupWarps;
-constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;  // 704
+constexpr int kWatchWarp = kConvWarp0 + kConvWarps;       // 22
+constexpr int kThreads = (kWatchWarp + 1) * 32;           // 736
 
 constexpr int kRawStages = 3;
 constexpr int kOpStages = 3;
@@ -86,9 +89,11 @@ constexpr int kEpiOff = kOpOff + kOpStages * kOpBytes;
 constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
 constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 + 2 + 1;
 constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;  // 16-byte aligned (bulk copies)
-// misc: TMEM address, abort flag, then the 16-byte signal words: in CTA 0 one
-// destination per (operand slot, converter warp of a group), and one source.
-constexpr int kSigOff = kMiscOff + 16;
+// misc: TMEM address, abort flag, one ready word per operand slot, then the
+// 16-byte signal words: in CTA 0 one destination per (operand slot, converter
+// warp of a group), and one source.
+constexpr int kReadyOff = kMiscOff + 8;
+constexpr int kSigOff = kMiscOff + 32;
 constexpr uint32_t kSigBytes = 16;
 constexpr uint32_t kSigSrcOff = kSigOff + kOpStages * kGroupWarps * kSigBytes;
 constexpr int kSmemBytes = kSigSrcOff + kSigBytes + 1024;  // + alignment slack
@@ -96,6 +101,7 @@ constexpr uint32_t kTmemCols = 2 * BK;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
+static_assert(kReadyOff + 4 * kOpStages <= kSigOff, "ready words fit before the signal area");
 static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
@@ -265,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tmem_empty(i), 2 * kEpiWarps);  // epilogues of both CTAs (used in CTA 0)
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < kOpStages; ++i)
+      reinterpret_cast<volatile uint32_t*>(smem + kReadyOff)[i] = 0u;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -340,7 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < tl.ns; ++s, ++it) {
           const uint32_t slot = it % kOpStages;
           NF4_PROBE(32, it);
-          if (!mbar_wait_cluster(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
+          // The watcher warp has seen stage `it`'s operand barrier complete
+          // when it publishes it + 1 in the slot's ready word.
+          if (!flag_wait(sbase + kReadyOff + 4u * slot, it + 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -369,6 +379,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         for (uint32_t l = (lt > 2 ? lt - 2 : 0u); l < lt; ++l)
           mbar_wait_cluster(tmem_empty(l & 1u), (l >> 1) & 1u, nullptr);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWatchWarp) {
+    // ---------------------------------------------------------------- watcher (CTA 0)
+    // Absorbs the latency of the operand-barrier waits for the MMA thread: it
+    // runs up to kOpStages stages ahead (the converters cannot fill a slot again
+    // before its MMAs complete) and publishes each completed stage.
+    if (rank == 0 && lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = cluster; ok && t < total_tiles; t += nclusters) {
+        const Tile tl = tile_at(descs, count, t);
+        for (int s = 0; s < tl.ns; ++s, ++it) {
+          const uint32_t slot = it % kOpStages;
+          if (!mbar_wait_cluster(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          st_release_shared(sbase + kReadyOff + 4u * slot, it + 1u);
+        }
       }
     }
     __syncwarp();

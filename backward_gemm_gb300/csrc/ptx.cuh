@@ -149,6 +149,34 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Shared-memory flag word written by one thread and polled by another.
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Spin until the flag word equals `want`; bounded like mbar_wait.
+__device__ __forceinline__ bool flag_wait(uint32_t addr, uint32_t want, volatile int* abort_flag) {
+  if (ld_acquire_shared(addr) == want) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (ld_acquire_shared(addr) == want) return true;
+    if (abort_flag != nullptr && *abort_flag != 0) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicExch(&g_status, kStatusTimeout);
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- proxies
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor-core operand reads, TMA).
