@@ -333,8 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer (CTA 0)
     if (rank == 0 && lane == 0) {
+      // This thread shares its SM sub-partition with busy converter warps and
+      // is on the critical path: per stage it only polls the ready word,
+      // issues 4 MMAs and commits.  Descriptors of slot 0 are built once; a
+      // slot's are those plus its offset in the 16-byte address field.
       constexpr uint32_t idesc = idesc_f16_f32(BMP, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
-      uint32_t it = 0, lt = 0;
+      const uint64_t a_desc0 = smem_desc_sw128(sbase + kOpOff, 16, kSbo);
+      const uint64_t b_desc0 = smem_desc_sw128(sbase + kOpOff + kABytes, kBLbo, kSbo);
+      constexpr uint32_t kBStep = (2u * kSbo) >> 4;  // +2 n-groups per MMA K-step
+      const uint32_t ready0 = sbase + kReadyOff;
+      uint32_t it = 0, lt = 0, slot = 0;
       bool ok = true;
       for (int t = cluster; ok && t < total_tiles; t += nclusters, ++lt) {
         const Tile tl = tile_at(descs, count, t);
@@ -345,28 +353,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BK;
-        for (int s = 0; s < tl.ns; ++s, ++it) {
-          const uint32_t slot = it % kOpStages;
+        for (int s = 0; s < tl.ns; ++s) {
           NF4_PROBE(32, it);
           // The watcher warp has seen stage `it`'s operand barrier complete
           // when it publishes it + 1 in the slot's ready word.
-          if (!flag_wait(sbase + kReadyOff + 4u * slot, it + 1u, abort_flag)) {
+          if (!flag_wait(ready0 + 4u * slot, it + 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           NF4_PROBE(33, it);
-          const uint32_t a_addr = sbase + kOpOff + slot * kOpBytes;
-          const uint64_t a_desc = smem_desc_sw128(a_addr, 16, kSbo);
-          const uint64_t b_desc = smem_desc_sw128(a_addr + kABytes, kBLbo, kSbo);
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
-            tc_mma_f16_pair(d_tmem, a_desc + 2u * kk, b_desc + (2u * kSbo >> 4) * kk, idesc,
-                            (s | kk) != 0 ? 1u : 0u);
-          }
+          const uint64_t off = static_cast<uint64_t>((slot * kOpBytes) >> 4);
+          const uint64_t a = a_desc0 + off, b = b_desc0 + off;
+          // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
+          tc_mma_f16_pair(d_tmem, a, b, idesc, s != 0 ? 1u : 0u);
+          tc_mma_f16_pair(d_tmem, a + 2u, b + kBStep, idesc, 1u);
+          tc_mma_f16_pair(d_tmem, a + 4u, b + 2u * kBStep, idesc, 1u);
+          tc_mma_f16_pair(d_tmem, a + 6u, b + 3u * kBStep, idesc, 1u);
           tc_commit_pair(empty_op(slot), 0x3);
           NF4_PROBE(38, it);
+          ++it;
+          slot = (slot + 1u == static_cast<uint32_t>(kOpStages)) ? 0u : slot + 1u;
         }
         if (!ok) break;
         tc_commit_pair(tmem_full(acc), 0x3);
@@ -398,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          NF4_PROBE(31, it);
           st_release_shared(sbase + kReadyOff + 4u * slot, it + 1u);
         }
       }
