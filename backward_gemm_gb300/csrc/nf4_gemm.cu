@@ -361,7 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          tc_fence_after();
+          // No tcgen05 fence here: the operands were handed to the async proxy
+          // by their writers (fence.proxy.async before the barrier arrive) and
+          // this thread acquired the barrier's completion through the ready
+          // word; a tcgen05.fence per stage would keep the MMAs of consecutive
+          // stages from overlapping.
           NF4_PROBE(33, it);
           const uint64_t off = static_cast<uint64_t>((slot * kOpBytes) >> 4);
           const uint64_t a = a_desc0 + off, b = b_desc0 + off;
