@@ -458,10 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t oslot = it % kOpStages;
       const bool probe = (lane == 0);
       const int cw = cg_thread >> 5;  // converter warp 0..15
+      if (probe && cw % kGroupWarps == 0) NF4_PROBE(29, it);
       // All lanes wait; the warp goes on only if every lane saw the phase
       // complete, so a timeout never leaves the warp divergent.
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_raw(rslot), (it / kRawStages) & 1u, abort_flag)))
         break;
+      if (probe && (cg_thread >> 5) % kGroupWarps == 0) NF4_PROBE(28, it);
 
       // Raw inputs of this thread -> registers; then the raw slot is released.
       const uint8_t* raw = smem + kRawOff + rslot * kRawBytes;
