@@ -208,10 +208,14 @@ __device__ __forceinline__ float cc_scale(const ConvCursor& c, uint32_t rank, in
 // the two CTAs of cluster 0 record clock64() at fixed points of each role into
 // a device buffer [cta][event][slot]; event kTraceEvents-1 slot 0 is the clock
 // right after the start-up cluster barrier, the common reference of both CTAs.
+// Events: 0-15 converter warp after its operand-slot wait, 16-31 converter warp
+// done, 32/33/38 MMA before wait / after wait / after commit, 35/36 epilogue
+// tile start / end, 39 reference, 40 producer issue, 41 watcher sees stage,
+// 42 converter group leader sees raw data, 43 converter group leader starts.
 #ifdef NF4_TRACE
 __device__ unsigned long long* g_trace = nullptr;
 constexpr int kTraceSlots = 512;
-constexpr int kTraceEvents = 40;
+constexpr int kTraceEvents = 48;
 #define NF4_PROBE(ev, idx)                                                               \
   do {                                                                                   \
     if (blockIdx.x < 2 && g_trace != nullptr && (idx) < kTraceSlots)                     \
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          NF4_PROBE(30, it);
+          NF4_PROBE(40, it);
           const uint32_t fb = full_raw(slot);
           mbar_arrive_expect_tx(fb, bytes);
           const uint32_t dst = sbase + kRawOff + slot * kRawBytes;
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          NF4_PROBE(31, it);
+          NF4_PROBE(41, it);
           st_release_shared(sbase + kReadyOff + 4u * slot, it + 1u);
         }
       }
@@ -458,12 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t oslot = it % kOpStages;
       const bool probe = (lane == 0);
       const int cw = cg_thread >> 5;  // converter warp 0..15
-      if (probe && cw % kGroupWarps == 0) NF4_PROBE(29, it);
+      if (probe && cw % kGroupWarps == 0) NF4_PROBE(43, it);
       // All lanes wait; the warp goes on only if every lane saw the phase
       // complete, so a timeout never leaves the warp divergent.
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_raw(rslot), (it / kRawStages) & 1u, abort_flag)))
         break;
-      if (probe && (cg_thread >> 5) % kGroupWarps == 0) NF4_PROBE(28, it);
+      if (probe && (cg_thread >> 5) % kGroupWarps == 0) NF4_PROBE(42, it);
 
       // Raw inputs of this thread -> registers; then the raw slot is released.
       const uint8_t* raw = smem + kRawOff + rslot * kRawBytes;
