@@ -73,36 +73,45 @@ constexpr int kConvWarps = kConvGroups * kGroupWarps;
 constexpr int kWatchWarp = kConvWarp0 + kConvWarps;       // 22
 constexpr int kThreads = (kWatchWarp + 1) * 32;           // 736
 
-constexpr int kRawStages = 3;
-constexpr int kOpStages = 3;
 constexpr int kGoBoxBytes = BM * 128;                  // one 128-byte-wide box of 128 rows
-constexpr int kGoBytes = 2 * kGoBoxBytes;              // fp32: 64 columns = two boxes
 constexpr int kNf4Bytes = BN * (BKC / 2);              // 64 rows n x 64 bytes
-constexpr int kRawBytes = kGoBytes + kNf4Bytes;        // 36 KB
 constexpr int kABytes = BM * BN * 2;                   // 16 KB f16
 constexpr int kBBytes = BKC * BN * 2;                  // 16 KB f16
 constexpr int kOpBytes = kABytes + kBBytes;            // 32 KB
 constexpr int kEpiBufBytes = 32 * 128;                 // 32 rows x 32 fp32
-constexpr int kRawOff = 0;
-constexpr int kOpOff = kRawOff + kRawStages * kRawBytes;
-constexpr int kEpiOff = kOpOff + kOpStages * kOpBytes;
-constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
-constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 + 2 + 1;
-constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;  // 16-byte aligned (bulk copies)
-// misc: TMEM address, abort flag, one ready word per operand slot, then the
-// 16-byte signal words: in CTA 0 one destination per (operand slot, converter
-// warp of a group), and one source.
-constexpr int kReadyOff = kMiscOff + 8;
-constexpr int kSigOff = kMiscOff + 32;
 constexpr uint32_t kSigBytes = 16;
-constexpr uint32_t kSigSrcOff = kSigOff + kOpStages * kGroupWarps * kSigBytes;
-constexpr int kSmemBytes = kSigSrcOff + kSigBytes + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 2 * BK;
 
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
-static_assert(kReadyOff + 4 * kOpStages <= kSigOff, "ready words fit before the signal area");
-static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
+// Shared-memory layout of one kernel configuration: RS raw stages holding GOB
+// bytes of grad_out and the NF4 bytes, OS operand stages, the epilogue staging,
+// barriers and flags.  bf16 grad_out needs half the raw bytes of fp32, which
+// buys a deeper ring on both sides.
+template <int RS, int OS, int GOB>
+struct Layout {
+  static constexpr int kRawStages = RS;
+  static constexpr int kOpStages = OS;
+  static constexpr int kGoBytes = GOB;
+  static constexpr int kRawBytes = GOB + kNf4Bytes;
+  static constexpr int kRawOff = 0;
+  static constexpr int kOpOff = kRawOff + RS * kRawBytes;
+  static constexpr int kEpiOff = kOpOff + OS * kOpBytes;
+  static constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
+  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1;
+  // misc: TMEM address, abort flag, one ready word per operand slot, then the
+  // 16-byte signal words: in CTA 0 one destination per (operand slot,
+  // converter warp of a group), and one source.
+  static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
+  static constexpr int kReadyOff = kMiscOff + 8;
+  static constexpr int kSigOff = kMiscOff + 32;
+  static constexpr uint32_t kSigSrcOff = kSigOff + OS * kGroupWarps * kSigBytes;
+  static constexpr int kSmemBytes = kSigSrcOff + kSigBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
+  static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
+  static_assert(kReadyOff + 4 * OS <= kSigOff, "ready words fit before the signal area");
+};
+using LayoutF32 = Layout<3, 3, 2 * kGoBoxBytes>;  // any fp32 grad_out in the launch
+using LayoutBF16 = Layout<4, 4, kGoBoxBytes>;     // bf16 grad_out only
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
 // 8 rows n per 1024-byte atom; atoms along k are kBLbo apart, atoms along n 1 KB.
@@ -227,9 +236,22 @@ constexpr int kTraceEvents = 48;
 #endif
 
 // ------------------------------------------------------------------ kernel
+template <class L>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_a_kernel(const __grid_constant__ ProblemDesc single, const ProblemDesc* __restrict__ batch,
                  int count, int total_tiles) {
+  constexpr int kRawStages = L::kRawStages;
+  constexpr int kOpStages = L::kOpStages;
+  constexpr int kGoBytes = L::kGoBytes;
+  constexpr int kRawBytes = L::kRawBytes;
+  constexpr int kRawOff = L::kRawOff;
+  constexpr int kOpOff = L::kOpOff;
+  constexpr int kEpiOff = L::kEpiOff;
+  constexpr int kBarOff = L::kBarOff;
+  constexpr int kMiscOff = L::kMiscOff;
+  constexpr int kReadyOff = L::kReadyOff;
+  constexpr int kSigOff = L::kSigOff;
+  constexpr uint32_t kSigSrcOff = L::kSigSrcOff;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // Pointer arithmetic on the shared array keeps the shared address space
   // visible to the compiler, so plain loads and stores below are ld/st.shared.
@@ -303,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = cluster; ok && t < total_tiles; t += nclusters) {
         const Tile tl = tile_at(descs, count, t);
         const bool f32 = tl.dtype == NF4_F32;
-        const uint32_t bytes = (f32 ? kGoBytes : kGoBoxBytes) + kNf4Bytes;
+        const uint32_t bytes = (f32 ? 2 * kGoBoxBytes : kGoBoxBytes) + kNf4Bytes;
         const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
         const int x_nf4 = tl.kt * (BK / 2) + static_cast<int>(rank) * (BKC / 2);
         for (int s = 0; s < tl.ns; ++s, ++it) {
@@ -700,21 +722,18 @@ static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* sca
   return NF4_OK;
 }
 
-struct DeviceInfo {
-  int max_clusters = 0;  // pairs of CTAs that fit on the device at once
-  bool ready = false;
-};
-
-static int device_info(DeviceInfo** out) {
-  static DeviceInfo infos[64];
+// Largest number of pairs of CTAs of kernel configuration L that fit on the
+// current device at once (also sets the kernel's shared-memory limit).
+template <class L>
+static int max_clusters(int* out) {
+  static int cached[64] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NF4_ERR_CUDA;
   std::lock_guard<std::mutex> lock(mu);
-  DeviceInfo& di = infos[dev];
-  if (!di.ready) {
-    if (cudaFuncSetAttribute(bwd_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
+  if (cached[dev] == 0) {
+    if (cudaFuncSetAttribute(bwd_a_kernel<L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmemBytes) != cudaSuccess)
       return NF4_ERR_CUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -727,26 +746,26 @@ static int device_info(DeviceInfo** out) {
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = L::kSmemBytes;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, bwd_a_kernel, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&clusters, bwd_a_kernel<L>, &cfg) != cudaSuccess ||
         clusters <= 0)
       clusters = sms / 2;
-    di.max_clusters = clusters;
-    di.ready = true;
+    cached[dev] = clusters;
   }
-  *out = &di;
+  *out = cached[dev];
   return NF4_OK;
 }
 
-static int launch(const ProblemDesc& single, const ProblemDesc* batch, int count, int total_tiles,
-                  cudaStream_t stream) {
-  DeviceInfo* di = nullptr;
-  const int rc = device_info(&di);
+template <class L>
+static int launch_layout(const ProblemDesc& single, const ProblemDesc* batch, int count,
+                         int total_tiles, cudaStream_t stream) {
+  int maxc = 0;
+  const int rc = max_clusters<L>(&maxc);
   if (rc != NF4_OK) return rc;
-  const int clusters = std::min(total_tiles, di->max_clusters);
+  const int clusters = std::min(total_tiles, maxc);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -755,13 +774,21 @@ static int launch(const ProblemDesc& single, const ProblemDesc* batch, int count
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, bwd_a_kernel, single, batch, count, total_tiles) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, bwd_a_kernel<L>, single, batch, count, total_tiles) != cudaSuccess)
     return NF4_ERR_CUDA;
   return launch_status();
+}
+
+// all_bf16: every problem of the launch has bf16 grad_out (the deeper-ring
+// layout only has room for bf16 raw stages).
+static int launch(const ProblemDesc& single, const ProblemDesc* batch, int count, int total_tiles,
+                  bool all_bf16, cudaStream_t stream) {
+  return all_bf16 ? launch_layout<LayoutBF16>(single, batch, count, total_tiles, stream)
+                  : launch_layout<LayoutF32>(single, batch, count, total_tiles, stream);
 }
 
 }  // namespace nf4
@@ -798,7 +825,7 @@ extern "C" int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float
   if (rc != NF4_OK) return rc;
   const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
   if (tiles > INT_MAX) return NF4_ERR_INVALID;
-  return launch(d, nullptr, 1, static_cast<int>(tiles), as_stream(stream));
+  return launch(d, nullptr, 1, static_cast<int>(tiles), go_dtype == NF4_BF16, as_stream(stream));
 }
 
 extern "C" int nf4_backward_a(const float* grad_out, const float* scales, const uint8_t* data,
@@ -862,8 +889,10 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
   }
   ProblemDesc unused;
   std::memset(&unused, 0, sizeof(unused));
+  bool all_bf16 = true;
+  for (const ProblemDesc& d : descs) all_bf16 = all_bf16 && d.dtype == NF4_BF16;
   return launch(unused, static_cast<const ProblemDesc*>(workspace), static_cast<int>(descs.size()),
-                static_cast<int>(total), st);
+                static_cast<int>(total), all_bf16, st);
 }
 
 #ifdef NF4_TRACE
@@ -977,5 +1006,7 @@ extern "C" int nf4_backward_a_batched_noalloc(const nf4_problem* problems, int c
   }
   ProblemDesc unused;
   std::memset(&unused, 0, sizeof(unused));
-  return launch(unused, ws, n, static_cast<int>(total), st);
+  bool all_bf16 = true;
+  for (int i = 0; i < n; ++i) all_bf16 = all_bf16 && problems[order[i]].go_dtype == NF4_BF16;
+  return launch(unused, ws, n, static_cast<int>(total), all_bf16, st);
 }

@@ -164,6 +164,19 @@ def test_batched_matches_single_and_oracle():
         assert_close(out.cpu().numpy(), ref, bound, str(p))
 
 
+def test_batched_bf16_only_matches_single():
+    """A grouped launch whose problems all have bf16 grad_out (the deeper-ring
+    layout) gives the single-problem results bit for bit."""
+    probs = [Problem(300, 136, 640, BF16, 1e-2, 0.02, True, 51),
+             Problem(520, 512, 1536, BF16, 1e-2, 0.02, False, 52)]
+    items = [(to_device_go(make_grad_out(p), p.go_dtype),
+              nb().quantize(torch.from_numpy(make_weight(p)).cuda()), None) for p in probs]
+    outs = nb().backward_a_batched(items)
+    nb().check_error()
+    for (go, w, _), out in zip(items, outs):
+        assert torch.equal(out, nb().backward_a(go, w))
+
+
 def test_batched_full_step_shapes_one_layer():
     """One layer's seven projections at a reduced token count, grouped."""
     full = CONFIGS["full_step"][:7]
