@@ -49,6 +49,8 @@ SIGNATURES = {
     "nf4_backward_a_batched": (_i, [C.POINTER(Nf4Problem), _i, _vp, _sz, _vp]),
     "nf4_check_error": (_i, [_vp]),
     "nf4_backward_a_batched_noalloc": (_i, [C.POINTER(Nf4Problem), _i, _vp]),
+    "nf4_set_small_m_max": (_i, [_i]),
+    "nf4_small_m_split": (_i, [_i, _i, _i, _i, C.POINTER(_i)]),
 }
 
 _lib = None
@@ -198,6 +200,34 @@ def backward_a_batched_noalloc(items):
     _check(lib().nf4_backward_a_batched_noalloc(arr, len(items), _stream()),
            "nf4_backward_a_batched_noalloc")
     return [out for _, _, out in items]
+
+
+def set_small_m_max(m_max: int) -> int:
+    """Largest M sent to the few-token kernel (0..64); returns the previous limit."""
+    return int(lib().nf4_set_small_m_max(int(m_max)))
+
+
+class small_m_max:
+    """Context manager: ``with small_m_max(0): ...`` runs the block with that limit."""
+
+    def __init__(self, m_max: int):
+        self.m_max, self.prev = int(m_max), None
+
+    def __enter__(self):
+        self.prev = set_small_m_max(self.m_max)
+        return self
+
+    def __exit__(self, *exc):
+        set_small_m_max(self.prev)
+        return False
+
+
+def small_m_split(N: int, K: int, sms: int, cta_slots: int) -> tuple[int, int]:
+    """(cluster size S, 64-wide N stages per cluster rank) the few-token path picks
+    on `sms` SMs that hold `cta_slots` of its CTAs at once."""
+    per = C.c_int(0)
+    S = lib().nf4_small_m_split(N, K, sms, cta_slots, C.byref(per))
+    return int(S), int(per.value)
 
 
 def check_error() -> None:

@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -53,6 +54,8 @@
 #include "nf4_common.h"
 #include "nf4_dequant.cuh"
 #include "ptx.cuh"
+#include "nf4_trace.cuh"
+#include "nf4_small_m.cuh"
 
 namespace nf4 {
 
@@ -213,27 +216,7 @@ __device__ __forceinline__ float cc_scale(const ConvCursor& c, uint32_t rank, in
   return __ldg(c.scales + static_cast<int64_t>(n) * c.KB + b);
 }
 
-// Optional timing probes (compiled in only with -DNF4_TRACE, for profiling):
-// the two CTAs of cluster 0 record clock64() at fixed points of each role into
-// a device buffer [cta][event][slot]; event kTraceEvents-1 slot 0 is the clock
-// right after the start-up cluster barrier, the common reference of both CTAs.
-// Events: 0-15 converter warp after its operand-slot wait, 16-31 converter warp
-// done, 32/33/38 MMA before wait / after wait / after commit, 35/36 epilogue
-// tile start / end, 39 reference, 40 producer issue, 41 watcher sees stage,
-// 42 converter group leader sees raw data, 43 converter group leader starts.
-#ifdef NF4_TRACE
-__device__ unsigned long long* g_trace = nullptr;
-constexpr int kTraceSlots = 512;
-constexpr int kTraceEvents = 48;
-#define NF4_PROBE(ev, idx)                                                               \
-  do {                                                                                   \
-    if (blockIdx.x < 2 && g_trace != nullptr && (idx) < kTraceSlots)                     \
-      g_trace[(blockIdx.x * kTraceEvents + (ev)) * kTraceSlots + (idx)] =                 \
-          static_cast<unsigned long long>(clock64());                                    \
-  } while (0)
-#else
-#define NF4_PROBE(ev, idx) do { } while (0)
-#endif
+
 
 // ------------------------------------------------------------------ kernel
 template <class L>
@@ -791,11 +774,170 @@ static int launch(const ProblemDesc& single, const ProblemDesc* batch, int count
                   : launch_layout<LayoutF32>(single, batch, count, total_tiles, stream);
 }
 
+// ------------------------------------------------------------------ small M
+namespace small_m {
+
+static std::atomic<int> g_max_m{64};
+
+static int fill(SmallDesc* d, const void* go, int dtype, const float* scales, const uint8_t* data,
+                float* grad_A, int M, int N, int K, int mp) {
+  std::memset(d, 0, sizeof(*d));
+  const bool f32 = dtype == NF4_F32;
+  if (!encode_2d(&d->tm_go, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 go, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(N) * (f32 ? 4 : 2), f32 ? 32 : 64, static_cast<uint32_t>(mp),
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return NF4_ERR_CUDA;
+  if (!encode_2d(&d->tm_nf4, CU_TENSOR_MAP_DATA_TYPE_UINT8, data, static_cast<uint64_t>(K / 2),
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), SK / 2, SN,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return NF4_ERR_CUDA;
+  d->scales = scales;
+  d->grad_A = grad_A;
+  d->M = M;
+  d->N = N;
+  d->K = K;
+  d->dtype = dtype;
+  return NF4_OK;
+}
+
+// Clusters of S CTAs of configuration C that fit on the current device at once,
+// for every S = 1..kMaxCluster (0 where S does not fit), and the SM count.
+template <class C>
+static int occupancy(const int** clusters, int* sms_out) {
+  static int cached[64][kMaxCluster + 1];
+  static int sms_cached[64];
+  static bool done[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NF4_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    auto kern = small_m_kernel<C>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+      return NF4_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NF4_ERR_CUDA;
+    for (int S = 1; S <= kMaxCluster; ++S) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(static_cast<unsigned>(S * 64), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();  // a size the device cannot schedule: not a sticky error
+        n = 0;
+      }
+      cached[dev][S] = n;
+    }
+    sms_cached[dev] = sms;
+    done[dev] = true;
+  }
+  *clusters = cached[dev];
+  *sms_out = sms_cached[dev];
+  return NF4_OK;
+}
+
+// Cluster size for T k-tiles of `chunks` stages each: the S whose launch keeps
+// the most loaded SM busiest for the shortest time, counting the stages of the
+// CTAs that share an SM (and whole extra waves if the clusters do not all fit),
+// plus a fixed cost per CTA for its start-up and the reduction.
+static int choose_split(int T, int chunks, const int* clusters, int sms, int* per_out) {
+  constexpr int64_t kFixedStages = 2;
+  int64_t best = INT64_MAX;
+  int best_s = 1, best_per = chunks;
+  for (int S = 1; S <= std::min(kMaxCluster, chunks); ++S) {
+    const int per = (chunks + S - 1) / S;
+    if ((chunks + per - 1) / per != S) continue;  // same slices as a smaller S
+    const int64_t fit = clusters[S];
+    if (fit <= 0) continue;
+    const int64_t live = std::min<int64_t>(T, fit);
+    const int64_t waves = (T + fit - 1) / fit;
+    const int64_t per_sm = (live * S + sms - 1) / sms;
+    const int64_t cost = waves * per_sm * (per + kFixedStages);
+    if (cost < best) {
+      best = cost;
+      best_s = S;
+      best_per = per;
+    }
+  }
+  *per_out = best_per;
+  return best_s;
+}
+
+template <class C>
+static int launch(SmallDesc& d, cudaStream_t stream) {
+  const int* clusters = nullptr;
+  int sms = 0;
+  int rc = occupancy<C>(&clusters, &sms);
+  if (rc != NF4_OK) return rc;
+  const int T = (d.K + SK - 1) / SK;
+  const int chunks = (d.N + SN - 1) / SN;
+  int per = chunks;
+  const int S = choose_split(T, chunks, clusters, sms, &per);
+  if (clusters[S] <= 0) return NF4_ERR_CUDA;
+  d.n_per_cta = per * SN;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(T * S), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, small_m_kernel<C>, d) != cudaSuccess) return NF4_ERR_CUDA;
+  return launch_status();
+}
+
+static int run(const void* go, int dtype, const float* scales, const uint8_t* data,
+               float* grad_A, int M, int N, int K, cudaStream_t stream) {
+  const int mp = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+  SmallDesc d;
+  const int rc = fill(&d, go, dtype, scales, data, grad_A, M, N, K, mp);
+  if (rc != NF4_OK) return rc;
+  if (mp == 16) return launch<Cfg16>(d, stream);
+  if (mp == 32) return launch<Cfg32>(d, stream);
+  return launch<Cfg64>(d, stream);
+}
+
+}  // namespace small_m
 }  // namespace nf4
 
 using namespace nf4;
 
 extern "C" int nf4_abi_version(void) { return 1; }
+
+extern "C" int nf4_set_small_m_max(int m_max) {
+  if (m_max < 0) m_max = 0;
+  if (m_max > 64) m_max = 64;
+  return small_m::g_max_m.exchange(m_max);
+}
+
+extern "C" int nf4_small_m_split(int N, int K, int sms, int cta_slots, int* per_out) {
+  // Host-only planning rule of the small-M kernel: clusters of S CTAs are
+  // assumed to fit cta_slots / S times at once.
+  if (N <= 0 || K <= 0 || sms <= 0 || cta_slots <= 0 || per_out == nullptr) return -1;
+  int fit[small_m::kMaxCluster + 1] = {0};
+  for (int S = 1; S <= small_m::kMaxCluster; ++S) fit[S] = cta_slots / S;
+  const int T = (K + small_m::SK - 1) / small_m::SK;
+  const int chunks = (N + small_m::SN - 1) / small_m::SN;
+  return small_m::choose_split(T, chunks, fit, sms, per_out);
+}
 
 extern "C" const char* nf4_status_string(int status) {
   switch (status) {
@@ -820,6 +962,8 @@ extern "C" int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float
                ? NF4_OK
                : NF4_ERR_CUDA;
   }
+  if (M <= small_m::g_max_m.load())
+    return small_m::run(grad_out, go_dtype, scales, data, grad_A, M, N, K, as_stream(stream));
   ProblemDesc d;
   rc = fill_desc(&d, grad_out, go_dtype, scales, data, grad_A, M, N, K);
   if (rc != NF4_OK) return rc;
@@ -849,6 +993,7 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
   cudaStream_t st = as_stream(stream);
   std::vector<ProblemDesc> descs;
   descs.reserve(count);
+  const int small_max = small_m::g_max_m.load();
   for (int i = 0; i < count; ++i) {
     const nf4_problem& p = problems[i];
     if (p.M == 0) continue;
@@ -856,6 +1001,14 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
       if (cudaMemsetAsync(p.grad_A, 0, sizeof(float) * static_cast<size_t>(p.M) * p.K, st) !=
           cudaSuccess)
         return NF4_ERR_CUDA;
+      continue;
+    }
+    if (p.M <= small_max) {
+      // Few tokens: the problem's own launch of the few-token kernel, so that
+      // it gets the same result as a single call.
+      const int rc = small_m::run(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N,
+                                  p.K, st);
+      if (rc != NF4_OK) return rc;
       continue;
     }
     descs.emplace_back();
@@ -962,6 +1115,7 @@ extern "C" int nf4_backward_a_batched_noalloc(const nf4_problem* problems, int c
   int order[kNoAllocMaxProblems];
   int stages[kNoAllocMaxProblems];
   int n = 0;
+  const int small_max = small_m::g_max_m.load();
   for (int i = 0; i < count; ++i) {
     const nf4_problem& p = problems[i];
     if (p.M == 0) continue;
@@ -969,6 +1123,12 @@ extern "C" int nf4_backward_a_batched_noalloc(const nf4_problem* problems, int c
       if (cudaMemsetAsync(p.grad_A, 0, sizeof(float) * static_cast<size_t>(p.M) * p.K, st) !=
           cudaSuccess)
         return NF4_ERR_CUDA;
+      continue;
+    }
+    if (p.M <= small_max) {
+      const int rc = small_m::run(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N,
+                                  p.K, st);
+      if (rc != NF4_OK) return rc;
       continue;
     }
     const int ns = (p.N + BN - 1) / BN;

@@ -1,0 +1,41 @@
+// nf4_trace.cuh -- optional timing probes, compiled in only with -DNF4_TRACE.
+//
+// The first two CTAs of a launch record clock64() at fixed points of each role
+// into a device buffer [cta][event][slot] set with nf4_debug_set_trace(); the
+// event numbers are listed at each kernel.  Without NF4_TRACE the probes expand
+// to nothing.
+#pragma once
+
+namespace nf4 {
+// Pair kernel (bwd_a_kernel):
+// the two CTAs of cluster 0 record clock64() at fixed points of each role into
+// a device buffer [cta][event][slot]; event kTraceEvents-1 slot 0 is the clock
+// right after the start-up cluster barrier, the common reference of both CTAs.
+// Events: 0-15 converter warp after its operand-slot wait, 16-31 converter warp
+// done, 32/33/38 MMA before wait / after wait / after commit, 35/36 epilogue
+// tile start / end, 39 reference, 40 producer issue, 41 watcher sees stage,
+// 42 converter group leader sees raw data, 43 converter group leader starts.
+//
+// Few-token kernel (small_m_kernel), CTAs 0 and 1 (k-tile 0, cluster ranks 0
+// and 1 when S > 1): slot s of events 0-6 and 8 is stage s.  0 producer issues
+// the NF4 box, 1 producer issues grad_out box 0, 2 first warp of the group has
+// the raw stage, 3 it has the operand slot, 4 it has finished the stage, 8 the
+// group's last warp has finished it, 5 MMA thread has the stage, 6 MMA thread
+// has committed it.  Event 7: slot 0 after start-up (the reference), 1
+// accumulator ready, 2 partial tile written, 3 after the first cluster
+// barrier, 4 reduction stored, 5 after the last cluster barrier.
+#ifdef NF4_TRACE
+__device__ unsigned long long* g_trace = nullptr;
+constexpr int kTraceSlots = 512;
+constexpr int kTraceEvents = 48;
+#define NF4_PROBE(ev, idx)                                                               \
+  do {                                                                                   \
+    if (blockIdx.x < 2 && g_trace != nullptr && (idx) < kTraceSlots)                     \
+      g_trace[(blockIdx.x * kTraceEvents + (ev)) * kTraceSlots + (idx)] =                 \
+          static_cast<unsigned long long>(clock64());                                    \
+  } while (0)
+#else
+#define NF4_PROBE(ev, idx) do { } while (0)
+#endif
+
+}  // namespace nf4

@@ -238,7 +238,7 @@ def bench_ours(args, rank, world, dev):
     roof["peak_source"] = (f"{peak_kind} {'sustained' if long_run else 'burst'} bf16 "
                            "(f16 nominal rate = bf16)" if roof["bound"] == "tensor"
                            else f"{peak_kind} HBM copy")
-    roof["kernel"] = "bwd_a_kernel"
+    roof["kernel"] = kernel_names(probs)
 
     line = {
         "metric": "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline",
@@ -252,12 +252,38 @@ def bench_ours(args, rank, world, dev):
                    "parallelism": f"dp{world} (M-sharded replicas, no collective)"},
         "e2e": e2e,
         "roofline": roof,
-        "gpu_launches": K,
+        "gpu_launches": K * launches_per_step(probs),
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(probs, budget_s=args.cpu_seconds)
     return line
+
+
+SMALL_M_MAX = 64      # the library's default few-token limit (nf4_set_small_m_max)
+DESCS_PER_UPLOAD = 60  # descriptors per upload kernel of a grouped launch
+
+
+def kernel_names(probs) -> str:
+    """The library kernels one step launches: the few-token kernel for M <= 64,
+    the pair kernel otherwise."""
+    names = []
+    if any(p.M <= SMALL_M_MAX for p in probs):
+        names.append("small_m_kernel")
+    if any(p.M > SMALL_M_MAX for p in probs):
+        names.append("bwd_a_kernel")
+    return " + ".join(names)
+
+
+def launches_per_step(probs) -> int:
+    """Kernel launches of one step through the C ABI: a single problem is one
+    launch; a grouped call launches one few-token kernel per problem with
+    M <= 64, then the descriptor uploads and one grouped GEMM for the rest."""
+    if len(probs) == 1:
+        return 1
+    few = sum(1 for p in probs if p.M <= SMALL_M_MAX)
+    rest = len(probs) - few
+    return few + ((-(-rest // DESCS_PER_UPLOAD) + 1) if rest else 0)
 
 
 def bench_e2e(args, probs, host_go, set0, stream, dev, flops, world):

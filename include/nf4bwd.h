@@ -104,6 +104,28 @@ int nf4_backward_a(const float* grad_out, const float* scales, const uint8_t* da
 int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float* scales,
                       const uint8_t* data, float* grad_A, int M, int N, int K, void* stream);
 
+/*
+ * Few-token path.  A call of nf4_backward_a / nf4_backward_a_ex with M at most
+ * this limit runs a kernel built for small M: the weight is streamed once
+ * (256 output columns per CTA, all tokens at once) and the shared dimension N
+ * is split over a cluster of up to 16 CTAs whose partial sums are added in a
+ * fixed order (the result is deterministic, but its rounding differs from the
+ * general kernel's).  The default limit is 64, the
+ * largest allowed; 0 sends every M to the general kernel.  Returns the previous
+ * limit.  Process-wide; takes effect for calls made after it returns.
+ */
+int nf4_set_small_m_max(int m_max);
+
+/*
+ * The small-M path's choice of cluster size S for an N x K weight, as a pure
+ * host computation (no device is touched): `sms` SMs holding `cta_slots` CTAs
+ * at once in all, so that cta_slots / S clusters of size S fit.  Writes to
+ * *per_out the number of 64-wide N stages of each cluster rank and returns S
+ * (1..16), or -1 for a non-positive argument or a NULL per_out.  The launch
+ * makes the same choice from the device's real cluster occupancy.
+ */
+int nf4_small_m_split(int N, int K, int sms, int cta_slots, int* per_out);
+
 /* One projection of a grouped launch. */
 typedef struct nf4_problem {
   const void* grad_out; /* [M][N], type go_dtype */
@@ -128,7 +150,10 @@ size_t nf4_backward_a_batched_workspace(int count);
  * (tensor maps, pointers, sizes) into it -- the descriptors travel as kernel
  * parameters, so nothing on the host has to outlive the call -- and then the
  * GEMM kernel that reads them.  The workspace must not be reused by another
- * call until this one has run.
+ * call until this one has run.  Problems with M at most the few-token limit
+ * (nf4_set_small_m_max) are not part of the grouped launch: each runs as its
+ * own launch of the few-token kernel, so every problem's grad_A equals, bit
+ * for bit, what a single call gives.
  */
 int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspace,
                            size_t workspace_bytes, void* stream);
@@ -141,7 +166,8 @@ int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspa
  * cudaMalloc would synchronise the device, or in a process whose device memory
  * is all reserved up front.
  *
- * Same problems, rules and results as nf4_backward_a_batched, but the
+ * Same problems, rules and results as nf4_backward_a_batched (few-token
+ * problems included), but the
  * per-problem descriptors go to a fixed array inside the library (a
  * file-scope device array of 128 KiB, reserved on every GPU that loads the
  * library until the process exits), so the call takes no workspace.

@@ -116,6 +116,58 @@ def test_small_problems_full_check(p):
     run_problem(p)
 
 
+# ---------------------------------------------------------------- few-token path
+# M <= 64 runs the swap-AB kernel with N split over a cluster; the same
+# problems also run through the general kernel (small-M limit 0).
+FEW = [
+    Problem(1, 64, 64, F32, 1.0, 0.02, False, 20, "m1-k64"),
+    Problem(16, 1536, 1536, F32, 1e-2, 0.02, False, 21, "m16-q"),
+    Problem(16, 200, 320, F32, 1.0, 0.02, True, 22, "m16-ragged"),
+    Problem(13, 4104, 192, BF16, 1.0, 0.02, True, 23, "m13-bf16-long-n"),
+    Problem(32, 520, 640, F32, 1.0, 0.02, False, 24, "m32"),
+    Problem(17, 1032, 384, BF16, 1e-2, 0.02, True, 25, "m17-bf16"),
+    Problem(64, 2048, 256, F32, 1.0, 0.015, False, 26, "m64"),
+    Problem(33, 96, 1088, BF16, 1.0, 0.02, False, 27, "m33-bf16-k-tail"),
+    Problem(16, 14336, 256, F32, 1.0, 0.015, False, 28, "m16-max-split"),
+]
+
+
+@pytest.mark.parametrize("route", ["few-token", "general"])
+@pytest.mark.parametrize("p", FEW, ids=lambda p: p.name)
+def test_few_token_problems_full_check(p, route):
+    with nb().small_m_max(64 if route == "few-token" else 0):
+        run_problem(p)
+
+
+def test_few_token_one_hot_rows_exact():
+    """One-hot rows on the split path: exactly one cluster rank holds the
+    nonzero product, the other partials are zeros, so the sum is exact."""
+    K, N = 384, 1280
+    B = make_weight(Problem(1, N, K, F32, 1.0, 0.02, True, seed=29))
+    w, data_o, scales_o = _weight_from_oracle(B)
+    ns = [0, 63, 64, 127, 128, 639, 640, 641, 1000, 1279]
+    go = np.zeros((len(ns) + 2, N), dtype=np.float32)
+    for i, n in enumerate(ns):
+        go[i, n] = 1.0
+    with nb().small_m_max(64):
+        ga = nb().backward_a(torch.from_numpy(go).cuda(), w).cpu().numpy()
+    bt = oracle.dequantize_f16(scales_o, data_o, K, N).view(np.float16).astype(np.float32)
+    for i, n in enumerate(ns):
+        np.testing.assert_array_equal(ga[i], bt[n], err_msg=f"row {i} n={n}")
+    assert np.all(ga[len(ns):] == 0)
+
+
+def test_few_token_deterministic():
+    p = Problem(16, 14336, 1024, F32, 1.0, 0.015, False, 30)
+    go = to_device_go(make_grad_out(p), F32)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    with nb().small_m_max(64):
+        a = nb().backward_a(go, w)
+        for _ in range(3):
+            assert torch.equal(a, nb().backward_a(go, w))
+    nb().check_error()
+
+
 def test_deterministic():
     p = Problem(300, 192, 640, F32, 1.0, 0.02, True, 11)
     go = to_device_go(make_grad_out(p), F32)
@@ -125,7 +177,7 @@ def test_deterministic():
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("name", ["down_proj", "large_a", "q_proj"])
+@pytest.mark.parametrize("name", ["down_proj", "large_a", "q_proj", "small_m_a", "small_m_b"])
 def test_full_size_runs_are_bit_identical(name):
     """Three launches on the same inputs give the same grad_A in every element:
     no float atomics, no split reductions, and no race between the pipeline's
@@ -255,12 +307,21 @@ def test_rejects_bad_arguments_without_launching():
     assert L.nf4_backward_a(*args(out=out.data_ptr() + 8)) == nb().NF4_ERR_ALIGN
     assert L.nf4_backward_a(*args(go=None)) == nb().NF4_ERR_INVALID
     # Grouped launch without (or with too small) a workspace.
-    probs = (nb().Nf4Problem * 1)(nb().Nf4Problem(go.data_ptr(), 0, w.scales.data_ptr(),
-                                                  w.data.data_ptr(), out.data_ptr(), 16, 64, 128))
+    go100 = torch.zeros((100, 64), device="cuda")
+    out100 = torch.zeros((100, 128), device="cuda")
+    probs = (nb().Nf4Problem * 1)(nb().Nf4Problem(go100.data_ptr(), 0, w.scales.data_ptr(),
+                                                  w.data.data_ptr(), out100.data_ptr(), 100, 64,
+                                                  128))
     assert L.nf4_backward_a_batched(probs, 1, None, 0, s) == nb().NF4_ERR_WORKSPACE
     ws = torch.empty(64, dtype=torch.uint8, device="cuda")
     assert L.nf4_backward_a_batched(probs, 1, ws.data_ptr(), 64, s) == nb().NF4_ERR_WORKSPACE
+    # Few-token problems run as their own launches and need no workspace.
+    few = (nb().Nf4Problem * 1)(nb().Nf4Problem(go.data_ptr(), 0, w.scales.data_ptr(),
+                                                w.data.data_ptr(), out.data_ptr(), 16, 64, 128))
+    out.fill_(1.0)
+    assert L.nf4_backward_a_batched(few, 1, None, 0, s) == nb().NF4_OK
     nb().check_error()
+    assert torch.all(out == 0)  # grad_out is zero
 
 
 # ---------------------------------------------------------------- full-size workloads
