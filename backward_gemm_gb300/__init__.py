@@ -48,6 +48,7 @@ SIGNATURES = {
     "nf4_backward_a_batched_workspace": (_sz, [_i]),
     "nf4_backward_a_batched": (_i, [C.POINTER(Nf4Problem), _i, _vp, _sz, _vp]),
     "nf4_check_error": (_i, [_vp]),
+    "nf4_check_error_site": (_i, [_vp, C.POINTER(C.c_uint)]),
     "nf4_backward_a_batched_noalloc": (_i, [C.POINTER(Nf4Problem), _i, _vp]),
     "nf4_set_small_m_max": (_i, [_i]),
     "nf4_small_m_split": (_i, [_i, _i, _i, _i, C.POINTER(_i)]),
@@ -231,5 +232,11 @@ def small_m_split(N: int, K: int, sms: int, cta_slots: int) -> tuple[int, int]:
 
 
 def check_error() -> None:
-    """Synchronise the current stream and raise if a kernel's bounded wait gave up."""
-    _check(lib().nf4_check_error(_stream()), "nf4_check_error")
+    """Synchronise the current stream and raise if a kernel's bounded wait gave up
+    (the message then says which block, thread and barrier)."""
+    site = (C.c_uint * 4)()
+    rc = lib().nf4_check_error_site(_stream(), site)
+    if rc == NF4_ERR_TIMEOUT:
+        raise Nf4Error(rc, f"nf4_check_error (first wait that gave up: block {site[0] - 1}, "
+                           f"thread {site[1]}, shared address {site[2]:#x}, waiting for {site[3]})")
+    _check(rc, "nf4_check_error")

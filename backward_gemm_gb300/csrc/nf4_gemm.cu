@@ -83,6 +83,7 @@ constexpr int kBBytes = BKC * BN * 2;                  // 16 KB f16
 constexpr int kOpBytes = kABytes + kBBytes;            // 32 KB
 constexpr int kEpiBufBytes = 32 * 128;                 // 32 rows x 32 fp32
 constexpr uint32_t kSigBytes = 16;
+constexpr long long kAbortLingerCycles = 4000000;  // ~2 ms: far longer than a copy's latency
 constexpr uint32_t kTmemCols = 2 * BK;
 
 // Shared-memory layout of one kernel configuration: RS raw stages holding GOB
@@ -112,8 +113,15 @@ struct Layout {
   static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
   static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
   static_assert(kReadyOff + 4 * OS <= kSigOff, "ready words fit before the signal area");
+  static_assert(RS * 3 <= 32, "one producer lane per (raw slot, box)");
+  // Each raw slot must always be consumed by the same converter group.  A group
+  // waits for a slot's phase by parity only; if the slot alternated between the
+  // groups, a group could wait for phase k while phase k-1 (the other group's
+  // stage, copy still in flight) is incomplete, and the completed phase k-2 has
+  // the same parity: the wait would pass on stale data.
+  static_assert(RS % kConvGroups == 0, "raw slots are not shared between converter groups");
 };
-using LayoutF32 = Layout<3, 3, 2 * kGoBoxBytes>;  // any fp32 grad_out in the launch
+using LayoutF32 = Layout<2, 4, 2 * kGoBoxBytes>;  // any fp32 grad_out in the launch
 using LayoutBF16 = Layout<4, 4, kGoBoxBytes>;     // bf16 grad_out only
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
@@ -219,6 +227,9 @@ __device__ __forceinline__ float cc_scale(const ConvCursor& c, uint32_t rank, in
 
 
 // ------------------------------------------------------------------ kernel
+// Progress slots (NF4_PROGRESS builds): 0 producer stages issued, 1 MMA stages
+// committed, 2 MMA tiles committed, 3 watcher stages published, 4-19 stages
+// finished by converter warp 0-15, 20-23 tiles stored by epilogue warp 0-3.
 template <class L>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_a_kernel(const __grid_constant__ ProblemDesc single, const ProblemDesc* __restrict__ batch,
@@ -298,35 +309,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      if (count == 1) {
-        tma_prefetch_desc(&descs[0].tm_go);
-        tma_prefetch_desc(&descs[0].tm_nf4);
-      }
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = cluster; ok && t < total_tiles; t += nclusters) {
-        const Tile tl = tile_at(descs, count, t);
-        const bool f32 = tl.dtype == NF4_F32;
-        const uint32_t bytes = (f32 ? 2 * kGoBoxBytes : kGoBoxBytes) + kNf4Bytes;
-        const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
-        const int x_nf4 = tl.kt * (BK / 2) + static_cast<int>(rank) * (BKC / 2);
-        for (int s = 0; s < tl.ns; ++s, ++it) {
-          const uint32_t slot = it % kRawStages;
-          const uint32_t ph = (it / kRawStages) & 1u;
-          if (!mbar_wait(empty_raw(slot), ph ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          NF4_PROBE(40, it);
-          const uint32_t fb = full_raw(slot);
-          mbar_arrive_expect_tx(fb, bytes);
-          const uint32_t dst = sbase + kRawOff + slot * kRawBytes;
-          tma_load_2d(dst, &tl.p->tm_go, s * BN, row0, fb);
-          if (f32) tma_load_2d(dst + kGoBoxBytes, &tl.p->tm_go, s * BN + 32, row0, fb);
-          tma_load_2d(dst + kGoBytes, &tl.p->tm_nf4, x_nf4, s * BN, fb);
+    // A thread's bulk-tensor copies are served one after another, so every
+    // (ring slot, box) pair has its own lane: lane 3*slot + b issues box b of
+    // the stages that use `slot` (b = 0 grad_out columns 0-31 (fp32) or 0-63
+    // (bf16) and the stage's byte count, b = 1 fp32 columns 32-63, b = 2 the
+    // NF4 bytes).  Stages go in order and lane 0 alone waits for a slot (lanes
+    // of one warp waiting on different barriers would wake together).  Boxes may
+    // land before the byte count is registered: the phase cannot complete while
+    // that arrival is pending.
+    const int my_slot = lane / 3, box = lane % 3;
+    if (lane == 0 && count == 1) {
+      tma_prefetch_desc(&descs[0].tm_go);
+      tma_prefetch_desc(&descs[0].tm_nf4);
+    }
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = cluster; ok && t < total_tiles; t += nclusters) {
+      const Tile tl = tile_at(descs, count, t);
+      const bool f32 = tl.dtype == NF4_F32;
+      const uint32_t bytes = (f32 ? 2 * kGoBoxBytes : kGoBoxBytes) + kNf4Bytes;
+      const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
+      const int x_nf4 = tl.kt * (BK / 2) + static_cast<int>(rank) * (BKC / 2);
+      const CUtensorMap* map = box == 2 ? &tl.p->tm_nf4 : &tl.p->tm_go;
+      const bool my_box = box != 1 || f32;
+      for (int s = 0; s < tl.ns; ++s, ++it) {
+        const uint32_t slot = it % kRawStages;
+        bool free_slot = true;
+        if (lane == 0) free_slot = mbar_wait(empty_raw(slot), ((it / kRawStages) & 1u) ^ 1u, abort_flag);
+        if (!__shfl_sync(0xFFFFFFFFu, free_slot, 0)) {
+          ok = false;
+          break;
         }
+        if (my_box && my_slot == static_cast<int>(slot)) {
+          const uint32_t fb = full_raw(slot);
+          const uint32_t dst = sbase + kRawOff + slot * kRawBytes +
+                               (box == 0 ? 0u : (box == 1 ? static_cast<uint32_t>(kGoBoxBytes)
+                                                          : static_cast<uint32_t>(kGoBytes)));
+          if (box == 0) {
+            mbar_arrive_expect_tx(fb, bytes);
+            NF4_PROBE(40, it);
+          }
+          tma_load_2d(dst, map, box == 2 ? x_nf4 : s * BN + 32 * box, box == 2 ? s * BN : row0, fb);
+        }
+        if (lane == 0) NF4_PROGRESS_SET(0, it + 1);
+        __syncwarp();
       }
+    }
+    if (lane == 0) {
       // Every issued copy must land before the CTA may exit.
       for (uint32_t i = (it > kRawStages ? it - kRawStages : 0u); i < it; ++i)
         mbar_wait(full_raw(i % kRawStages), (i / kRawStages) & 1u, nullptr);
@@ -385,11 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_mma_f16_pair(d_tmem, a + 6u, b + 3u * kBStep, idesc, 1u);
           tc_commit_pair(empty_op(slot), 0x3);
           NF4_PROBE(38, it);
+          NF4_PROGRESS_SET(1, it + 1);
           ++it;
           slot = (slot + 1u == static_cast<uint32_t>(kOpStages)) ? 0u : slot + 1u;
         }
         if (!ok) break;
         tc_commit_pair(tmem_full(acc), 0x3);
+        NF4_PROGRESS_SET(2, lt + 1);
       }
       // No MMA may still be writing TMEM (of either CTA) when it is released.
       tc_commit_pair(mma_done, 0x1);
@@ -420,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           NF4_PROBE(41, it);
           st_release_shared(sbase + kReadyOff + 4u * slot, it + 1u);
+          NF4_PROGRESS_SET(3, it + 1);
         }
       }
     }
@@ -550,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (probe) NF4_PROBE(16 + cw, it);
+      if (lane == 0) NF4_PROGRESS_SET(4 + cw, it + 1);
       it += kConvGroups;
     }
   } else {
@@ -592,6 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
       }
       if (threadIdx.x == 0) NF4_PROBE(36, lt);
+      if (lane == 0) NF4_PROGRESS_SET(20 + warp, lt + 1);
       if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
     }
@@ -605,6 +639,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  // After a wait gave up, CTA 1's converter warps may still have 16-byte signal
+  // copies in flight into this CTA's shared memory (on the normal path the
+  // watcher waits for all of them): keep the CTA resident for a bounded time
+  // so that they land before its shared memory is released.
+  if (rank == 0 && threadIdx.x == 0 && (*abort_flag != 0 || *(volatile unsigned int*)&g_status != 0)) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < kAbortLingerCycles) {
+    }
   }
 }
 
@@ -1048,7 +1091,24 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
                 static_cast<int>(total), all_bf16, st);
 }
 
+#ifdef NF4_PROGRESS
+extern "C" int nf4_debug_set_progress(void* buf) {
+  unsigned int* p = static_cast<unsigned int*>(buf);
+  return cudaMemcpyToSymbol(g_progress, &p, sizeof(p)) == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+}
+#endif
+
 #ifdef NF4_TRACE
+extern "C" int nf4_debug_timeouts(unsigned int* out, int max_entries) {
+  unsigned int n = 0;
+  if (cudaMemcpyFromSymbol(&n, g_timeout_count, sizeof(n)) != cudaSuccess) return -1;
+  const int k = static_cast<int>(n < 256u ? n : 256u) < max_entries ? static_cast<int>(n < 256u ? n : 256u)
+                                                                    : max_entries;
+  if (k > 0 && cudaMemcpyFromSymbol(out, g_timeout_log, sizeof(unsigned int) * 4 * k) != cudaSuccess)
+    return -1;
+  return static_cast<int>(n);
+}
+
 extern "C" int nf4_debug_set_trace(void* buf) {
   unsigned long long* p = static_cast<unsigned long long*>(buf);
   return cudaMemcpyToSymbol(g_trace, &p, sizeof(p)) == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
@@ -1056,12 +1116,21 @@ extern "C" int nf4_debug_set_trace(void* buf) {
 #endif
 
 extern "C" int nf4_check_error(void* stream) {
+  return nf4_check_error_site(stream, nullptr);
+}
+
+extern "C" int nf4_check_error_site(void* stream, unsigned int* site) {
+  if (site != nullptr) std::memset(site, 0, 4 * sizeof(unsigned int));
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return NF4_ERR_CUDA;
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return NF4_ERR_CUDA;
   if (v != 0) {
-    const unsigned int zero = 0;
-    cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+    unsigned int where[4] = {0, 0, 0, 0};
+    cudaMemcpyFromSymbol(where, g_timeout_site, sizeof(where));
+    if (site != nullptr) std::memcpy(site, where, sizeof(where));
+    const unsigned int zero[4] = {0, 0, 0, 0};
+    cudaMemcpyToSymbol(g_status, zero, sizeof(unsigned int));
+    cudaMemcpyToSymbol(g_timeout_site, zero, sizeof(zero));
     return NF4_ERR_TIMEOUT;
   }
   return cudaGetLastError() == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;

@@ -85,7 +85,11 @@ struct Config {
   static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kGoBytes % 1024 == 0,
                 "stage alignment");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(RS % 2 == 0 && (RS / 2) * kBoxLanes <= 32, "one producer lane per (slot, box)");
+  static_assert((RS / 2) * kBoxLanes <= 32, "one producer lane per (slot, box)");
+  // Each raw slot must always be consumed by the same converter group: a group
+  // waits for a slot's phase by parity only, and a slot shared with the other
+  // group could show a completed phase of the same parity two phases back.
+  static_assert(RS % kConvGroups == 0, "raw slots are not shared between converter groups");
 };
 
 // Operand slots outnumber the converter groups, so that a group can fill its

@@ -38,4 +38,19 @@ constexpr int kTraceEvents = 48;
 #define NF4_PROBE(ev, idx) do { } while (0)
 #endif
 
+// Progress counters (compiled in only with -DNF4_PROGRESS, for diagnosing a
+// stall): each role of each CTA stores how far it got into
+// g_progress[block][slot]; slots are listed at the kernel.
+#ifdef NF4_PROGRESS
+__device__ unsigned int* g_progress = nullptr;
+#define NF4_PROGRESS_SET(slot, value)                                                   \
+  do {                                                                                 \
+    if (g_progress != nullptr)                                                         \
+      *reinterpret_cast<volatile unsigned int*>(g_progress + blockIdx.x * 32 + (slot)) = \
+          static_cast<unsigned int>(value);                                            \
+  } while (0)
+#else
+#define NF4_PROGRESS_SET(slot, value) do { } while (0)
+#endif
+
 }  // namespace nf4

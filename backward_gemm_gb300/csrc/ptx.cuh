@@ -16,17 +16,46 @@ namespace nf4 {
 static __device__ unsigned int g_status = 0;
 
 constexpr unsigned int kStatusTimeout = 4;
-constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Wait limit in SM clock cycles (about 1 s at 2 GHz, longer at lower clocks).
+// Measured with the SM's own cycle counter: it only counts forward, so a wait
+// can only give up after really having waited (the global nanosecond timer is
+// not used for this: an adjustment of it would look like an instant timeout).
+constexpr long long kWaitLimitCycles = 2000000000ll;
+
+// Where the first wait that gave up was: block, thread, the shared-memory
+// address it waited on (barrier or flag word) and the parity or value it
+// wanted.  Written once (the first timeout wins) until nf4_check_error clears it.
+static __device__ unsigned int g_timeout_site[4] = {0, 0, 0, 0};
+
+#ifdef NF4_TRACE
+// Trace builds also log every wait that gave up (up to 256): block, thread,
+// address, wanted value.
+static __device__ unsigned int g_timeout_log[256][4];
+static __device__ unsigned int g_timeout_count = 0;
+#endif
+
+__device__ __forceinline__ void record_timeout(uint32_t addr, uint32_t want) {
+#ifdef NF4_TRACE
+  const unsigned int i = atomicAdd(&g_timeout_count, 1u);
+  if (i < 256u) {
+    g_timeout_log[i][0] = blockIdx.x;
+    g_timeout_log[i][1] = threadIdx.x;
+    g_timeout_log[i][2] = addr;
+    g_timeout_log[i][3] = want;
+  }
+#endif
+  atomicExch(&g_status, kStatusTimeout);
+  if (atomicCAS(&g_timeout_site[0], 0u, blockIdx.x + 1u) == 0u) {
+    g_timeout_site[1] = threadIdx.x;
+    g_timeout_site[2] = addr;
+    g_timeout_site[3] = want;
+  }
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -60,19 +89,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false (and
-// records kStatusTimeout) if that takes longer than kWaitLimitNs, or soon after
+// records kStatusTimeout) if that takes longer than kWaitLimitCycles, or soon after
 // another role of the CTA has given up (*abort_flag != 0).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag != 0) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicExch(&g_status, kStatusTimeout);
+    if (clock64() - t0 > kWaitLimitCycles) {
+      record_timeout(bar, parity);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;
     }
@@ -96,14 +125,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait_cluster(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag != 0) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicExch(&g_status, kStatusTimeout);
+    if (clock64() - t0 > kWaitLimitCycles) {
+      record_timeout(bar, parity);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;
     }
@@ -169,14 +198,14 @@ __device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
 // Spin until the flag word equals `want`; bounded like mbar_wait.
 __device__ __forceinline__ bool flag_wait(uint32_t addr, uint32_t want, volatile int* abort_flag) {
   if (ld_acquire_shared(addr) == want) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (ld_acquire_shared(addr) == want) return true;
     if (abort_flag != nullptr && *abort_flag != 0) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicExch(&g_status, kStatusTimeout);
+    if (clock64() - t0 > kWaitLimitCycles) {
+      record_timeout(addr, want);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;
     }

@@ -192,6 +192,14 @@ int nf4_backward_a_batched_noalloc(const nf4_problem* problems, int count, void*
  */
 int nf4_check_error(void* stream);
 
+/*
+ * As nf4_check_error, and if a wait gave up, where the first one was: site[0] =
+ * block index + 1, site[1] = thread index, site[2] = the shared-memory address
+ * waited on, site[3] = the phase parity or flag value it waited for.  `site`
+ * (4 words, host memory) is zeroed when there was no timeout; may be NULL.
+ */
+int nf4_check_error_site(void* stream, unsigned int* site);
+
 #ifdef __cplusplus
 }
 #endif
