@@ -101,7 +101,7 @@ struct Layout {
   static constexpr int kEpiOff = kOpOff + OS * kOpBytes;
   static constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
   static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1;
-  // misc: TMEM address, abort flag, one ready word per operand slot, then the
+  // misc: TMEM address, abort flag, the ready counter (and spare words), then the
   // 16-byte signal words: in CTA 0 one destination per (operand slot,
   // converter warp of a group), and one source.
   static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
@@ -112,7 +112,7 @@ struct Layout {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
   static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
-  static_assert(kReadyOff + 4 * OS <= kSigOff, "ready words fit before the signal area");
+  static_assert(kReadyOff + 4 * OS <= kSigOff, "ready counter fits before the signal area");
   static_assert(RS * 3 <= 32, "one producer lane per (raw slot, box)");
   // Each raw slot must always be consumed by the same converter group.  A group
   // waits for a slot's phase by parity only; if the slot alternated between the
@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  NF4_TRACE_INIT;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
@@ -372,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer (CTA 0)
     if (rank == 0 && lane == 0) {
       // This thread shares its SM sub-partition with busy converter warps and
-      // is on the critical path: per stage it only polls the ready word,
-      // issues 4 MMAs and commits.  Descriptors of slot 0 are built once; a
+      // is on the critical path: per stage it issues 4 MMAs and commits, and
+      // reads the ready counter only when it has caught up with it.  Descriptors of slot 0 are built once; a
       // slot's are those plus its offset in the 16-byte address field.
       constexpr uint32_t idesc = idesc_f16_f32(BMP, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
       const uint64_t a_desc0 = smem_desc_sw128(sbase + kOpOff, 16, kSbo);
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kBStep = (2u * kSbo) >> 4;  // +2 n-groups per MMA K-step
       const uint32_t ready0 = sbase + kReadyOff;
       uint32_t it = 0, lt = 0, slot = 0;
+      uint32_t avail = 0;  // stages the watcher has published as ready
       bool ok = true;
       for (int t = cluster; ok && t < total_tiles; t += nclusters, ++lt) {
         const Tile tl = tile_at(descs, count, t);
@@ -393,9 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * BK;
         for (int s = 0; s < tl.ns; ++s) {
           NF4_PROBE(32, it);
-          // The watcher warp has seen stage `it`'s operand barrier complete
-          // when it publishes it + 1 in the slot's ready word.
-          if (!flag_wait(ready0 + 4u * slot, it + 1u, abort_flag)) {
+          // The watcher publishes, in order, how many stages' operand barriers
+          // it has seen complete; the counter is read again only when this
+          // thread has caught up with it, so stages that are already ready go
+          // to the tensor core back to back.
+          if (avail <= it && !flag_wait_ge(ready0, it + 1u, abort_flag, &avail)) {
             ok = false;
             break;
           }
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           NF4_PROBE(41, it);
-          st_release_shared(sbase + kReadyOff + 4u * slot, it + 1u);
+          st_release_shared(sbase + kReadyOff, it + 1u);
           NF4_PROGRESS_SET(3, it + 1);
         }
       }

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  NF4_TRACE_INIT;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < RS; ++i) {

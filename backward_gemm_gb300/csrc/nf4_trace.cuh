@@ -28,13 +28,17 @@ namespace nf4 {
 __device__ unsigned long long* g_trace = nullptr;
 constexpr int kTraceSlots = 512;
 constexpr int kTraceEvents = 48;
+// Each kernel caches the buffer pointer once (NF4_TRACE_INIT), so a probe is a
+// clock read and one store.
+#define NF4_TRACE_INIT unsigned long long* const nf4_trace_buf = blockIdx.x < 2 ? g_trace : nullptr
 #define NF4_PROBE(ev, idx)                                                               \
   do {                                                                                   \
-    if (blockIdx.x < 2 && g_trace != nullptr && (idx) < kTraceSlots)                     \
-      g_trace[(blockIdx.x * kTraceEvents + (ev)) * kTraceSlots + (idx)] =                 \
+    if (nf4_trace_buf != nullptr && (idx) < kTraceSlots)                                 \
+      nf4_trace_buf[(blockIdx.x * kTraceEvents + (ev)) * kTraceSlots + (idx)] =           \
           static_cast<unsigned long long>(clock64());                                    \
   } while (0)
 #else
+#define NF4_TRACE_INIT do { } while (0)
 #define NF4_PROBE(ev, idx) do { } while (0)
 #endif
 

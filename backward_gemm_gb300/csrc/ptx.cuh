@@ -212,6 +212,35 @@ __device__ __forceinline__ bool flag_wait(uint32_t addr, uint32_t want, volatile
   }
 }
 
+// Spin until the counter word is at least `want` (it only grows); bounded like
+// mbar_wait.  The value read is left in *seen, so a caller that is behind can
+// consume every step the counter already covers without reading it again.
+__device__ __forceinline__ bool flag_wait_ge(uint32_t addr, uint32_t want, volatile int* abort_flag,
+                                             uint32_t* seen) {
+  uint32_t v = ld_acquire_shared(addr);
+  if (v >= want) {
+    *seen = v;
+    return true;
+  }
+  const long long t0 = clock64();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i) {
+      v = ld_acquire_shared(addr);
+      if (v >= want) {
+        *seen = v;
+        return true;
+      }
+    }
+    if (abort_flag != nullptr && *abort_flag != 0) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      record_timeout(addr, want);
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- proxies
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor-core operand reads, TMA).

@@ -216,6 +216,36 @@ def test_batched_matches_single_and_oracle():
         assert_close(out.cpu().numpy(), ref, bound, str(p))
 
 
+def test_grouped_full_step_repeated_launches_are_identical():
+    """The 196-projection training step as one grouped launch, 12 times: no wait
+    may give up and every launch must give the same grad_A bit for bit.  (A
+    raw-ring slot shared by both converter groups once let a parity wait pass
+    on stale data: wrong values first, then a stall, after a few such launches.)"""
+    probs = CONFIGS["full_step"]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    items = []
+    for p in probs:
+        go = torch.randn((p.M, p.N), device="cuda", generator=g) * p.go_std
+        w = nb().NF4Weight(torch.randint(0, 256, (p.N, p.K // 2), dtype=torch.uint8, device="cuda",
+                                         generator=g),
+                           torch.rand((p.N, p.K // 64), device="cuda", generator=g) * 0.05, p.K, p.N)
+        items.append((go, w, torch.empty((p.M, p.K), device="cuda")))
+    ws = nb().batched_workspace(len(items))
+    watch = [0, 5, 6, 98, 195]  # q, up, down of layer 0; a middle and the last projection
+    first = None
+    for _ in range(12):
+        outs = nb().backward_a_batched(items, ws)
+        nb().check_error()
+        snap = [outs[i].clone() for i in watch]
+        if first is None:
+            first = snap
+        else:
+            for i, a, b in zip(watch, first, snap):
+                assert torch.equal(a, b), f"projection {i} differs between launches"
+    del items, outs, first
+
+
 def test_batched_bf16_only_matches_single():
     """A grouped launch whose problems all have bf16 grad_out (the deeper-ring
     layout) gives the single-problem results bit for bit."""
