@@ -81,7 +81,9 @@ constexpr int kNf4Bytes = BN * (BKC / 2);              // 64 rows n x 64 bytes
 constexpr int kABytes = BM * BN * 2;                   // 16 KB f16
 constexpr int kBBytes = BKC * BN * 2;                  // 16 KB f16
 constexpr int kOpBytes = kABytes + kBBytes;            // 32 KB
-constexpr int kEpiBufBytes = 32 * 128;                 // 32 rows x 32 fp32
+constexpr int kEpiCols = 16;                           // fp32 columns per epilogue store
+constexpr int kEpiBufBytes = 32 * kEpiCols * 4;        // 32 rows x 16 fp32 (64-byte rows)
+constexpr int kEpiBufs = 2;  // staging buffers per epilogue warp: a store drains while the next fills
 constexpr uint32_t kSigBytes = 16;
 constexpr long long kAbortLingerCycles = 4000000;  // ~2 ms: far longer than a copy's latency
 constexpr uint32_t kTmemCols = 2 * BK;
@@ -99,7 +101,7 @@ struct Layout {
   static constexpr int kRawOff = 0;
   static constexpr int kOpOff = kRawOff + RS * kRawBytes;
   static constexpr int kEpiOff = kOpOff + OS * kOpBytes;
-  static constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufBytes;
+  static constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufs * kEpiBufBytes;
   static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1;
   // misc: TMEM address, abort flag, the ready counter (and spare words), then the
   // 16-byte signal words: in CTA 0 one destination per (operand slot,
@@ -133,7 +135,7 @@ constexpr uint32_t kSbo = 1024;
 struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
   CUtensorMap tm_go;   // grad_out [M][N], box 128 rows x 128 bytes, 128B swizzle
   CUtensorMap tm_nf4;  // codes [N][K/2] bytes, box 64 rows x 64 bytes, 64B swizzle
-  CUtensorMap tm_out;  // grad_A [M][K] fp32, box 32 rows x 32 columns, 128B swizzle
+  CUtensorMap tm_out;  // grad_A [M][K] fp32, box 32 rows x 16 columns, 64B swizzle
   const float* scales;
   float* grad_A;
   int M, N, K, dtype;
@@ -273,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   NF4_TRACE_INIT;
+  if (threadIdx.x == 0) NF4_PROBE(44, 0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
@@ -592,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     const uint32_t tmem_empty_leader0 = mapa_shared(tmem_empty(0), 0);
-    uint8_t* buf = smem + kEpiOff + warp * kEpiBufBytes;
+    uint8_t* const buf0 = smem + kEpiOff + warp * kEpiBufs * kEpiBufBytes;
     uint32_t lt = 0;
     for (int t = cluster; t < total_tiles; t += nclusters, ++lt) {
       const Tile tl = tile_at(descs, count, t);
@@ -604,21 +607,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM + warp * 32;
       const uint32_t taddr = tmem_base + acc * BK + (static_cast<uint32_t>(warp * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BK / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, r);
+      for (int c = 0; c < BK / kEpiCols; ++c) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(taddr + c * kEpiCols, r);
         tmem_wait_ld();
-        if (lane == 0) bulk_wait_read<0>();  // the previous store has read `buf`
+        // Two staging buffers: at most one store may still be reading, so the
+        // one that last used this buffer is done with it.
+        uint8_t* const buf = buf0 + (c & 1) * kEpiBufBytes;
+        if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
         __syncwarp();
-        // Row `lane` of the 32 x 32 fp32 block, 128-byte swizzled.
+        // Row `lane` of the 32 x 16 fp32 block, 64-byte swizzled (16-byte chunk
+        // q of row r at q ^ ((r / 2) % 4)).
+        const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          *reinterpret_cast<uint4*>(buf + lane * 128 + ((static_cast<uint32_t>(q4) ^ (lane & 7)) << 4)) =
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<uint4*>(buf + lane * (kEpiCols * 4) + ((static_cast<uint32_t>(q4) ^ sw) << 4)) =
               make_uint4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * 32, row0, smem_addr(buf));
+          tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * kEpiCols, row0, smem_addr(buf));
           bulk_commit();
         }
       }
@@ -630,16 +638,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (threadIdx.x == 0) NF4_PROBE(36, lt);
       if (lane == 0) NF4_PROGRESS_SET(20 + warp, lt + 1);
-      if (lane == 0) bulk_wait_read<0>();
-      __syncwarp();
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
   }
 
   tc_fence_before();
+  if (threadIdx.x == 0) NF4_PROBE(44, 1);
   __syncthreads();
   cluster_sync();  // the leader's MMAs are done and no remote arrive is in flight
+  if (threadIdx.x == 0) NF4_PROBE(44, 2);
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, kTmemCols);
@@ -736,8 +744,8 @@ static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* sca
                  CU_TENSOR_MAP_SWIZZLE_64B))
     return NF4_ERR_CUDA;
   if (!encode_2d(&d->tm_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, grad_A, static_cast<uint64_t>(K),
-                 static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 4, 32, 32,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 4, kEpiCols, 32,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
     return NF4_ERR_CUDA;
   d->scales = scales;
   d->grad_A = grad_A;

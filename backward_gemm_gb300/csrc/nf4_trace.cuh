@@ -14,7 +14,9 @@ namespace nf4 {
 // Events: 0-15 converter warp after its operand-slot wait, 16-31 converter warp
 // done, 32/33/38 MMA before wait / after wait / after commit, 35/36 epilogue
 // tile start / end, 39 reference, 40 producer issue, 41 watcher sees stage,
-// 42 converter group leader sees raw data, 43 converter group leader starts.
+// 42 converter group leader sees raw data, 43 converter group leader starts,
+// 44 slot 0 kernel entry / slot 1 all roles done / slot 2 after the last
+// cluster barrier.
 //
 // Few-token kernel (small_m_kernel), CTAs 0 and 1 (k-tile 0, cluster ranks 0
 // and 1 when S > 1): slot s of events 0-6 and 8 is stage s.  0 producer issues
