@@ -165,10 +165,14 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int
   r.N = p->N;
   r.K = p->K;
   r.dtype = p->dtype;
+  // Output-column tiles vary fastest: the pairs running at the same time then
+  // share a few 256-row blocks of grad_out, which stay in L2 while every column
+  // tile of them is computed (row-block-fastest order made them stream grad_out
+  // from DRAM once per column tile when it does not fit in L2).
   const int local = t - p->tile_begin;
-  const int tm = p->tiles_m;
-  r.mt = local % tm;
-  r.kt = local / tm;
+  const int tk = p->tiles_k;
+  r.mt = local / tk;
+  r.kt = local % tk;
   r.ns = p->n_stages;
   return r;
 }

@@ -323,16 +323,34 @@ def bench_e2e(args, probs, host_go, set0, stream, dev, flops, world):
             "steps": steps}
 
 
+def kernel_source_digest() -> str:
+    """SHA-256 over the CUDA sources of the library (file names and contents)."""
+    import hashlib
+
+    csrc = os.path.join(ROOT, "backward_gemm_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
 def traffic_for(workload: str):
-    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary of
-    this workload, if one exists for the current kernel (else null)."""
+    """DRAM bytes (read + write) per launch of this workload's kernel, from the
+    committed ncu summary, or null when there is none or when the kernel sources
+    changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        return t.get(workload)
     except (OSError, ValueError):
         return None
+    if t.get("kernel_source_sha256") != kernel_source_digest():
+        return None
+    entry = t.get("workloads", {}).get(workload)
+    return None if entry is None else entry.get("dram_bytes_per_launch")
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
