@@ -45,6 +45,8 @@ SIGNATURES = {
     "nf4_dequantize_f16": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
     "nf4_backward_a": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "nf4_backward_a_ex": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "nf4_backward_a_ws_bytes": (_sz, [_i, _i]),
+    "nf4_backward_a_ws": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
     "nf4_backward_a_batched_workspace": (_sz, [_i]),
     "nf4_backward_a_batched": (_i, [C.POINTER(Nf4Problem), _i, _vp, _sz, _vp]),
     "nf4_check_error": (_i, [_vp]),
@@ -156,6 +158,37 @@ def backward_a(grad_out: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = 
     _check(lib().nf4_backward_a_ex(_ptr(grad_out), _dtype_code(grad_out), _ptr(w.scales),
                                    _ptr(w.data), _ptr(out), M, N, w.K, _stream()),
            "nf4_backward_a_ex")
+    return out
+
+
+def ws_workspace(M: int, N: int, device=None) -> torch.Tensor:
+    """Device workspace for :func:`backward_a_ws` (the f16 copy of grad_out)."""
+    n = int(lib().nf4_backward_a_ws_bytes(M, N))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def backward_a_ws(grad_out: torch.Tensor, w: NF4Weight, workspace: torch.Tensor | None = None,
+                  out: torch.Tensor | None = None):
+    """As :func:`backward_a`, through ``nf4_backward_a_ws``: grad_out is first
+    rounded to f16 into ``workspace`` by its own pass, and the GEMM loads the A
+    operand with TMA.  Same result as :func:`backward_a`, bit for bit."""
+    _require_cuda_contig("grad_out", grad_out)
+    M, N = grad_out.shape
+    if N != w.N:
+        raise ValueError(f"grad_out has N={N}, weight has N={w.N}")
+    if out is None:
+        out = torch.empty((M, w.K), dtype=torch.float32, device=grad_out.device)
+    _require_cuda_contig("out", out)
+    if out.dtype != torch.float32 or tuple(out.shape) != (M, w.K):
+        raise ValueError("out must be float32 [M, K]")
+    if workspace is None:
+        workspace = ws_workspace(M, N, grad_out.device)
+    _require_cuda_contig("workspace", workspace)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().nf4_backward_a_ws(_ptr(grad_out), _dtype_code(grad_out), _ptr(w.scales),
+                                   _ptr(w.data), _ptr(out), M, N, w.K, _ptr(workspace), nbytes,
+                                   _stream()),
+           "nf4_backward_a_ws")
     return out
 
 

@@ -74,7 +74,6 @@ constexpr int kConvGroups = 2;   // group g converts the stages it with it % 2 =
 constexpr int kGroupWarps = 8;   // warps per group (256 threads)
 constexpr int kConvWarps = kConvGroups * kGroupWarps;
 constexpr int kWatchWarp = kConvWarp0 + kConvWarps;       // 22
-constexpr int kThreads = (kWatchWarp + 1) * 32;           // 736
 
 constexpr int kGoBoxBytes = BM * 128;                  // one 128-byte-wide box of 128 rows
 constexpr int kNf4Bytes = BN * (BKC / 2);              // 64 rows n x 64 bytes
@@ -92,17 +91,27 @@ constexpr uint32_t kTmemCols = 2 * BK;
 // bytes of grad_out and the NF4 bytes, OS operand stages, the epilogue staging,
 // barriers and flags.  bf16 grad_out needs half the raw bytes of fp32, which
 // buys a deeper ring on both sides.
-template <int RS, int OS, int GOB>
+//
+// RA > 0 selects the pre-converted variant: grad_out was rounded to f16 by a
+// separate pass, and a TMA copy writes each stage's A operand straight into a
+// ring of RA A slots (no raw grad_out, no converter work on A); the operand
+// slots then hold B^T only.
+template <int RS, int OS, int GOB, int RA = 0>
 struct Layout {
+  static constexpr bool kPreA = RA > 0;
   static constexpr int kRawStages = RS;
   static constexpr int kOpStages = OS;
+  static constexpr int kAStages = RA;
   static constexpr int kGoBytes = GOB;
   static constexpr int kRawBytes = GOB + kNf4Bytes;
+  static constexpr int kOpSlotBytes = kPreA ? kBBytes : kOpBytes;
+  static constexpr int kBInOp = kPreA ? 0 : kABytes;  // offset of B^T in an operand slot
   static constexpr int kRawOff = 0;
-  static constexpr int kOpOff = kRawOff + RS * kRawBytes;
-  static constexpr int kEpiOff = kOpOff + OS * kOpBytes;
+  static constexpr int kAOff = kRawOff + RS * kRawBytes;
+  static constexpr int kOpOff = kAOff + RA * kABytes;
+  static constexpr int kEpiOff = kOpOff + OS * kOpSlotBytes;
   static constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufs * kEpiBufBytes;
-  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1;
+  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1 + 2 * RA;
   // misc: TMEM address, abort flag, the ready counter (and spare words), then the
   // 16-byte signal words: in CTA 0 one destination per (operand slot,
   // converter warp of a group), and one source.
@@ -111,20 +120,26 @@ struct Layout {
   static constexpr int kSigOff = kMiscOff + 32;
   static constexpr uint32_t kSigSrcOff = kSigOff + OS * kGroupWarps * kSigBytes;
   static constexpr int kSmemBytes = kSigSrcOff + kSigBytes + 1024;  // + alignment slack
+  // The pre-converted variant adds one warp: the A-operand producer.
+  static constexpr int kThreads = (kWatchWarp + 1 + (kPreA ? 1 : 0)) * 32;  // 736 or 768
+  static constexpr int kBoxes = kPreA ? 1 : 3;  // raw-ring boxes per stage
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
+  static_assert(kRawBytes % 1024 == 0 && kOpSlotBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
   static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
   static_assert(kReadyOff + 4 * OS <= kSigOff, "ready counter fits before the signal area");
-  static_assert(RS * 3 <= 32, "one producer lane per (raw slot, box)");
+  static_assert(RS * kBoxes <= 32 && RA <= 32, "one producer lane per (ring slot, box)");
   // Each raw slot must always be consumed by the same converter group.  A group
   // waits for a slot's phase by parity only; if the slot alternated between the
   // groups, a group could wait for phase k while phase k-1 (the other group's
   // stage, copy still in flight) is incomplete, and the completed phase k-2 has
-  // the same parity: the wait would pass on stale data.
-  static_assert(RS % kConvGroups == 0, "raw slots are not shared between converter groups");
+  // the same parity: the wait would pass on stale data.  The same holds for the
+  // operand slots, whose release the groups also wait for by parity.
+  static_assert(RS % kConvGroups == 0 && OS % kConvGroups == 0,
+                "ring slots are not shared between converter groups");
 };
 using LayoutF32 = Layout<2, 4, 2 * kGoBoxBytes>;  // any fp32 grad_out in the launch
 using LayoutBF16 = Layout<4, 4, kGoBoxBytes>;     // bf16 grad_out only
+using LayoutPreA = Layout<6, 4, 0, 7>;            // grad_out pre-converted to f16
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
 // 8 rows n per 1024-byte atom; atoms along k are kBLbo apart, atoms along n 1 KB.
@@ -237,7 +252,7 @@ __device__ __forceinline__ float cc_scale(const ConvCursor& c, uint32_t rank, in
 // committed, 2 MMA tiles committed, 3 watcher stages published, 4-19 stages
 // finished by converter warp 0-15, 20-23 tiles stored by epilogue warp 0-3.
 template <class L>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(L::kThreads, 1)
     bwd_a_kernel(const __grid_constant__ ProblemDesc single, const ProblemDesc* __restrict__ batch,
                  int count, int total_tiles) {
   constexpr int kRawStages = L::kRawStages;
@@ -245,7 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kGoBytes = L::kGoBytes;
   constexpr int kRawBytes = L::kRawBytes;
   constexpr int kRawOff = L::kRawOff;
+  // A-ring depth, 1 (never used) in the variants without an A ring so that the
+  // slot arithmetic below stays well defined.
+  constexpr int kAStages = L::kPreA ? L::kAStages : 1;
+  constexpr int kAOff = L::kAOff;
   constexpr int kOpOff = L::kOpOff;
+  constexpr int kOpSlotBytes = L::kOpSlotBytes;
   constexpr int kEpiOff = L::kEpiOff;
   constexpr int kBarOff = L::kBarOff;
   constexpr int kMiscOff = L::kMiscOff;
@@ -273,6 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 2 + i);
   };
   const uint32_t mma_done = bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 4);
+  // Pre-converted variant: A ring.  full_a lives in CTA 0 and counts the bytes
+  // of both CTAs' A copies; empty_a is signalled by the MMA commit in both.
+  auto full_a = [&](uint32_t i) { return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + i); };
+  auto empty_a = [&](uint32_t i) {
+    return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + kAStages + i);
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -299,6 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tmem_empty(i), 2 * kEpiWarps);  // epilogues of both CTAs (used in CTA 0)
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < L::kAStages; ++i) {  // none without an A ring
+      mbar_init(full_a(i), 1);  // CTA 0's A producer registers both CTAs' bytes
+      mbar_init(empty_a(i), 1);
+    }
     for (int i = 0; i < kOpStages; ++i)
       reinterpret_cast<volatile uint32_t*>(smem + kReadyOff)[i] = 0u;
     *abort_flag = 0;
@@ -321,11 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (ring slot, box) pair has its own lane: lane 3*slot + b issues box b of
     // the stages that use `slot` (b = 0 grad_out columns 0-31 (fp32) or 0-63
     // (bf16) and the stage's byte count, b = 1 fp32 columns 32-63, b = 2 the
-    // NF4 bytes).  Stages go in order and lane 0 alone waits for a slot (lanes
+    // NF4 bytes; the pre-converted variant has only the NF4 box, lane = slot).
+    // Stages go in order and lane 0 alone waits for a slot (lanes
     // of one warp waiting on different barriers would wake together).  Boxes may
     // land before the byte count is registered: the phase cannot complete while
     // that arrival is pending.
-    const int my_slot = lane / 3, box = lane % 3;
+    const int my_slot = lane / L::kBoxes;
+    const int box = L::kPreA ? 2 : lane % 3;
     if (lane == 0 && count == 1) {
       tma_prefetch_desc(&descs[0].tm_go);
       tma_prefetch_desc(&descs[0].tm_nf4);
@@ -335,7 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = cluster; ok && t < total_tiles; t += nclusters) {
       const Tile tl = tile_at(descs, count, t);
       const bool f32 = tl.dtype == NF4_F32;
-      const uint32_t bytes = (f32 ? 2 * kGoBoxBytes : kGoBoxBytes) + kNf4Bytes;
+      const uint32_t bytes =
+          L::kPreA ? kNf4Bytes : (f32 ? 2 * kGoBoxBytes : kGoBoxBytes) + kNf4Bytes;
       const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
       const int x_nf4 = tl.kt * (BK / 2) + static_cast<int>(rank) * (BKC / 2);
       const CUtensorMap* map = box == 2 ? &tl.p->tm_nf4 : &tl.p->tm_go;
@@ -353,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dst = sbase + kRawOff + slot * kRawBytes +
                                (box == 0 ? 0u : (box == 1 ? static_cast<uint32_t>(kGoBoxBytes)
                                                           : static_cast<uint32_t>(kGoBytes)));
-          if (box == 0) {
+          if (box == 0 || L::kPreA) {
             mbar_arrive_expect_tx(fb, bytes);
             NF4_PROBE(40, it);
           }
@@ -384,11 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // reads the ready counter only when it has caught up with it.  Descriptors of slot 0 are built once; a
       // slot's are those plus its offset in the 16-byte address field.
       constexpr uint32_t idesc = idesc_f16_f32(BMP, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
-      const uint64_t a_desc0 = smem_desc_sw128(sbase + kOpOff, 16, kSbo);
-      const uint64_t b_desc0 = smem_desc_sw128(sbase + kOpOff + kABytes, kBLbo, kSbo);
+      const uint64_t a_desc0 = smem_desc_sw128(sbase + (L::kPreA ? kAOff : kOpOff), 16, kSbo);
+      const uint64_t b_desc0 = smem_desc_sw128(sbase + kOpOff + L::kBInOp, kBLbo, kSbo);
       constexpr uint32_t kBStep = (2u * kSbo) >> 4;  // +2 n-groups per MMA K-step
       const uint32_t ready0 = sbase + kReadyOff;
-      uint32_t it = 0, lt = 0, slot = 0;
+      uint32_t it = 0, lt = 0, slot = 0, aslot = 0;
       uint32_t avail = 0;  // stages the watcher has published as ready
       bool ok = true;
       for (int t = cluster; ok && t < total_tiles; t += nclusters, ++lt) {
@@ -416,14 +449,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // word; a tcgen05.fence per stage would keep the MMAs of consecutive
           // stages from overlapping.
           NF4_PROBE(33, it);
-          const uint64_t off = static_cast<uint64_t>((slot * kOpBytes) >> 4);
-          const uint64_t a = a_desc0 + off, b = b_desc0 + off;
+          const uint64_t off = static_cast<uint64_t>((slot * kOpSlotBytes) >> 4);
+          const uint64_t a =
+              a_desc0 + (L::kPreA ? static_cast<uint64_t>((aslot * kABytes) >> 4) : off);
+          const uint64_t b = b_desc0 + off;
           // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
           tc_mma_f16_pair(d_tmem, a, b, idesc, s != 0 ? 1u : 0u);
           tc_mma_f16_pair(d_tmem, a + 2u, b + kBStep, idesc, 1u);
           tc_mma_f16_pair(d_tmem, a + 4u, b + 2u * kBStep, idesc, 1u);
           tc_mma_f16_pair(d_tmem, a + 6u, b + 3u * kBStep, idesc, 1u);
           tc_commit_pair(empty_op(slot), 0x3);
+          if constexpr (L::kPreA) {
+            tc_commit_pair(empty_a(aslot), 0x3);
+            aslot = (aslot + 1u == static_cast<uint32_t>(kAStages)) ? 0u : aslot + 1u;
+          }
           NF4_PROBE(38, it);
           NF4_PROGRESS_SET(1, it + 1);
           ++it;
@@ -456,6 +495,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = tile_at(descs, count, t);
         for (int s = 0; s < tl.ns; ++s, ++it) {
           const uint32_t slot = it % kOpStages;
+          if constexpr (L::kPreA) {
+            if (!mbar_wait_cluster(full_a(it % kAStages), (it / kAStages) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+          }
           if (!mbar_wait_cluster(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
             ok = false;
             break;
@@ -465,6 +510,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           NF4_PROGRESS_SET(3, it + 1);
         }
       }
+    }
+    __syncwarp();
+  } else if (L::kPreA && warp == kWatchWarp + 1) {
+    // ---------------------------------------------------------------- A producer (pre-converted)
+    // Each CTA copies its 128 rows x 64 columns of the f16 grad_out into an A
+    // slot as soon as the MMAs that last read the slot are done; both copies
+    // complete on CTA 0's full_a barrier, for which CTA 0 registers 2 x 16 KB.
+    // Lane `slot` issues the copies of that slot (a thread's bulk copies are
+    // served one after another); lane 0 alone waits.
+    const uint32_t full_a_leader0 = mapa_shared(full_a(0), 0);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = cluster; ok && t < total_tiles; t += nclusters) {
+      const Tile tl = tile_at(descs, count, t);
+      const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
+      for (int s = 0; s < tl.ns; ++s, ++it) {
+        const uint32_t slot = it % kAStages;
+        bool free_slot = true;
+        if (lane == 0)
+          free_slot = mbar_wait_cluster(empty_a(slot), ((it / kAStages) & 1u) ^ 1u, abort_flag);
+        if (!__shfl_sync(0xFFFFFFFFu, free_slot, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == static_cast<int>(slot)) {
+          if (rank == 0) mbar_arrive_expect_tx(full_a(slot), 2u * kABytes);
+          tma_load_2d_pair(sbase + kAOff + slot * kABytes, &tl.p->tm_go, s * BN, row0,
+                           full_a_leader0 + 8u * slot);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && ok) {
+      // The last commits into this CTA's empty_a barriers (they also mean that
+      // the last copies landed: their MMAs read them) must arrive before exit.
+      for (uint32_t i = (it > kAStages ? it - kAStages : 0u); i < it; ++i)
+        mbar_wait_cluster(empty_a(i % kAStages), (i / kAStages) & 1u, nullptr);
     }
     __syncwarp();
   } else if (warp >= kConvWarp0) {
@@ -520,7 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Raw inputs of this thread -> registers; then the raw slot is released.
       const uint8_t* raw = smem + kRawOff + rslot * kRawBytes;
       uint4 g[8];
-      if (f32) {
+      if constexpr (L::kPreA) {
+        (void)f32;
+      } else if (f32) {
         const uint8_t* src = raw + ahalf * kGoBoxBytes + ar * 128;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -542,13 +626,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      ((it / kOpStages) & 1u) ^ 1u, abort_flag)))
         break;
       if (probe) NF4_PROBE(cw, it);
-      uint8_t* a_op = smem + kOpOff + oslot * kOpBytes;
-      uint8_t* b_op = a_op + kABytes;
+      uint8_t* a_op = smem + kOpOff + oslot * kOpSlotBytes;
+      uint8_t* b_op = a_op + L::kBInOp;
 
       // grad_out -> f16 A operand (K-major, 128B swizzle: chunk c of row r at c ^ (r % 8)).
       uint8_t* a_row = a_op + ar * 128;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < (L::kPreA ? 0 : 4); ++i) {
         uint4 h;
         if (f32) {
           const uint4 x0 = g[2 * i], x1 = g[2 * i + 1];
@@ -660,7 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // copies in flight into this CTA's shared memory (on the normal path the
   // watcher waits for all of them): keep the CTA resident for a bounded time
   // so that they land before its shared memory is released.
-  if (rank == 0 && threadIdx.x == 0 && (*abort_flag != 0 || *(volatile unsigned int*)&g_status != 0)) {
+  // In the pre-converted variant CTA 1's own A copies complete only on CTA 0's
+  // barrier, so CTA 1 cannot see them land: it lingers too.
+  if ((rank == 0 || L::kPreA) && threadIdx.x == 0 &&
+      (*abort_flag != 0 || *(volatile unsigned int*)&g_status != 0)) {
     const long long t0 = clock64();
     while (clock64() - t0 < kAbortLingerCycles) {
     }
@@ -683,6 +770,46 @@ __global__ void upload_descs_kernel(const __grid_constant__ DescChunk chunk, Pro
   uint4* out = reinterpret_cast<uint4*>(dst);
   const int words = n * static_cast<int>(sizeof(ProblemDesc) / sizeof(uint4));
   for (int i = threadIdx.x; i < words; i += blockDim.x) out[i] = src[i];
+}
+
+// ------------------------------------------------------------------ f16 pre-pass
+// grad_out [M][N] (fp32 or bf16) -> f16 [M][ldh], ldh = N rounded up to 8:
+// the A operand of the pre-converted GEMM variant, with the same rounding the
+// converter warps apply (bf16 widened exactly to fp32, then fp32 -> f16 to
+// nearest even).  One thread per 8 elements of a row (16 bytes written);
+// columns N..ldh-1 are written as zeros (the GEMM's tensor map ends at N and
+// never reads them).  Pure streaming: coalesced 16-byte loads and stores.
+__global__ void __launch_bounds__(256) to_f16_kernel(const void* __restrict__ src, int f32,
+                                                     uint16_t* __restrict__ dst, int M, int N,
+                                                     int ldh) {
+  const int groups = ldh >> 3;
+  const int64_t total = static_cast<int64_t>(M) * groups;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t m = i / groups;
+    const int c = static_cast<int>(i - m * groups) << 3;
+    uint4 h;
+    if (f32) {
+      // N % 4 == 0: a group is either whole, half (4 columns) or past N.
+      const float4* row = reinterpret_cast<const float4*>(static_cast<const float*>(src) + m * N);
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 a = c < N ? __ldcs(row + (c >> 2)) : z;
+      const float4 b = c + 4 < N ? __ldcs(row + (c >> 2) + 1) : z;
+      h.x = pack_f16x2(a.x, a.y);
+      h.y = pack_f16x2(a.z, a.w);
+      h.z = pack_f16x2(b.x, b.y);
+      h.w = pack_f16x2(b.z, b.w);
+    } else {
+      // N % 8 == 0: whole groups only (ldh == N).
+      const uint4 w = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) +
+                                                            m * N + c));
+      h.x = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+      h.y = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+      h.z = pack_f16x2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+      h.w = pack_f16x2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+    }
+    *reinterpret_cast<uint4*>(dst + m * ldh + c) = h;
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -734,15 +861,9 @@ static int check_problem(const void* go, int dtype, const float* scales, const u
   return NF4_OK;
 }
 
-static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* scales,
-                     const uint8_t* data, float* grad_A, int M, int N, int K) {
-  std::memset(d, 0, sizeof(*d));
-  const bool f32 = dtype == NF4_F32;
-  if (!encode_2d(&d->tm_go, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                 go, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
-                 static_cast<uint64_t>(N) * (f32 ? 4 : 2), f32 ? 32 : 64, BM,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return NF4_ERR_CUDA;
+// Everything of a descriptor but the grad_out map.
+static int fill_desc_rest(ProblemDesc* d, int dtype, const float* scales, const uint8_t* data,
+                          float* grad_A, int M, int N, int K) {
   if (!encode_2d(&d->tm_nf4, CU_TENSOR_MAP_DATA_TYPE_UINT8, data, static_cast<uint64_t>(K / 2),
                  static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), BKC / 2, BN,
                  CU_TENSOR_MAP_SWIZZLE_64B))
@@ -762,6 +883,64 @@ static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* sca
   d->n_stages = (N + BN - 1) / BN;
   d->tile_begin = 0;
   return NF4_OK;
+}
+
+static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* scales,
+                     const uint8_t* data, float* grad_A, int M, int N, int K) {
+  std::memset(d, 0, sizeof(*d));
+  const bool f32 = dtype == NF4_F32;
+  if (!encode_2d(&d->tm_go, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 go, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                 static_cast<uint64_t>(N) * (f32 ? 4 : 2), f32 ? 32 : 64, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return NF4_ERR_CUDA;
+  return fill_desc_rest(d, dtype, scales, data, grad_A, M, N, K);
+}
+
+// Row pitch (elements) and bytes of the f16 copy of an M x N grad_out.
+static inline int f16_pitch(int N) { return (N + 7) & ~7; }
+static inline size_t f16_bytes(int M, int N) {
+  return sizeof(uint16_t) * static_cast<size_t>(M) * static_cast<size_t>(f16_pitch(N));
+}
+
+// Descriptor of the pre-converted variant: the A map reads the f16 copy (box
+// 64 columns x 128 rows, 128-byte swizzle = the K-major A operand layout).
+static int fill_desc_pre(ProblemDesc* d, const uint16_t* go_f16, const float* scales,
+                         const uint8_t* data, float* grad_A, int M, int N, int K) {
+  std::memset(d, 0, sizeof(*d));
+  if (!encode_2d(&d->tm_go, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, go_f16, static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(f16_pitch(N)) * 2, BN, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return NF4_ERR_CUDA;
+  // dtype is not read by this variant (its A operand is f16 already).
+  return fill_desc_rest(d, NF4_BF16, scales, data, grad_A, M, N, K);
+}
+
+static int sm_count(int* out) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return NF4_ERR_CUDA;
+  if (cached[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+      return NF4_ERR_CUDA;
+    cached[dev] = sms;
+  }
+  *out = cached[dev];
+  return NF4_OK;
+}
+
+static int launch_to_f16(const void* go, int dtype, uint16_t* dst, int M, int N,
+                         cudaStream_t stream) {
+  int sms = 0;
+  const int rc = sm_count(&sms);
+  if (rc != NF4_OK) return rc;
+  const int64_t work = static_cast<int64_t>(M) * (f16_pitch(N) >> 3);
+  const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sms) * 8);
+  to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(go, dtype == NF4_F32 ? 1 : 0,
+                                                                    dst, M, N, f16_pitch(N));
+  return cudaGetLastError() == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
 
 // Largest number of pairs of CTAs of kernel configuration L that fit on the
@@ -787,7 +966,7 @@ static int max_clusters(int* out) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(L::kThreads, 1, 1);
     cfg.dynamicSmemBytes = L::kSmemBytes;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -815,7 +994,7 @@ static int launch_layout(const ProblemDesc& single, const ProblemDesc* batch, in
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(L::kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -1034,6 +1213,37 @@ extern "C" int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float
 extern "C" int nf4_backward_a(const float* grad_out, const float* scales, const uint8_t* data,
                               float* grad_A, int M, int N, int K, void* stream) {
   return nf4_backward_a_ex(grad_out, NF4_F32, scales, data, grad_A, M, N, K, stream);
+}
+
+extern "C" size_t nf4_backward_a_ws_bytes(int M, int N) {
+  if (M <= 0 || N <= 0) return 0;
+  return f16_bytes(M, N);
+}
+
+extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float* scales,
+                                 const uint8_t* data, float* grad_A, int M, int N, int K,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_problem(grad_out, go_dtype, scales, data, grad_A, M, N, K);
+  if (rc != NF4_OK || M == 0) return rc;
+  if (N == 0) {
+    return cudaMemsetAsync(grad_A, 0, sizeof(float) * static_cast<size_t>(M) * K,
+                           as_stream(stream)) == cudaSuccess
+               ? NF4_OK
+               : NF4_ERR_CUDA;
+  }
+  if (M <= small_m::g_max_m.load())
+    return small_m::run(grad_out, go_dtype, scales, data, grad_A, M, N, K, as_stream(stream));
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < f16_bytes(M, N))
+    return NF4_ERR_WORKSPACE;
+  uint16_t* go_f16 = static_cast<uint16_t*>(workspace);
+  ProblemDesc d;
+  rc = fill_desc_pre(&d, go_f16, scales, data, grad_A, M, N, K);
+  if (rc != NF4_OK) return rc;
+  const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
+  if (tiles > INT_MAX) return NF4_ERR_INVALID;
+  rc = launch_to_f16(grad_out, go_dtype, go_f16, M, N, as_stream(stream));
+  if (rc != NF4_OK) return rc;
+  return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles), as_stream(stream));
 }
 
 extern "C" size_t nf4_backward_a_batched_workspace(int count) {

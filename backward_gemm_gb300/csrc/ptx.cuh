@@ -264,6 +264,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// The same load issued by either CTA of a pair into its own shared memory, with
+// the completion counted on an mbarrier of the pair's leader CTA (`bar` is that
+// barrier's cluster address, from mapa_shared).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x,
+                                                 int32_t y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
 // 2-D tiled bulk tensor store shared -> global (rows/columns outside the tensor
 // are not written), tracked by the bulk async-group of the issuing thread.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src) {

@@ -126,7 +126,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm
-def make_input_sets(probs, copies, dev):
+def make_input_sets(probs, copies, dev, entry="plain"):
     import backward_gemm_gb300 as nb
 
     sets = []
@@ -142,18 +142,28 @@ def make_input_sets(probs, copies, dev):
             w = nb.quantize(torch.from_numpy(B).to(dev))
             out = torch.empty((p.M, p.K), dtype=torch.float32, device=dev)
             items.append((go_t, w, out))
-        ws = nb.batched_workspace(len(items), dev) if len(items) > 1 else None
+        if len(items) > 1:
+            ws = nb.batched_workspace(len(items), dev)
+        elif entry == "ws":
+            ws = nb.ws_workspace(probs[0].M, probs[0].N, dev)
+        else:
+            ws = None
         sets.append((items, ws))
     torch.cuda.synchronize()
     return sets, base_go
 
 
 def run_step(items, ws):
+    """One step through the public API.  A single problem with a workspace runs
+    nf4_backward_a_ws (f16 pre-pass, then the GEMM), without one nf4_backward_a_ex."""
     import backward_gemm_gb300 as nb
 
     if len(items) == 1:
         go, w, out = items[0]
-        nb.backward_a(go, w, out=out)
+        if ws is None:
+            nb.backward_a(go, w, out=out)
+        else:
+            nb.backward_a_ws(go, w, ws, out=out)
     else:
         nb.backward_a_batched(items, ws)
 
@@ -172,9 +182,11 @@ def bench_ours(args, rank, world, dev):
     probs = workloads()[args.workload]
     flops = sum(p.flops for p in probs)
     alg_bytes = sum(p.algorithmic_bytes for p in probs)
-    per_set = sum(p.go_bytes + 4 * p.M * p.K + p.K * p.N // 2 for p in probs)
+    entry = args.entry if len(probs) == 1 and probs[0].M > SMALL_M_MAX else "plain"
+    per_set = sum(p.go_bytes + 4 * p.M * p.K + p.K * p.N // 2
+                  + (2 * p.M * p.N if entry == "ws" else 0) for p in probs)
     copies = max(2, min(16, -(-2 * L2_BYTES // per_set)))
-    sets, host_go = make_input_sets(probs, copies, dev)
+    sets, host_go = make_input_sets(probs, copies, dev, entry)
     stream = torch.cuda.Stream(device=dev)
 
     with torch.cuda.stream(stream):
@@ -238,7 +250,7 @@ def bench_ours(args, rank, world, dev):
     roof["peak_source"] = (f"{peak_kind} {'sustained' if long_run else 'burst'} bf16 "
                            "(f16 nominal rate = bf16)" if roof["bound"] == "tensor"
                            else f"{peak_kind} HBM copy")
-    roof["kernel"] = kernel_names(probs)
+    roof["kernel"] = kernel_names(probs, entry)
 
     line = {
         "metric": "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline",
@@ -249,10 +261,12 @@ def bench_ours(args, rank, world, dev):
                    "gflop_per_step": flops / 1e9, "algorithmic_mb_per_step": alg_bytes / 1e6,
                    "l2": f"rotating {copies} input sets, {copies * per_set / 2**20:.0f} MiB > L2",
                    "timing": f"CUDA graph of {copies} steps, CUDA events",
+                   "entry": "nf4_backward_a_ws" if entry == "ws" else (
+                       "nf4_backward_a_ex" if len(probs) == 1 else "nf4_backward_a_batched"),
                    "parallelism": f"dp{world} (M-sharded replicas, no collective)"},
         "e2e": e2e,
         "roofline": roof,
-        "gpu_launches": K * launches_per_step(probs),
+        "gpu_launches": K * launches_per_step(probs, entry),
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu:
@@ -264,23 +278,26 @@ SMALL_M_MAX = 64      # the library's default few-token limit (nf4_set_small_m_m
 DESCS_PER_UPLOAD = 60  # descriptors per upload kernel of a grouped launch
 
 
-def kernel_names(probs) -> str:
+def kernel_names(probs, entry="plain") -> str:
     """The library kernels one step launches: the few-token kernel for M <= 64,
-    the pair kernel otherwise."""
+    the pair kernel otherwise (after the f16 pre-pass with the ws entry)."""
     names = []
     if any(p.M <= SMALL_M_MAX for p in probs):
         names.append("small_m_kernel")
     if any(p.M > SMALL_M_MAX for p in probs):
         names.append("bwd_a_kernel")
+        if entry == "ws":
+            names.insert(0, "to_f16_kernel")
     return " + ".join(names)
 
 
-def launches_per_step(probs) -> int:
+def launches_per_step(probs, entry="plain") -> int:
     """Kernel launches of one step through the C ABI: a single problem is one
-    launch; a grouped call launches one few-token kernel per problem with
-    M <= 64, then the descriptor uploads and one grouped GEMM for the rest."""
+    launch (two with the ws entry: the f16 pre-pass and the GEMM); a grouped
+    call launches one few-token kernel per problem with M <= 64, then the
+    descriptor uploads and one grouped GEMM for the rest."""
     if len(probs) == 1:
-        return 1
+        return 2 if entry == "ws" and probs[0].M > SMALL_M_MAX else 1
     few = sum(1 for p in probs if p.M <= SMALL_M_MAX)
     rest = len(probs) - few
     return few + ((-(-rest // DESCS_PER_UPLOAD) + 1) if rest else 0)
@@ -445,6 +462,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="q_proj", choices=sorted(workloads()))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--entry", default="plain", choices=["plain", "ws"],
+                    help="single-problem entry point: nf4_backward_a_ex, or nf4_backward_a_ws "
+                         "(f16 pre-pass into a workspace, then the GEMM)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -105,6 +105,34 @@ int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float* scales,
                       const uint8_t* data, float* grad_A, int M, int N, int K, void* stream);
 
 /*
+ * Bytes of device workspace nf4_backward_a_ws needs for an M x N grad_out: an
+ * f16 copy with rows padded to a multiple of 8 elements, 2 * M * ((N + 7) & ~7)
+ * bytes (0 when M or N is not positive).
+ */
+size_t nf4_backward_a_ws_bytes(int M, int N);
+
+/*
+ * As nf4_backward_a_ex, in two launches on `stream`: a streaming pass rounds
+ * grad_out to f16 (the rounding the GEMM applies to its A operand anyway: page
+ * above, build_ptx "PHASE 1", cvt.rn.f16) into `workspace`, then the GEMM loads
+ * its A operand from that copy with TMA instead of converting it in shared
+ * memory.  The result equals nf4_backward_a_ex's bit for bit.  The pages have
+ * no counterpart of the split: it trades 6 (fp32) or 4 (bf16) bytes of HBM
+ * traffic per grad_out element for shared-memory bandwidth inside the GEMM.
+ *   workspace        caller-owned device memory, 256-byte aligned, at least
+ *                    nf4_backward_a_ws_bytes(M, N) bytes; overwritten; must not
+ *                    be used by anything else until the stream has run the call
+ *   workspace_bytes  its size; too small, NULL or misaligned returns
+ *                    NF4_ERR_WORKSPACE and enqueues nothing
+ * M at most the few-token limit (nf4_set_small_m_max), M == 0 and N == 0 take
+ * the same paths as nf4_backward_a_ex and do not touch the workspace (it may
+ * then be NULL).
+ */
+int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float* scales,
+                      const uint8_t* data, float* grad_A, int M, int N, int K, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
  * Few-token path.  A call of nf4_backward_a / nf4_backward_a_ex with M at most
  * this limit runs a kernel built for small M: the weight is streamed once
  * (256 output columns per CTA, all tokens at once) and the shared dimension N

@@ -45,15 +45,20 @@ def sample_rows(M: int, n: int = 12, seed: int = 0) -> np.ndarray:
     return np.array(rows, dtype=np.int32)
 
 
-def run_problem(p: Problem, rows=None, check_codes: bool = True):
+def run_problem(p: Problem, rows=None, check_codes: bool = True, entry: str = "plain"):
     """Quantise B and run the GEMM on the GPU; compare with the oracle.  rows=None
-    compares every element, otherwise only the given rows of grad_A."""
+    compares every element, otherwise only the given rows of grad_A.  entry
+    "ws" runs nf4_backward_a_ws (f16 pre-pass into a workspace) instead of
+    nf4_backward_a_ex."""
     import backward_gemm_gb300 as nb
 
     go = make_grad_out(p)
     B = make_weight(p)
     w = nb.quantize(torch.from_numpy(B).cuda())
-    ga = nb.backward_a(to_device_go(go, p.go_dtype), w)
+    if entry == "ws":
+        ga = nb.backward_a_ws(to_device_go(go, p.go_dtype), w)
+    else:
+        ga = nb.backward_a(to_device_go(go, p.go_dtype), w)
     nb.check_error()
     data_o, scales_o = oracle.quantize(B)
     if check_codes:

@@ -361,3 +361,77 @@ FULL = [(name, p) for name in ("q_proj", "mlp", "large") for p in CONFIGS[name]]
 @pytest.mark.parametrize("name,p", FULL, ids=[p.name for _, p in FULL])
 def test_full_size_sampled_rows(name, p):
     run_problem(p, rows=sample_rows(p.M, 10, p.seed))
+
+
+# ---------------------------------------------------------------- pre-converted entry point
+# nf4_backward_a_ws rounds grad_out to f16 in a pass of its own and feeds the
+# GEMM's A operand by TMA; the tile order, the MMAs and their order are those of
+# the plain entry point, so the two results agree bit for bit.
+WS = SMALL + [
+    Problem(300, 196, 640, F32, 1.0, 0.02, True, 40, "ws-pitch-pad"),   # f16 rows padded to 200
+    Problem(200, 4, 192, F32, 1.0, 0.02, False, 41, "ws-n4"),            # one half group per row
+    Problem(513, 1032, 768, BF16, 1e-2, 0.02, True, 42, "ws-bf16-3-row-pairs"),
+]
+
+
+@pytest.mark.parametrize("p", WS, ids=lambda p: p.name)
+def test_ws_full_check(p):
+    with nb().small_m_max(0):
+        run_problem(p, entry="ws")
+
+
+@pytest.mark.parametrize("p", WS, ids=lambda p: p.name)
+def test_ws_equals_plain_bitwise(p):
+    go = to_device_go(make_grad_out(p), p.go_dtype)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    with nb().small_m_max(0):
+        plain = nb().backward_a(go, w)
+        pre = nb().backward_a_ws(go, w)
+    nb().check_error()
+    assert torch.equal(plain, pre)
+
+
+@pytest.mark.parametrize("name,p", FULL, ids=[p.name for _, p in FULL])
+def test_ws_full_size_sampled_rows_and_bitwise(name, p):
+    if p.M <= 64:
+        pytest.skip("few-token shapes take the same path through both entry points")
+    run_problem(p, rows=sample_rows(p.M, 6, p.seed + 1), check_codes=False, entry="ws")
+    go = to_device_go(make_grad_out(p), p.go_dtype)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    ws = nb().ws_workspace(p.M, p.N)
+    first = nb().backward_a_ws(go, w, ws)
+    again = nb().backward_a_ws(go, w, ws)
+    plain = nb().backward_a(go, w)
+    nb().check_error()
+    assert torch.equal(first, again)
+    assert torch.equal(first, plain)
+
+
+def test_ws_rejects_bad_workspace_without_launching():
+    import ctypes as C
+
+    L = nb().lib()
+    p = Problem(300, 192, 640, F32, 1.0, 0.02, False, 43)
+    go = to_device_go(make_grad_out(p), F32)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    need = int(L.nf4_backward_a_ws_bytes(p.M, p.N))
+    assert need == 2 * p.M * ((p.N + 7) // 8 * 8)
+    out = torch.full((p.M, p.K), 7.0, device="cuda")
+    ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
+
+    def call(ptr, nbytes, M=p.M):
+        return L.nf4_backward_a_ws(C.c_void_p(go.data_ptr()), F32, C.c_void_p(w.scales.data_ptr()),
+                                   C.c_void_p(w.data.data_ptr()), C.c_void_p(out.data_ptr()), M,
+                                   p.N, p.K, ptr, nbytes, None)
+
+    with nb().small_m_max(64):
+        assert call(None, 0) == nb().NF4_ERR_WORKSPACE
+        assert call(C.c_void_p(ws.data_ptr()), need - 1) == nb().NF4_ERR_WORKSPACE
+        assert call(C.c_void_p(ws.data_ptr() + 16), need) == nb().NF4_ERR_WORKSPACE
+        torch.cuda.synchronize()
+        assert bool((out == 7.0).all())
+        # Few tokens: the few-token kernel, no workspace needed.
+        assert call(None, 0, M=16) == nb().NF4_OK
+        nb().check_error()
+        assert call(C.c_void_p(ws.data_ptr()), need) == nb().NF4_OK
+        nb().check_error()
