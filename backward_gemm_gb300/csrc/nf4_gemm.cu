@@ -77,6 +77,7 @@ constexpr int kWatchWarp = kConvWarp0 + kConvWarps;       // 22
 
 constexpr int kGoBoxBytes = BM * 128;                  // one 128-byte-wide box of 128 rows
 constexpr int kNf4Bytes = BN * (BKC / 2);              // 64 rows n x 64 bytes
+constexpr int kScaleBytes = BN * 16;                   // 64 rows n x 4 block scales
 constexpr int kABytes = BM * BN * 2;                   // 16 KB f16
 constexpr int kBBytes = BKC * BN * 2;                  // 16 KB f16
 constexpr int kOpBytes = kABytes + kBBytes;            // 32 KB
@@ -88,8 +89,8 @@ constexpr long long kAbortLingerCycles = 4000000;  // ~2 ms: far longer than a c
 constexpr uint32_t kTmemCols = 2 * BK;
 
 // Shared-memory layout of one kernel configuration: RS raw stages holding GOB
-// bytes of grad_out and the NF4 bytes, OS operand stages, the epilogue staging,
-// barriers and flags.  bf16 grad_out needs half the raw bytes of fp32, which
+// bytes of grad_out, the NF4 bytes and the stage's block scales, OS operand
+// stages, the epilogue staging, barriers and flags.  bf16 grad_out needs half the raw bytes of fp32, which
 // buys a deeper ring on both sides.
 //
 // RA > 0 selects the pre-converted variant: grad_out was rounded to f16 by a
@@ -103,7 +104,8 @@ struct Layout {
   static constexpr int kOpStages = OS;
   static constexpr int kAStages = RA;
   static constexpr int kGoBytes = GOB;
-  static constexpr int kRawBytes = GOB + kNf4Bytes;
+  static constexpr int kRawBytes = GOB + kNf4Bytes + kScaleBytes;
+  static constexpr int kScaleOff = GOB + kNf4Bytes;  // within a raw slot
   static constexpr int kOpSlotBytes = kPreA ? kBBytes : kOpBytes;
   static constexpr int kBInOp = kPreA ? 0 : kABytes;  // offset of B^T in an operand slot
   static constexpr int kRawOff = 0;
@@ -122,7 +124,7 @@ struct Layout {
   static constexpr int kSmemBytes = kSigSrcOff + kSigBytes + 1024;  // + alignment slack
   // The pre-converted variant adds one warp: the A-operand producer.
   static constexpr int kThreads = (kWatchWarp + 1 + (kPreA ? 1 : 0)) * 32;  // 736 or 768
-  static constexpr int kBoxes = kPreA ? 1 : 3;  // raw-ring boxes per stage
+  static constexpr int kBoxes = kPreA ? 2 : 4;  // raw-ring boxes per stage
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kRawBytes % 1024 == 0 && kOpSlotBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
   static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
@@ -138,7 +140,7 @@ struct Layout {
                 "ring slots are not shared between converter groups");
 };
 using LayoutF32 = Layout<2, 4, 2 * kGoBoxBytes>;  // any fp32 grad_out in the launch
-using LayoutBF16 = Layout<4, 4, kGoBoxBytes>;     // bf16 grad_out only
+using LayoutBF16 = Layout<2, 4, kGoBoxBytes>;     // bf16 grad_out only
 using LayoutPreA = Layout<6, 4, 0, 7>;            // grad_out pre-converted to f16
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
@@ -148,23 +150,30 @@ constexpr uint32_t kSbo = 1024;
 
 // ------------------------------------------------------------------ problems
 struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
-  CUtensorMap tm_go;   // grad_out [M][N], box 128 rows x 128 bytes, 128B swizzle
-  CUtensorMap tm_nf4;  // codes [N][K/2] bytes, box 64 rows x 64 bytes, 64B swizzle
-  CUtensorMap tm_out;  // grad_A [M][K] fp32, box 32 rows x 16 columns, 64B swizzle
+  CUtensorMap tm_go;      // grad_out [M][N], box 128 rows x 128 bytes, 128B swizzle
+  CUtensorMap tm_nf4;     // codes [N][K/2] bytes, box 64 rows x 64 bytes, 64B swizzle
+  CUtensorMap tm_out;     // grad_A [M][K] fp32, box 32 rows x 16 columns, 64B swizzle
+  CUtensorMap tm_scales;  // scales [N][K/64] fp32, box 64 rows x 4 (if scale_tma)
   const float* scales;
   float* grad_A;
   int M, N, K, dtype;
   int tiles_m, tiles_k, n_stages, tile_begin;  // tiles_m counts 256-row pair tiles
+  // 1: the block scales of a stage travel with its NF4 bytes as one more TMA
+  // box (needs K % 256 == 0 and 16-byte aligned scales, so that the scale rows
+  // are 16-byte strided); 0: each converter thread loads its scale from global
+  // memory a turn ahead of its use.
+  int scale_tma;
 };
 
 static_assert(sizeof(ProblemDesc) % 16 == 0, "descriptor copy granularity");
+static_assert(sizeof(ProblemDesc) == 640, "descriptor size (the no-allocation array holds 256)");
 
 // One pair tile of one problem, with the problem's fields read once into
 // registers (the inline-asm memory clobbers would otherwise force reloads).
 struct Tile {
   const ProblemDesc* p;
   int M, N, K, dtype;
-  int mt, kt, ns;
+  int mt, kt, ns, stma;
 };
 
 __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int t) {
@@ -189,6 +198,7 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int
   r.mt = local / tk;
   r.kt = local % tk;
   r.ns = p->n_stages;
+  r.stma = p->scale_tma;
   return r;
 }
 
@@ -196,7 +206,7 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int
 // next, with the fields of that tile's problem needed for the scale loads.
 struct ConvCursor {
   int t, s, ns, kt, N, KB;
-  bool f32;
+  bool f32, stma;
   const float* scales;
 };
 
@@ -209,6 +219,7 @@ __device__ __forceinline__ void cc_load(ConvCursor& c, const ProblemDesc* descs,
     c.N = tl.N;
     c.KB = tl.K >> 6;
     c.f32 = tl.dtype == NF4_F32;
+    c.stma = tl.stma != 0;
     c.scales = tl.p->scales;
   }
 }
@@ -222,6 +233,7 @@ __device__ __forceinline__ void cc_start(ConvCursor& c, int t0, const ProblemDes
   c.N = 0;
   c.KB = 0;
   c.f32 = true;
+  c.stma = false;
   c.scales = nullptr;
   cc_load(c, descs, count, total_tiles);
 }
@@ -348,16 +360,17 @@ __global__ void __launch_bounds__(L::kThreads, 1)
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA producer
     // A thread's bulk-tensor copies are served one after another, so every
-    // (ring slot, box) pair has its own lane: lane 3*slot + b issues box b of
+    // (ring slot, box) pair has its own lane: lane 4*slot + b issues box b of
     // the stages that use `slot` (b = 0 grad_out columns 0-31 (fp32) or 0-63
     // (bf16) and the stage's byte count, b = 1 fp32 columns 32-63, b = 2 the
-    // NF4 bytes; the pre-converted variant has only the NF4 box, lane = slot).
+    // NF4 bytes, b = 3 the block scales; the pre-converted variant has only
+    // boxes 2 (with the byte count) and 3, lane 2*slot + b - 2).
     // Stages go in order and lane 0 alone waits for a slot (lanes
     // of one warp waiting on different barriers would wake together).  Boxes may
     // land before the byte count is registered: the phase cannot complete while
     // that arrival is pending.
     const int my_slot = lane / L::kBoxes;
-    const int box = L::kPreA ? 2 : lane % 3;
+    const int box = L::kPreA ? 2 + (lane & 1) : (lane & 3);
     if (lane == 0 && count == 1) {
       tma_prefetch_desc(&descs[0].tm_go);
       tma_prefetch_desc(&descs[0].tm_nf4);
@@ -367,12 +380,17 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     for (int t = cluster; ok && t < total_tiles; t += nclusters) {
       const Tile tl = tile_at(descs, count, t);
       const bool f32 = tl.dtype == NF4_F32;
-      const uint32_t bytes =
-          L::kPreA ? kNf4Bytes : (f32 ? 2 * kGoBoxBytes : kGoBoxBytes) + kNf4Bytes;
+      const uint32_t bytes = (L::kPreA ? 0u : (f32 ? 2u * kGoBoxBytes : kGoBoxBytes)) +
+                             kNf4Bytes + (tl.stma ? kScaleBytes : 0u);
       const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
       const int x_nf4 = tl.kt * (BK / 2) + static_cast<int>(rank) * (BKC / 2);
-      const CUtensorMap* map = box == 2 ? &tl.p->tm_nf4 : &tl.p->tm_go;
-      const bool my_box = box != 1 || f32;
+      const CUtensorMap* map =
+          box == 3 ? &tl.p->tm_scales : (box == 2 ? &tl.p->tm_nf4 : &tl.p->tm_go);
+      // x of each box: grad_out column, NF4 byte column, or the first of the
+      // pair tile's 4 block scales (4 floats = 16 bytes per k-tile).
+      const int x_box = box == 3 ? tl.kt * 4 : (box == 2 ? x_nf4 : 32 * box);
+      const bool my_box = box == 3 ? tl.stma != 0 : (box != 1 || f32);
+      const bool registers = L::kPreA ? box == 2 : box == 0;
       for (int s = 0; s < tl.ns; ++s, ++it) {
         const uint32_t slot = it % kRawStages;
         bool free_slot = true;
@@ -383,14 +401,17 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         }
         if (my_box && my_slot == static_cast<int>(slot)) {
           const uint32_t fb = full_raw(slot);
-          const uint32_t dst = sbase + kRawOff + slot * kRawBytes +
-                               (box == 0 ? 0u : (box == 1 ? static_cast<uint32_t>(kGoBoxBytes)
-                                                          : static_cast<uint32_t>(kGoBytes)));
-          if (box == 0 || L::kPreA) {
+          const uint32_t dst =
+              sbase + kRawOff + slot * kRawBytes +
+              (box == 0 ? 0u
+                        : (box == 1 ? static_cast<uint32_t>(kGoBoxBytes)
+                                    : (box == 2 ? static_cast<uint32_t>(kGoBytes)
+                                                : static_cast<uint32_t>(L::kScaleOff))));
+          if (registers) {
             mbar_arrive_expect_tx(fb, bytes);
             NF4_PROBE(40, it);
           }
-          tma_load_2d(dst, map, box == 2 ? x_nf4 : s * BN + 32 * box, box == 2 ? s * BN : row0, fb);
+          tma_load_2d(dst, map, box >= 2 ? x_box : s * BN + x_box, box >= 2 ? s * BN : row0, fb);
         }
         if (lane == 0) NF4_PROGRESS_SET(0, it + 1);
         __syncwarp();
@@ -411,11 +432,13 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer (CTA 0)
-    if (rank == 0 && lane == 0) {
-      // This thread shares its SM sub-partition with busy converter warps and
-      // is on the critical path: per stage it issues 4 MMAs and commits, and
-      // reads the ready counter only when it has caught up with it.  Descriptors of slot 0 are built once; a
-      // slot's are those plus its offset in the 16-byte address field.
+    if (rank == 0) {
+      // The whole warp runs this loop and one elected lane issues the MMAs and
+      // commits (a warp-converged issuer keeps their operands in uniform
+      // registers, see elect_one).  Per stage: 4 MMAs and the commits; the
+      // ready counter is read only when the warp has caught up with it.
+      // Descriptors of slot 0 are built once; a slot's are those plus its
+      // offset in the 16-byte address field.
       constexpr uint32_t idesc = idesc_f16_f32(BMP, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
       const uint64_t a_desc0 = smem_desc_sw128(sbase + (L::kPreA ? kAOff : kOpOff), 16, kSbo);
       const uint64_t b_desc0 = smem_desc_sw128(sbase + kOpOff + L::kBInOp, kBLbo, kSbo);
@@ -427,53 +450,64 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       for (int t = cluster; ok && t < total_tiles; t += nclusters, ++lt) {
         const Tile tl = tile_at(descs, count, t);
         const uint32_t acc = lt & 1u;
-        if (!mbar_wait_cluster(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u, abort_flag)) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u,
+                                                       abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BK;
         for (int s = 0; s < tl.ns; ++s) {
-          NF4_PROBE(32, it);
+          if (lane == 0) NF4_PROBE(32, it);
           // The watcher publishes, in order, how many stages' operand barriers
-          // it has seen complete; the counter is read again only when this
-          // thread has caught up with it, so stages that are already ready go
-          // to the tensor core back to back.
-          if (avail <= it && !flag_wait_ge(ready0, it + 1u, abort_flag, &avail)) {
-            ok = false;
-            break;
+          // it has seen complete; lane 0 reads the counter again only when the
+          // warp has caught up with it, so stages that are already ready go to
+          // the tensor core back to back.
+          if (avail <= it) {
+            uint32_t seen = 0;
+            bool got = true;
+            if (lane == 0) got = flag_wait_ge(ready0, it + 1u, abort_flag, &seen);
+            avail = __shfl_sync(0xFFFFFFFFu, seen, 0);
+            if (!__shfl_sync(0xFFFFFFFFu, got, 0)) {
+              ok = false;
+              break;
+            }
           }
           // No tcgen05 fence here: the operands were handed to the async proxy
           // by their writers (fence.proxy.async before the barrier arrive) and
-          // this thread acquired the barrier's completion through the ready
-          // word; a tcgen05.fence per stage would keep the MMAs of consecutive
-          // stages from overlapping.
-          NF4_PROBE(33, it);
+          // lane 0 acquired the barrier's completion through the ready word
+          // (shared with the warp by the shuffle); a tcgen05.fence per stage
+          // would keep the MMAs of consecutive stages from overlapping.
+          if (lane == 0) NF4_PROBE(33, it);
           const uint64_t off = static_cast<uint64_t>((slot * kOpSlotBytes) >> 4);
           const uint64_t a =
               a_desc0 + (L::kPreA ? static_cast<uint64_t>((aslot * kABytes) >> 4) : off);
           const uint64_t b = b_desc0 + off;
-          // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
-          tc_mma_f16_pair(d_tmem, a, b, idesc, s != 0 ? 1u : 0u);
-          tc_mma_f16_pair(d_tmem, a + 2u, b + kBStep, idesc, 1u);
-          tc_mma_f16_pair(d_tmem, a + 4u, b + 2u * kBStep, idesc, 1u);
-          tc_mma_f16_pair(d_tmem, a + 6u, b + 3u * kBStep, idesc, 1u);
-          tc_commit_pair(empty_op(slot), 0x3);
-          if constexpr (L::kPreA) {
-            tc_commit_pair(empty_a(aslot), 0x3);
-            aslot = (aslot + 1u == static_cast<uint32_t>(kAStages)) ? 0u : aslot + 1u;
+          if (elect_one()) {
+            // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
+            tc_mma_f16_pair(d_tmem, a, b, idesc, s != 0 ? 1u : 0u);
+            tc_mma_f16_pair(d_tmem, a + 2u, b + kBStep, idesc, 1u);
+            tc_mma_f16_pair(d_tmem, a + 4u, b + 2u * kBStep, idesc, 1u);
+            tc_mma_f16_pair(d_tmem, a + 6u, b + 3u * kBStep, idesc, 1u);
+            tc_commit_pair(empty_op(slot), 0x3);
+            if constexpr (L::kPreA) tc_commit_pair(empty_a(aslot), 0x3);
           }
-          NF4_PROBE(38, it);
-          NF4_PROGRESS_SET(1, it + 1);
+          __syncwarp();
+          if (lane == 0) NF4_PROBE(38, it);
+          if (lane == 0) NF4_PROGRESS_SET(1, it + 1);
           ++it;
           slot = (slot + 1u == static_cast<uint32_t>(kOpStages)) ? 0u : slot + 1u;
+          if constexpr (L::kPreA)
+            aslot = (aslot + 1u == static_cast<uint32_t>(kAStages)) ? 0u : aslot + 1u;
         }
         if (!ok) break;
-        tc_commit_pair(tmem_full(acc), 0x3);
-        NF4_PROGRESS_SET(2, lt + 1);
+        if (elect_one()) tc_commit_pair(tmem_full(acc), 0x3);
+        __syncwarp();
+        if (lane == 0) NF4_PROGRESS_SET(2, lt + 1);
       }
       // No MMA may still be writing TMEM (of either CTA) when it is released.
-      tc_commit_pair(mma_done, 0x1);
+      if (elect_one()) tc_commit_pair(mma_done, 0x1);
+      __syncwarp();
       mbar_wait(mma_done, 0, nullptr);
       // The epilogues' arrivals for the last two tiles are not needed by any MMA,
       // but the CTA may not exit while one from the other CTA is still in flight.
@@ -500,6 +534,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
               ok = false;
               break;
             }
+            NF4_PROBE(46, it);
           }
           if (!mbar_wait_cluster(full_op(slot), (it / kOpStages) & 1u, abort_flag)) {
             ok = false;
@@ -538,6 +573,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           if (rank == 0) mbar_arrive_expect_tx(full_a(slot), 2u * kABytes);
           tma_load_2d_pair(sbase + kAOff + slot * kABytes, &tl.p->tm_go, s * BN, row0,
                            full_a_leader0 + 8u * slot);
+          NF4_PROBE(45, it);
         }
         __syncwarp();
       }
@@ -572,19 +608,25 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     ConvCursor nxt;
     cc_start(nxt, cluster, descs, count, total_tiles);
     for (int i = 0; i < group; ++i) cc_next(nxt, nclusters, descs, count, total_tiles);
+    // (Scales that travel with the raw stage are read from it instead.)
     bool cur_valid = nxt.t < total_tiles;
     bool cur_f32 = nxt.f32;
-    float scale_cur = cur_valid ? cc_scale(nxt, rank, bj, bn) : 0.0f;
+    bool cur_stma = nxt.stma;
+    float scale_cur = cur_valid && !cur_stma ? cc_scale(nxt, rank, bj, bn) : 0.0f;
     cc_next(nxt, nclusters, descs, count, total_tiles);
     cc_next(nxt, nclusters, descs, count, total_tiles);
+    // This thread's scale within a raw slot's scale box (row bn, 16 bytes per row).
+    const uint32_t scale_off = L::kScaleOff + bn * 16 + (2u * rank + bj) * 4u;
 
     uint32_t it = static_cast<uint32_t>(group);
     while (cur_valid) {
-      const float scale = scale_cur;
+      const float scale_pre = scale_cur;
       const bool f32 = cur_f32;
+      const bool stma = cur_stma;
       cur_valid = nxt.t < total_tiles;
       cur_f32 = nxt.f32;
-      scale_cur = cur_valid ? cc_scale(nxt, rank, bj, bn) : 0.0f;
+      cur_stma = nxt.stma;
+      scale_cur = cur_valid && !cur_stma ? cc_scale(nxt, rank, bj, bn) : 0.0f;
       cc_next(nxt, nclusters, descs, count, total_tiles);
       cc_next(nxt, nclusters, descs, count, total_tiles);
 
@@ -616,6 +658,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           g[i] = *reinterpret_cast<const uint4*>(src + (((4u * ahalf + i) ^ aswz) << 4));
       }
       const uint4 q = *reinterpret_cast<const uint4*>(raw + kGoBytes + bn * (BKC / 2) + qchunk);
+      const float scale = stma ? *reinterpret_cast<const float*>(raw + scale_off) : scale_pre;
       // The slot is refilled by TMA (async proxy) once released: order these
       // generic-proxy reads before that write.
       fence_proxy_async_smem();
@@ -661,8 +704,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           *reinterpret_cast<uint4*>(dst + (((4u * bh + e) ^ bswz) << 4)) =
               dequant_word(words[e], tb);
       }
+      if (probe) NF4_PROBE(48 + cw, it);
       fence_proxy_async_smem();
       __syncwarp();
+      if (probe) NF4_PROBE(64 + cw, it);
       if (lane == 0) {
         if (rank == 1) {
           // A 16-byte copy into CTA 0 that completes on CTA 0's operand barrier;
@@ -758,7 +803,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
 // Descriptors of a grouped launch travel to the workspace as kernel parameters
 // (copied by value at launch, also when the launch is captured in a CUDA graph),
 // kDescsPerUpload at a time.
-constexpr int kDescsPerUpload = 60;
+constexpr int kDescsPerUpload = 48;
 struct DescChunk {
   ProblemDesc d[kDescsPerUpload];
 };
@@ -864,6 +909,15 @@ static int check_problem(const void* go, int dtype, const float* scales, const u
 // Everything of a descriptor but the grad_out map.
 static int fill_desc_rest(ProblemDesc* d, int dtype, const float* scales, const uint8_t* data,
                           float* grad_A, int M, int N, int K) {
+  const int KB = K / 64;
+  d->scale_tma = 0;
+  if (KB % 4 == 0 && aligned(scales, 16)) {
+    if (!encode_2d(&d->tm_scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales,
+                   static_cast<uint64_t>(KB), static_cast<uint64_t>(N),
+                   static_cast<uint64_t>(KB) * 4, 4, BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return NF4_ERR_CUDA;
+    d->scale_tma = 1;
+  }
   if (!encode_2d(&d->tm_nf4, CU_TENSOR_MAP_DATA_TYPE_UINT8, data, static_cast<uint64_t>(K / 2),
                  static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), BKC / 2, BN,
                  CU_TENSOR_MAP_SWIZZLE_64B))
@@ -1372,7 +1426,7 @@ extern "C" int nf4_check_error_site(void* stream, unsigned int* site) {
 // call of nf4_backward_a_batched_noalloc on that GPU.
 namespace nf4 {
 constexpr int kNoAllocMaxProblems = 256;
-constexpr size_t kNoAllocBytes = kNoAllocMaxProblems * sizeof(ProblemDesc);  // 128 KiB
+constexpr size_t kNoAllocBytes = kNoAllocMaxProblems * sizeof(ProblemDesc);  // 160 KiB
 static __device__ __align__(256) unsigned char g_noalloc_descs[kNoAllocBytes];
 
 // Device address of g_noalloc_descs on the current device, looked up once per

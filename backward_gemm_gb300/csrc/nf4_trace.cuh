@@ -16,7 +16,9 @@ namespace nf4 {
 // tile start / end, 39 reference, 40 producer issue, 41 watcher sees stage,
 // 42 converter group leader sees raw data, 43 converter group leader starts,
 // 44 slot 0 kernel entry / slot 1 all roles done / slot 2 after the last
-// cluster barrier.
+// cluster barrier; pre-converted variant: 45 A producer issues the stage's A
+// copy, 46 watcher sees both A copies landed; 48-63 converter warp 0-15 has
+// stored its B^T chunks, 64-79 it has also passed the proxy fence.
 //
 // Few-token kernel (small_m_kernel), CTAs 0 and 1 (k-tile 0, cluster ranks 0
 // and 1 when S > 1): slot s of events 0-6 and 8 is stage s.  0 producer issues
@@ -29,7 +31,7 @@ namespace nf4 {
 #ifdef NF4_TRACE
 __device__ unsigned long long* g_trace = nullptr;
 constexpr int kTraceSlots = 512;
-constexpr int kTraceEvents = 48;
+constexpr int kTraceEvents = 88;
 // Each kernel caches the buffer pointer once (NF4_TRACE_INIT), so a probe is a
 // clock read and one store.
 #define NF4_TRACE_INIT unsigned long long* const nf4_trace_buf = blockIdx.x < 2 ? g_trace : nullptr

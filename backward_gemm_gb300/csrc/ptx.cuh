@@ -335,6 +335,19 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 }
 
 // D[tmem of both CTAs] (+)= A[rows of each CTA] * B[columns split over the pair].
+// One lane of the converged warp (elect.sync over all 32 lanes): the lane that
+// issues a warp's single-thread tcgen05 instructions.  Keeping the issuing warp
+// converged around them (rather than running the issue loop in one lane) lets
+// the compiler keep their operands in uniform registers; issuing from a
+// divergent lane measured about 40% fewer MMAs per second on GB300.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t accumulate) {
   asm volatile(

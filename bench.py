@@ -275,7 +275,7 @@ def bench_ours(args, rank, world, dev):
 
 
 SMALL_M_MAX = 64      # the library's default few-token limit (nf4_set_small_m_max)
-DESCS_PER_UPLOAD = 60  # descriptors per upload kernel of a grouped launch
+DESCS_PER_UPLOAD = 48  # descriptors per upload kernel of a grouped launch
 
 
 def kernel_names(probs, entry="plain") -> str:

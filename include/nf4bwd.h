@@ -197,7 +197,7 @@ int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspa
  * Same problems, rules and results as nf4_backward_a_batched (few-token
  * problems included), but the
  * per-problem descriptors go to a fixed array inside the library (a
- * file-scope device array of 128 KiB, reserved on every GPU that loads the
+ * file-scope device array of 160 KiB, reserved on every GPU that loads the
  * library until the process exits), so the call takes no workspace.
  *   count      at most 256 problems; more returns NF4_ERR_WORKSPACE and
  *              enqueues nothing
