@@ -47,6 +47,8 @@ SIGNATURES = {
     "nf4_backward_a_ex": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "nf4_backward_a_ws_bytes": (_sz, [_i, _i]),
     "nf4_backward_a_ws": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+    "nf4_split_plan": (_i, [_i, _i, _i, C.POINTER(_i), C.POINTER(_i)]),
+    "nf4_split_item": (_i, [_i, _i, _i, _i, _i, C.POINTER(_i)]),
     "nf4_backward_a_batched_workspace": (_sz, [_i]),
     "nf4_backward_a_batched": (_i, [C.POINTER(Nf4Problem), _i, _vp, _sz, _vp]),
     "nf4_check_error": (_i, [_vp]),
@@ -161,10 +163,39 @@ def backward_a(grad_out: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = 
     return out
 
 
-def ws_workspace(M: int, N: int, device=None) -> torch.Tensor:
-    """Device workspace for :func:`backward_a_ws` (the f16 copy of grad_out)."""
-    n = int(lib().nf4_backward_a_ws_bytes(M, N))
+def ws_workspace(M: int, N: int, device=None, split: bool = True) -> torch.Tensor:
+    """Device workspace for :func:`backward_a_ws`: the f16 copy of grad_out and,
+    with ``split``, room for splitting a last partial wave of tiles."""
+    if split:
+        n = int(lib().nf4_backward_a_ws_bytes(M, N))
+    else:
+        n = 2 * M * ((N + 7) // 8 * 8)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def split_plan(tiles: int, stages: int, pairs: int) -> tuple[int, int]:
+    """(dp_tiles, sk_tiles) of the ws entry point's split plan (host only)."""
+    dp, sk = C.c_int(0), C.c_int(0)
+    rc = lib().nf4_split_plan(tiles, stages, pairs, C.byref(dp), C.byref(sk))
+    if rc != 0:
+        raise ValueError("invalid split-plan arguments")
+    return dp.value, sk.value
+
+
+def split_items(tiles: int, stages: int, pairs: int, pair: int):
+    """The items of one pair under the split plan, in run order: tuples
+    (tile, s0, s1, first_partner, last_partner)."""
+    out = []
+    buf = (C.c_int * 5)()
+    k = 0
+    while True:
+        rc = lib().nf4_split_item(tiles, stages, pairs, pair, k, buf)
+        if rc < 0:
+            raise ValueError("invalid split-item arguments")
+        if rc == 0:
+            return out
+        out.append(tuple(buf))
+        k += 1
 
 
 def backward_a_ws(grad_out: torch.Tensor, w: NF4Weight, workspace: torch.Tensor | None = None,

@@ -81,8 +81,6 @@ constexpr int kScaleBytes = BN * 16;                   // 64 rows n x 4 block sc
 constexpr int kABytes = BM * BN * 2;                   // 16 KB f16
 constexpr int kBBytes = BKC * BN * 2;                  // 16 KB f16
 constexpr int kOpBytes = kABytes + kBBytes;            // 32 KB
-constexpr int kEpiCols = 16;                           // fp32 columns per epilogue store
-constexpr int kEpiBufBytes = 32 * kEpiCols * 4;        // 32 rows x 16 fp32 (64-byte rows)
 constexpr int kEpiBufs = 2;  // staging buffers per epilogue warp: a store drains while the next fills
 constexpr uint32_t kSigBytes = 16;
 constexpr long long kAbortLingerCycles = 4000000;  // ~2 ms: far longer than a copy's latency
@@ -97,9 +95,14 @@ constexpr uint32_t kTmemCols = 2 * BK;
 // separate pass, and a TMA copy writes each stage's A operand straight into a
 // ring of RA A slots (no raw grad_out, no converter work on A); the operand
 // slots then hold B^T only.
-template <int RS, int OS, int GOB, int RA = 0>
+template <int RS, int OS, int GOB, int RA = 0, int EC = 16>
 struct Layout {
   static constexpr bool kPreA = RA > 0;
+  // Epilogue chunk: EC fp32 columns of a warp's 32 rows per TMEM load and per
+  // TMA store (EC = 16: 64-byte rows, 64-byte swizzle; 32: 128-byte rows,
+  // 128-byte swizzle; fewer, larger chunks cost less per column).
+  static constexpr int kEpiCols = EC;
+  static constexpr int kEpiBufBytes = 32 * EC * 4;
   static constexpr int kRawStages = RS;
   static constexpr int kOpStages = OS;
   static constexpr int kAStages = RA;
@@ -113,7 +116,8 @@ struct Layout {
   static constexpr int kOpOff = kAOff + RA * kABytes;
   static constexpr int kEpiOff = kOpOff + OS * kOpSlotBytes;
   static constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufs * kEpiBufBytes;
-  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1 + 2 * RA;
+  // ... + one barrier per epilogue warp for reading other pairs' partial sums
+  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1 + 2 * RA + kEpiWarps;
   // misc: TMEM address, abort flag, the ready counter (and spare words), then the
   // 16-byte signal words: in CTA 0 one destination per (operand slot,
   // converter warp of a group), and one source.
@@ -141,7 +145,7 @@ struct Layout {
 };
 using LayoutF32 = Layout<2, 4, 2 * kGoBoxBytes>;  // any fp32 grad_out in the launch
 using LayoutBF16 = Layout<2, 4, kGoBoxBytes>;     // bf16 grad_out only
-using LayoutPreA = Layout<6, 4, 0, 7>;            // grad_out pre-converted to f16
+using LayoutPreA = Layout<6, 4, 0, 6, 32>;        // grad_out pre-converted to f16
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
 // 8 rows n per 1024-byte atom; atoms along k are kBLbo apart, atoms along n 1 KB.
@@ -202,19 +206,93 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int
   return r;
 }
 
-// Stage cursor of a converter group: which pair tile and stage it converts
-// next, with the fields of that tile's problem needed for the scale loads.
+// ------------------------------------------------------------------ work schedule
+// The work of a launch is a list of pair tiles, each a run of n_stages stages
+// (64 columns of the shared dimension N each).  Tiles [0, dp_tiles) go whole to
+// the pairs, round-robin.  When a single problem has too few tiles to keep every
+// pair busy for a whole number of waves, the remaining tiles [dp_tiles,
+// dp_tiles + sk_tiles) are cut by stages instead ("stream-K"): their stages,
+// numbered consecutively, are split into one contiguous run per pair.  A tile
+// whose stages fall to several pairs is finished by the pair holding its first
+// stage, which processes that part last of all its work; the others (later
+// stages of the tile, processed first) leave their fp32 partial sums in a
+// workspace and count a flag up, and the finishing pair adds them to its own
+// sum in pair order before storing the tile.  The split points depend only on
+// the problem and the number of pairs, so results are reproducible.
+struct SkArgs {
+  int dp_tiles;          // tiles done whole (all tiles when sk_tiles == 0)
+  int sk_tiles;          // tiles split by stages (single problem only)
+  int stages;            // stages per tile of the split region
+  float* partials;       // [pair][rank][BM][BK] fp32 partial sums
+  unsigned int* flags;   // [pair] epilogue warps (of both CTAs) done writing partials
+};
+
+// One piece of a pair's work: stages [s0, s1) of tile t (s1 clipped to the
+// tile's stage count by the caller for whole tiles).
+struct Item {
+  int t, s0, s1;
+};
+
+__host__ __device__ __forceinline__ int64_t sk_start(const SkArgs& sk, int q, int pairs) {
+  const int64_t W = static_cast<int64_t>(sk.sk_tiles) * sk.stages;
+  return W * q / pairs;
+}
+
+// Item k of pair c (k = 0, 1, ...); t < 0 when the pair has no more work.
+__host__ __device__ __forceinline__ Item item_at(const SkArgs& sk, int c, int pairs, int k) {
+  Item w;
+  const int ndp = c < sk.dp_tiles ? (sk.dp_tiles - 1 - c) / pairs + 1 : 0;
+  if (k < ndp) {
+    w.t = c + k * pairs;
+    w.s0 = 0;
+    w.s1 = INT_MAX;
+    return w;
+  }
+  w.t = -1;
+  w.s0 = w.s1 = 0;
+  if (sk.sk_tiles == 0) return w;
+  const int64_t st = sk_start(sk, c, pairs), en = sk_start(sk, c + 1, pairs);
+  const int64_t tile = st / sk.stages + (k - ndp);
+  const int64_t base = tile * sk.stages;
+  if (st >= en || base >= en) return w;
+  w.t = sk.dp_tiles + static_cast<int>(tile);
+  w.s0 = static_cast<int>(st > base ? st - base : 0);
+  w.s1 = static_cast<int>(en - base < sk.stages ? en - base : sk.stages);
+  return w;
+}
+
+// Whether pair q holds any split-region stage (with fewer such stages than
+// pairs, some pairs hold none; they write no partial sum).
+__host__ __device__ __forceinline__ bool sk_has_stages(const SkArgs& sk, int q, int pairs) {
+  return sk_start(sk, q, pairs) < sk_start(sk, q + 1, pairs);
+}
+
+// The pair that holds split-region stage x.
+__host__ __device__ __forceinline__ int sk_owner(const SkArgs& sk, int64_t x, int pairs) {
+  const int64_t W = static_cast<int64_t>(sk.sk_tiles) * sk.stages;
+  int q = static_cast<int>((x * pairs) / W);
+  if (q > pairs - 1) q = pairs - 1;
+  while (q > 0 && sk_start(sk, q, pairs) > x) --q;
+  while (q + 1 < pairs && sk_start(sk, q + 1, pairs) <= x) ++q;
+  return q;
+}
+
+// Stage cursor of a converter group: which item and stage it converts next,
+// with the fields of that tile's problem needed for the scale loads.
 struct ConvCursor {
-  int t, s, ns, kt, N, KB;
+  int k, t, s, s1, kt, N, KB;
   bool f32, stma;
   const float* scales;
 };
 
-__device__ __forceinline__ void cc_load(ConvCursor& c, const ProblemDesc* descs, int count,
-                                        int total_tiles) {
-  if (c.t < total_tiles) {
-    const Tile tl = tile_at(descs, count, c.t);
-    c.ns = tl.ns;
+__device__ __forceinline__ void cc_load(ConvCursor& c, const SkArgs& sk, int cluster, int pairs,
+                                        const ProblemDesc* descs, int count) {
+  const Item w = item_at(sk, cluster, pairs, c.k);
+  c.t = w.t;
+  if (w.t >= 0) {
+    const Tile tl = tile_at(descs, count, w.t);
+    c.s = w.s0;
+    c.s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
     c.kt = tl.kt;
     c.N = tl.N;
     c.KB = tl.K >> 6;
@@ -224,27 +302,26 @@ __device__ __forceinline__ void cc_load(ConvCursor& c, const ProblemDesc* descs,
   }
 }
 
-__device__ __forceinline__ void cc_start(ConvCursor& c, int t0, const ProblemDesc* descs,
-                                         int count, int total_tiles) {
-  c.t = t0;
+__device__ __forceinline__ void cc_start(ConvCursor& c, const SkArgs& sk, int cluster, int pairs,
+                                         const ProblemDesc* descs, int count) {
+  c.k = 0;
   c.s = 0;
-  c.ns = 1;
+  c.s1 = 1;
   c.kt = 0;
   c.N = 0;
   c.KB = 0;
   c.f32 = true;
   c.stma = false;
   c.scales = nullptr;
-  cc_load(c, descs, count, total_tiles);
+  cc_load(c, sk, cluster, pairs, descs, count);
 }
 
-__device__ __forceinline__ void cc_next(ConvCursor& c, int stride, const ProblemDesc* descs,
-                                        int count, int total_tiles) {
-  if (c.t >= total_tiles) return;
-  if (++c.s >= c.ns) {
-    c.s = 0;
-    c.t += stride;
-    cc_load(c, descs, count, total_tiles);
+__device__ __forceinline__ void cc_next(ConvCursor& c, const SkArgs& sk, int cluster, int pairs,
+                                        const ProblemDesc* descs, int count) {
+  if (c.t < 0) return;
+  if (++c.s >= c.s1) {
+    ++c.k;
+    cc_load(c, sk, cluster, pairs, descs, count);
   }
 }
 
@@ -266,7 +343,7 @@ __device__ __forceinline__ float cc_scale(const ConvCursor& c, uint32_t rank, in
 template <class L>
 __global__ void __launch_bounds__(L::kThreads, 1)
     bwd_a_kernel(const __grid_constant__ ProblemDesc single, const ProblemDesc* __restrict__ batch,
-                 int count, int total_tiles) {
+                 int count, const __grid_constant__ SkArgs sk) {
   constexpr int kRawStages = L::kRawStages;
   constexpr int kOpStages = L::kOpStages;
   constexpr int kGoBytes = L::kGoBytes;
@@ -311,6 +388,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
   auto empty_a = [&](uint32_t i) {
     return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + kAStages + i);
   };
+  // Split tiles: epilogue warp w's barrier for bulk loads of partial sums.
+  auto part_bar = [&](uint32_t w) {
+    return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + 2 * L::kAStages + w);
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -341,6 +422,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       mbar_init(full_a(i), 1);  // CTA 0's A producer registers both CTAs' bytes
       mbar_init(empty_a(i), 1);
     }
+    for (int i = 0; i < kEpiWarps; ++i) mbar_init(part_bar(i), 1);
     for (int i = 0; i < kOpStages; ++i)
       reinterpret_cast<volatile uint32_t*>(smem + kReadyOff)[i] = 0u;
     *abort_flag = 0;
@@ -377,8 +459,11 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     }
     uint32_t it = 0;
     bool ok = true;
-    for (int t = cluster; ok && t < total_tiles; t += nclusters) {
-      const Tile tl = tile_at(descs, count, t);
+    for (int k = 0; ok; ++k) {
+      const Item w = item_at(sk, cluster, nclusters, k);
+      if (w.t < 0) break;
+      const Tile tl = tile_at(descs, count, w.t);
+      const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
       const bool f32 = tl.dtype == NF4_F32;
       const uint32_t bytes = (L::kPreA ? 0u : (f32 ? 2u * kGoBoxBytes : kGoBoxBytes)) +
                              kNf4Bytes + (tl.stma ? kScaleBytes : 0u);
@@ -391,7 +476,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       const int x_box = box == 3 ? tl.kt * 4 : (box == 2 ? x_nf4 : 32 * box);
       const bool my_box = box == 3 ? tl.stma != 0 : (box != 1 || f32);
       const bool registers = L::kPreA ? box == 2 : box == 0;
-      for (int s = 0; s < tl.ns; ++s, ++it) {
+      for (int s = w.s0; s < s1; ++s, ++it) {
         const uint32_t slot = it % kRawStages;
         bool free_slot = true;
         if (lane == 0) free_slot = mbar_wait(empty_raw(slot), ((it / kRawStages) & 1u) ^ 1u, abort_flag);
@@ -447,8 +532,11 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       uint32_t it = 0, lt = 0, slot = 0, aslot = 0;
       uint32_t avail = 0;  // stages the watcher has published as ready
       bool ok = true;
-      for (int t = cluster; ok && t < total_tiles; t += nclusters, ++lt) {
-        const Tile tl = tile_at(descs, count, t);
+      for (int k = 0; ok; ++k, ++lt) {
+        const Item w = item_at(sk, cluster, nclusters, k);
+        if (w.t < 0) break;
+        const Tile tl = tile_at(descs, count, w.t);
+        const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
         const uint32_t acc = lt & 1u;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u,
                                                        abort_flag))) {
@@ -457,7 +545,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BK;
-        for (int s = 0; s < tl.ns; ++s) {
+        for (int s = w.s0; s < s1; ++s) {
           if (lane == 0) NF4_PROBE(32, it);
           // The watcher publishes, in order, how many stages' operand barriers
           // it has seen complete; lane 0 reads the counter again only when the
@@ -485,7 +573,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           const uint64_t b = b_desc0 + off;
           if (elect_one()) {
             // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
-            tc_mma_f16_pair(d_tmem, a, b, idesc, s != 0 ? 1u : 0u);
+            tc_mma_f16_pair(d_tmem, a, b, idesc, s != w.s0 ? 1u : 0u);
             tc_mma_f16_pair(d_tmem, a + 2u, b + kBStep, idesc, 1u);
             tc_mma_f16_pair(d_tmem, a + 4u, b + 2u * kBStep, idesc, 1u);
             tc_mma_f16_pair(d_tmem, a + 6u, b + 3u * kBStep, idesc, 1u);
@@ -525,9 +613,12 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     if (rank == 0 && lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = cluster; ok && t < total_tiles; t += nclusters) {
-        const Tile tl = tile_at(descs, count, t);
-        for (int s = 0; s < tl.ns; ++s, ++it) {
+      for (int k = 0; ok; ++k) {
+        const Item w = item_at(sk, cluster, nclusters, k);
+        if (w.t < 0) break;
+        const Tile tl = tile_at(descs, count, w.t);
+        const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
+        for (int s = w.s0; s < s1; ++s, ++it) {
           const uint32_t slot = it % kOpStages;
           if constexpr (L::kPreA) {
             if (!mbar_wait_cluster(full_a(it % kAStages), (it / kAStages) & 1u, abort_flag)) {
@@ -557,10 +648,13 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     const uint32_t full_a_leader0 = mapa_shared(full_a(0), 0);
     uint32_t it = 0;
     bool ok = true;
-    for (int t = cluster; ok && t < total_tiles; t += nclusters) {
-      const Tile tl = tile_at(descs, count, t);
+    for (int k = 0; ok; ++k) {
+      const Item w = item_at(sk, cluster, nclusters, k);
+      if (w.t < 0) break;
+      const Tile tl = tile_at(descs, count, w.t);
+      const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
       const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
-      for (int s = 0; s < tl.ns; ++s, ++it) {
+      for (int s = w.s0; s < s1; ++s, ++it) {
         const uint32_t slot = it % kAStages;
         bool free_slot = true;
         if (lane == 0)
@@ -606,15 +700,15 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     // `nxt` runs two stages (one group turn) ahead of the stage being converted,
     // so the block scale it needs is loaded a whole turn before its use.
     ConvCursor nxt;
-    cc_start(nxt, cluster, descs, count, total_tiles);
-    for (int i = 0; i < group; ++i) cc_next(nxt, nclusters, descs, count, total_tiles);
+    cc_start(nxt, sk, cluster, nclusters, descs, count);
+    for (int i = 0; i < group; ++i) cc_next(nxt, sk, cluster, nclusters, descs, count);
     // (Scales that travel with the raw stage are read from it instead.)
-    bool cur_valid = nxt.t < total_tiles;
+    bool cur_valid = nxt.t >= 0;
     bool cur_f32 = nxt.f32;
     bool cur_stma = nxt.stma;
     float scale_cur = cur_valid && !cur_stma ? cc_scale(nxt, rank, bj, bn) : 0.0f;
-    cc_next(nxt, nclusters, descs, count, total_tiles);
-    cc_next(nxt, nclusters, descs, count, total_tiles);
+    cc_next(nxt, sk, cluster, nclusters, descs, count);
+    cc_next(nxt, sk, cluster, nclusters, descs, count);
     // This thread's scale within a raw slot's scale box (row bn, 16 bytes per row).
     const uint32_t scale_off = L::kScaleOff + bn * 16 + (2u * rank + bj) * 4u;
 
@@ -623,12 +717,12 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       const float scale_pre = scale_cur;
       const bool f32 = cur_f32;
       const bool stma = cur_stma;
-      cur_valid = nxt.t < total_tiles;
+      cur_valid = nxt.t >= 0;
       cur_f32 = nxt.f32;
       cur_stma = nxt.stma;
       scale_cur = cur_valid && !cur_stma ? cc_scale(nxt, rank, bj, bn) : 0.0f;
-      cc_next(nxt, nclusters, descs, count, total_tiles);
-      cc_next(nxt, nclusters, descs, count, total_tiles);
+      cc_next(nxt, sk, cluster, nclusters, descs, count);
+      cc_next(nxt, sk, cluster, nclusters, descs, count);
 
       const uint32_t rslot = it % kRawStages;
       const uint32_t oslot = it % kOpStages;
@@ -727,48 +821,163 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
+    // Per item: a whole tile, or the first stages of a split tile, is read out
+    // of TMEM (plus, for a split tile, the other pairs' partial sums in pair
+    // order) and stored to grad_A through a staging buffer and TMA stores; the
+    // later stages of a split tile are left as a partial sum in this pair's
+    // workspace slot, followed by a count-up of the pair's flag.
     const uint32_t tmem_empty_leader0 = mapa_shared(tmem_empty(0), 0);
+    constexpr int kEpiCols = L::kEpiCols;
+    constexpr int kEpiBufBytes = L::kEpiBufBytes;
+    constexpr int kPieces = kEpiCols / 4;  // 16-byte pieces per staged row
     uint8_t* const buf0 = smem + kEpiOff + warp * kEpiBufs * kEpiBufBytes;
     uint32_t lt = 0;
-    for (int t = cluster; t < total_tiles; t += nclusters, ++lt) {
-      const Tile tl = tile_at(descs, count, t);
+    for (int k = 0;; ++k, ++lt) {
+      const Item w = item_at(sk, cluster, nclusters, k);
+      if (w.t < 0) break;
+      const Tile tl = tile_at(descs, count, w.t);
+      const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
+      const bool partial = w.s0 > 0;                // later stages of a split tile
+      const bool finish = !partial && s1 < tl.ns;  // first stages of a split tile
+      // Pairs whose partial sums complete this tile: cluster+1 .. q_last.
+      int q_last = cluster;
+      if (finish) {
+        const int64_t x_last = static_cast<int64_t>(w.t - sk.dp_tiles) * sk.stages + sk.stages - 1;
+        q_last = sk_owner(sk, x_last, nclusters);
+      }
       const uint32_t acc = lt & 1u;
       const bool got = mbar_wait_cluster(tmem_full(acc), (lt >> 1) & 1u, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       if (threadIdx.x == 0) NF4_PROBE(35, lt);
       tc_fence_after();
+      if (finish) {
+        // The other pairs wrote their parts first thing; wait for all of them.
+        bool ready = true;
+        if (lane == 0) {
+          for (int q = cluster + 1; ready && q <= q_last; ++q)
+            if (sk_has_stages(sk, q, nclusters))
+              ready = flag_wait_global_ge(sk.flags + q, 2u * kEpiWarps, abort_flag);
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) break;
+        if (threadIdx.x == 0) NF4_PROBE(37, k);
+      }
       const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM + warp * 32;
       const uint32_t taddr = tmem_base + acc * BK + (static_cast<uint32_t>(warp * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < BK / kEpiCols; ++c) {
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(taddr + c * kEpiCols, r);
-        tmem_wait_ld();
-        // Two staging buffers: at most one store may still be reading, so the
-        // one that last used this buffer is done with it.
-        uint8_t* const buf = buf0 + (c & 1) * kEpiBufBytes;
-        if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
-        __syncwarp();
-        // Row `lane` of the 32 x 16 fp32 block, 64-byte swizzled (16-byte chunk
-        // q of row r at q ^ ((r / 2) % 4)).
-        const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+      // Partial sums move as this warp's 16 staging-layout chunks (2 KB each,
+      // 32 KB per warp) between its slot in the workspace and shared memory.
+      constexpr uint32_t kWarpPartBytes = (BK / kEpiCols) * kEpiBufBytes;  // 32 KB
+      auto warp_slot = [&](int q) {
+        return reinterpret_cast<uint8_t*>(sk.partials) +
+               ((static_cast<size_t>(q) * 2 + rank) * kEpiWarps + warp) * kWarpPartBytes;
+      };
+      // Row `lane` of a 32-row chunk, swizzled as the TMA stores to grad_A
+      // read it (16-byte piece q of row r at q ^ ((r / 2) % 4) for 64-byte
+      // rows, q ^ (r % 8) for 128-byte rows); the partial sums keep the layout.
+      const uint32_t sw = kEpiCols == 16 ? (static_cast<uint32_t>(lane) >> 1) & 3u
+                                         : static_cast<uint32_t>(lane) & 7u;
+      auto stage_chunk = [&](uint8_t* buf, const uint32_t (&r)[kEpiCols]) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+        for (int q4 = 0; q4 < kPieces; ++q4)
           *reinterpret_cast<uint4*>(buf + lane * (kEpiCols * 4) + ((static_cast<uint32_t>(q4) ^ sw) << 4)) =
               make_uint4(r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2], r[4 * q4 + 3]);
+      };
+      // One 16-column chunk in r: through a staging buffer to grad_A (TMA
+      // store) or, for the later stages of a split tile, to this pair's slot.
+      auto emit_chunk = [&](int c, const uint32_t (&r)[kEpiCols]) {
+        // Two staging buffers: at most one copy may still be reading, so the
+        // one that last used this buffer is done with it.
+        uint8_t* const buf = buf0 + (c & 1) * kEpiBufBytes;
+        if (threadIdx.x == 0) NF4_PROBE(80, lt * 16 + c);
+        if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
+        __syncwarp();
+        if (threadIdx.x == 0) NF4_PROBE(81, lt * 16 + c);
+        stage_chunk(buf, r);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * kEpiCols, row0, smem_addr(buf));
+          if (partial)
+            bulk_store_s2g(warp_slot(cluster) + c * kEpiBufBytes, smem_addr(buf), kEpiBufBytes);
+          else
+            tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * kEpiCols, row0, smem_addr(buf));
           bulk_commit();
         }
+        if (threadIdx.x == 0) NF4_PROBE(82, lt * 16 + c);
+      };
+      if (!finish) {
+#pragma unroll 1
+        for (int c = 0; c < BK / kEpiCols; ++c) {
+          uint32_t r[kEpiCols];
+          if (threadIdx.x == 0) NF4_PROBE(83, lt * 16 + c);
+          tmem_ld_cols<kEpiCols>(taddr + c * kEpiCols, r);
+          tmem_wait_ld();
+          emit_chunk(c, r);
+        }
+      } else {
+        // First stages of a split tile, this pair's last item: its MMAs are
+        // done, so the operand rings are free.  Each contributing pair's
+        // partial sums (32 KB for this warp) are bulk-loaded into the rings
+        // and added to the accumulator in pair order; the last one goes out
+        // with the result, the earlier ones back into TMEM.
+        const uint32_t region = sbase + kRawOff + static_cast<uint32_t>(warp) * kWarpPartBytes;
+        const uint8_t* const region_ptr = smem + kRawOff + warp * kWarpPartBytes;
+        uint32_t j = 0;
+        bool ok_load = true;
+        for (int q = cluster + 1; ok_load && q <= q_last; ++q) {
+          if (!sk_has_stages(sk, q, nclusters)) continue;
+          bool more = false;  // another contributor after q
+          for (int q2 = q + 1; q2 <= q_last; ++q2) more = more || sk_has_stages(sk, q2, nclusters);
+          if (lane == 0) {
+            // Generic reads of this region (previous contributor) and the
+            // acquire of the counts come before the async-proxy copy.
+            fence_proxy_async_smem();
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(part_bar(warp), kWarpPartBytes);
+            bulk_load_g2s(region, warp_slot(q), kWarpPartBytes, part_bar(warp));
+          }
+          ok_load = __all_sync(0xFFFFFFFFu, mbar_wait(part_bar(warp), j & 1u, abort_flag));
+          if (!ok_load) break;
+#pragma unroll 1
+          for (int c = 0; c < BK / kEpiCols; ++c) {
+            uint32_t r[kEpiCols];
+            tmem_ld_cols<kEpiCols>(taddr + c * kEpiCols, r);
+            tmem_wait_ld();
+            const uint8_t* src = region_ptr + c * kEpiBufBytes + lane * (kEpiCols * 4);
+#pragma unroll
+            for (int q4 = 0; q4 < kPieces; ++q4) {
+              const float4 v = *reinterpret_cast<const float4*>(src + ((static_cast<uint32_t>(q4) ^ sw) << 4));
+              r[4 * q4] = __float_as_uint(__uint_as_float(r[4 * q4]) + v.x);
+              r[4 * q4 + 1] = __float_as_uint(__uint_as_float(r[4 * q4 + 1]) + v.y);
+              r[4 * q4 + 2] = __float_as_uint(__uint_as_float(r[4 * q4 + 2]) + v.z);
+              r[4 * q4 + 3] = __float_as_uint(__uint_as_float(r[4 * q4 + 3]) + v.w);
+            }
+            if (more) {
+              tmem_st_cols<kEpiCols>(taddr + c * kEpiCols, r);
+            } else {
+              emit_chunk(c, r);
+            }
+          }
+          if (more) tmem_wait_st();
+          __syncwarp();
+          ++j;
+        }
+        if (!ok_load) break;
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if (rank == 0) mbar_arrive(tmem_empty(acc));
         else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
+        if (partial) {
+          // The warp's partial sums are in global memory once its copies have
+          // completed; then they are made visible to generic-proxy readers and
+          // this warp is counted in.
+          bulk_wait<0>();
+          fence_proxy_async_global();
+          __threadfence();
+          red_release_gpu_add(sk.flags + cluster, 1u);
+        }
       }
+      if (partial && threadIdx.x == 0) NF4_PROBE(34, k);
       if (threadIdx.x == 0) NF4_PROBE(36, lt);
       if (lane == 0) NF4_PROGRESS_SET(20 + warp, lt + 1);
     }
@@ -821,39 +1030,62 @@ __global__ void upload_descs_kernel(const __grid_constant__ DescChunk chunk, Pro
 // grad_out [M][N] (fp32 or bf16) -> f16 [M][ldh], ldh = N rounded up to 8:
 // the A operand of the pre-converted GEMM variant, with the same rounding the
 // converter warps apply (bf16 widened exactly to fp32, then fp32 -> f16 to
-// nearest even).  One thread per 8 elements of a row (16 bytes written);
-// columns N..ldh-1 are written as zeros (the GEMM's tensor map ends at N and
-// never reads them).  Pure streaming: coalesced 16-byte loads and stores.
+// nearest even).  One thread per 16 elements of a row (two 16-byte stores, all
+// loads issued before the conversions); columns N..ldh-1 are written as zeros
+// (the GEMM's tensor map ends at N and never reads them).  Pure streaming.
+__device__ __forceinline__ uint4 f32x8_to_f16(const float4 a, const float4 b) {
+  uint4 h;
+  h.x = pack_f16x2(a.x, a.y);
+  h.y = pack_f16x2(a.z, a.w);
+  h.z = pack_f16x2(b.x, b.y);
+  h.w = pack_f16x2(b.z, b.w);
+  return h;
+}
+
+__device__ __forceinline__ uint4 bf16x8_to_f16(const uint4 w) {
+  uint4 h;
+  h.x = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+  h.y = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+  h.z = pack_f16x2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+  h.w = pack_f16x2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+  return h;
+}
+
 __global__ void __launch_bounds__(256) to_f16_kernel(const void* __restrict__ src, int f32,
                                                      uint16_t* __restrict__ dst, int M, int N,
-                                                     int ldh) {
-  const int groups = ldh >> 3;
+                                                     int ldh, unsigned int* __restrict__ flags,
+                                                     int nflags) {
+  // The split-tile flags of the GEMM that follows start from zero.
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < nflags; i += blockDim.x) flags[i] = 0u;
+  const int groups = (ldh + 15) >> 4;  // 16-element groups per row
   const int64_t total = static_cast<int64_t>(M) * groups;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t m = i / groups;
-    const int c = static_cast<int>(i - m * groups) << 3;
-    uint4 h;
+    const int c = static_cast<int>(i - m * groups) << 4;
+    uint16_t* out = dst + m * ldh + c;
+    const bool second = c + 8 < ldh;  // the group's second 8 columns exist in the copy
     if (f32) {
-      // N % 4 == 0: a group is either whole, half (4 columns) or past N.
+      // N % 4 == 0: each 4-column piece is either inside the row or past N.
       const float4* row = reinterpret_cast<const float4*>(static_cast<const float*>(src) + m * N);
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 a = c < N ? __ldcs(row + (c >> 2)) : z;
-      const float4 b = c + 4 < N ? __ldcs(row + (c >> 2) + 1) : z;
-      h.x = pack_f16x2(a.x, a.y);
-      h.y = pack_f16x2(a.z, a.w);
-      h.z = pack_f16x2(b.x, b.y);
-      h.w = pack_f16x2(b.z, b.w);
+      const int q = c >> 2;
+      const float4 a0 = c < N ? __ldcs(row + q) : z;
+      const float4 a1 = c + 4 < N ? __ldcs(row + q + 1) : z;
+      const float4 a2 = c + 8 < N ? __ldcs(row + q + 2) : z;
+      const float4 a3 = c + 12 < N ? __ldcs(row + q + 3) : z;
+      *reinterpret_cast<uint4*>(out) = f32x8_to_f16(a0, a1);
+      if (second) *reinterpret_cast<uint4*>(out + 8) = f32x8_to_f16(a2, a3);
     } else {
-      // N % 8 == 0: whole groups only (ldh == N).
-      const uint4 w = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) +
-                                                            m * N + c));
-      h.x = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
-      h.y = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
-      h.z = pack_f16x2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
-      h.w = pack_f16x2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+      // N % 8 == 0 and ldh == N: whole 8-column pieces only.
+      const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + m * N);
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 w0 = __ldcs(row + (c >> 3));
+      const uint4 w1 = second ? __ldcs(row + (c >> 3) + 1) : z;
+      *reinterpret_cast<uint4*>(out) = bf16x8_to_f16(w0);
+      if (second) *reinterpret_cast<uint4*>(out + 8) = bf16x8_to_f16(w1);
     }
-    *reinterpret_cast<uint4*>(dst + m * ldh + c) = h;
   }
 }
 
@@ -908,7 +1140,7 @@ static int check_problem(const void* go, int dtype, const float* scales, const u
 
 // Everything of a descriptor but the grad_out map.
 static int fill_desc_rest(ProblemDesc* d, int dtype, const float* scales, const uint8_t* data,
-                          float* grad_A, int M, int N, int K) {
+                          float* grad_A, int M, int N, int K, int epi_cols) {
   const int KB = K / 64;
   d->scale_tma = 0;
   if (KB % 4 == 0 && aligned(scales, 16)) {
@@ -923,8 +1155,9 @@ static int fill_desc_rest(ProblemDesc* d, int dtype, const float* scales, const 
                  CU_TENSOR_MAP_SWIZZLE_64B))
     return NF4_ERR_CUDA;
   if (!encode_2d(&d->tm_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, grad_A, static_cast<uint64_t>(K),
-                 static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 4, kEpiCols, 32,
-                 CU_TENSOR_MAP_SWIZZLE_64B))
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 4,
+                 static_cast<uint32_t>(epi_cols), 32,
+                 epi_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   d->scales = scales;
   d->grad_A = grad_A;
@@ -948,7 +1181,7 @@ static int fill_desc(ProblemDesc* d, const void* go, int dtype, const float* sca
                  static_cast<uint64_t>(N) * (f32 ? 4 : 2), f32 ? 32 : 64, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
-  return fill_desc_rest(d, dtype, scales, data, grad_A, M, N, K);
+  return fill_desc_rest(d, dtype, scales, data, grad_A, M, N, K, LayoutF32::kEpiCols);
 }
 
 // Row pitch (elements) and bytes of the f16 copy of an M x N grad_out.
@@ -967,7 +1200,7 @@ static int fill_desc_pre(ProblemDesc* d, const uint16_t* go_f16, const float* sc
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   // dtype is not read by this variant (its A operand is f16 already).
-  return fill_desc_rest(d, NF4_BF16, scales, data, grad_A, M, N, K);
+  return fill_desc_rest(d, NF4_BF16, scales, data, grad_A, M, N, K, LayoutPreA::kEpiCols);
 }
 
 static int sm_count(int* out) {
@@ -986,14 +1219,16 @@ static int sm_count(int* out) {
 }
 
 static int launch_to_f16(const void* go, int dtype, uint16_t* dst, int M, int N,
-                         cudaStream_t stream) {
+                         unsigned int* flags, int nflags, cudaStream_t stream) {
   int sms = 0;
   const int rc = sm_count(&sms);
   if (rc != NF4_OK) return rc;
-  const int64_t work = static_cast<int64_t>(M) * (f16_pitch(N) >> 3);
-  const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sms) * 8);
-  to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(go, dtype == NF4_F32 ? 1 : 0,
-                                                                    dst, M, N, f16_pitch(N));
+  // One 16-element group per thread; the grid covers all of them in one pass
+  // up to 64 resident blocks' worth per SM, beyond that threads loop.
+  const int64_t work = static_cast<int64_t>(M) * ((f16_pitch(N) + 15) >> 4);
+  const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sms) * 64);
+  to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      go, dtype == NF4_F32 ? 1 : 0, dst, M, N, f16_pitch(N), flags, nflags);
   return cudaGetLastError() == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
 }
 
@@ -1034,13 +1269,22 @@ static int max_clusters(int* out) {
   return NF4_OK;
 }
 
+// Launch over `total_tiles` tiles; sk == nullptr: all tiles whole, else the
+// split described by *sk (planned for this device's pair count).
 template <class L>
 static int launch_layout(const ProblemDesc& single, const ProblemDesc* batch, int count,
-                         int total_tiles, cudaStream_t stream) {
+                         int total_tiles, const SkArgs* sk_in, cudaStream_t stream) {
   int maxc = 0;
   const int rc = max_clusters<L>(&maxc);
   if (rc != NF4_OK) return rc;
-  const int clusters = std::min(total_tiles, maxc);
+  SkArgs sk;
+  std::memset(&sk, 0, sizeof(sk));
+  sk.dp_tiles = total_tiles;
+  int clusters = std::min(total_tiles, maxc);
+  if (sk_in != nullptr && sk_in->sk_tiles > 0) {
+    sk = *sk_in;
+    clusters = maxc;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1053,7 +1297,7 @@ static int launch_layout(const ProblemDesc& single, const ProblemDesc* batch, in
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, bwd_a_kernel<L>, single, batch, count, total_tiles) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, bwd_a_kernel<L>, single, batch, count, sk) != cudaSuccess)
     return NF4_ERR_CUDA;
   return launch_status();
 }
@@ -1062,8 +1306,8 @@ static int launch_layout(const ProblemDesc& single, const ProblemDesc* batch, in
 // layout only has room for bf16 raw stages).
 static int launch(const ProblemDesc& single, const ProblemDesc* batch, int count, int total_tiles,
                   bool all_bf16, cudaStream_t stream) {
-  return all_bf16 ? launch_layout<LayoutBF16>(single, batch, count, total_tiles, stream)
-                  : launch_layout<LayoutF32>(single, batch, count, total_tiles, stream);
+  return all_bf16 ? launch_layout<LayoutBF16>(single, batch, count, total_tiles, nullptr, stream)
+                  : launch_layout<LayoutF32>(single, batch, count, total_tiles, nullptr, stream);
 }
 
 // ------------------------------------------------------------------ small M
@@ -1269,9 +1513,75 @@ extern "C" int nf4_backward_a(const float* grad_out, const float* scales, const 
   return nf4_backward_a_ex(grad_out, NF4_F32, scales, data, grad_A, M, N, K, stream);
 }
 
+namespace nf4 {
+// Workspace of nf4_backward_a_ws: the f16 copy of grad_out, then (optional)
+// the split-tile flags and partial sums for `pairs` pairs of CTAs.
+constexpr size_t kPartialBytes = static_cast<size_t>(2) * BM * BK * sizeof(float);  // 256 KiB
+static inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+static inline size_t sk_bytes(int pairs) {
+  return round256(sizeof(unsigned int) * static_cast<size_t>(pairs)) +
+         kPartialBytes * static_cast<size_t>(pairs);
+}
+
+// Split plan for T tiles of S stages over `pairs` pairs: whole waves stay whole;
+// the last, partial wave is split by stages when that saves every pair at
+// least kSplitMinSaving stages of the wave (S - rem * S / pairs).  A split
+// tile costs an extra partial-sum epilogue and a dependent finishing epilogue
+// (measured on GB300: worth roughly 30 stages of 64 on the critical path), so
+// smaller savings are not taken.
+constexpr int kSplitMinSaving = 40;
+static void plan_split(int T, int S, int pairs, SkArgs* sk) {
+  sk->dp_tiles = T;
+  sk->sk_tiles = 0;
+  sk->stages = S;
+  if (pairs <= 1 || S <= 1) return;
+  const int rem = T % pairs;
+  if (rem == 0) return;
+  if (static_cast<int64_t>(S) * (pairs - rem) < static_cast<int64_t>(kSplitMinSaving) * pairs)
+    return;
+  sk->dp_tiles = T - rem;
+  sk->sk_tiles = rem;
+}
+}  // namespace nf4
+
+extern "C" int nf4_split_plan(int tiles, int stages, int pairs, int* dp_tiles, int* sk_tiles) {
+  if (tiles <= 0 || stages <= 0 || pairs <= 0 || dp_tiles == nullptr || sk_tiles == nullptr)
+    return -1;
+  SkArgs sk;
+  std::memset(&sk, 0, sizeof(sk));
+  plan_split(tiles, stages, pairs, &sk);
+  *dp_tiles = sk.dp_tiles;
+  *sk_tiles = sk.sk_tiles;
+  return 0;
+}
+
+extern "C" int nf4_split_item(int tiles, int stages, int pairs, int pair, int k, int* item) {
+  if (tiles <= 0 || stages <= 0 || pairs <= 0 || pair < 0 || pair >= pairs || k < 0 ||
+      item == nullptr)
+    return -1;
+  SkArgs sk;
+  std::memset(&sk, 0, sizeof(sk));
+  plan_split(tiles, stages, pairs, &sk);
+  const Item w = item_at(sk, pair, pairs, k);
+  if (w.t < 0) return 0;
+  item[0] = w.t;
+  item[1] = w.s0;
+  item[2] = w.s1 < stages ? w.s1 : stages;
+  // Pairs whose partial sums the item's epilogue adds (a first-stage item of
+  // a split tile): those of item[3] .. item[4] inclusive that hold any stage
+  // (nf4_split_item reports them), none when item[4] < item[3].
+  item[3] = pair + 1;
+  item[4] = pair;
+  if (w.t >= sk.dp_tiles && w.s0 == 0 && item[2] < stages)
+    item[4] = sk_owner(sk, static_cast<int64_t>(w.t - sk.dp_tiles) * stages + stages - 1, pairs);
+  return 1;
+}
+
 extern "C" size_t nf4_backward_a_ws_bytes(int M, int N) {
   if (M <= 0 || N <= 0) return 0;
-  return f16_bytes(M, N);
+  int pairs = 0;
+  if (max_clusters<LayoutPreA>(&pairs) != NF4_OK || pairs <= 0) return round256(f16_bytes(M, N));
+  return round256(f16_bytes(M, N)) + sk_bytes(pairs);
 }
 
 extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float* scales,
@@ -1295,9 +1605,30 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
   if (rc != NF4_OK) return rc;
   const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
   if (tiles > INT_MAX) return NF4_ERR_INVALID;
-  rc = launch_to_f16(grad_out, go_dtype, go_f16, M, N, as_stream(stream));
+  int pairs = 0;
+  rc = max_clusters<LayoutPreA>(&pairs);
   if (rc != NF4_OK) return rc;
-  return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles), as_stream(stream));
+  // The split needs its flags and partial sums after the f16 copy; a workspace
+  // holding only the copy runs every tile whole.
+  SkArgs sk;
+  std::memset(&sk, 0, sizeof(sk));
+  const size_t base = round256(f16_bytes(M, N));
+  unsigned int* flags = nullptr;
+  int nflags = 0;
+  if (workspace_bytes >= base + sk_bytes(pairs)) {
+    plan_split(static_cast<int>(tiles), d.n_stages, pairs, &sk);
+    if (sk.sk_tiles > 0) {
+      uint8_t* w = static_cast<uint8_t*>(workspace) + base;
+      flags = reinterpret_cast<unsigned int*>(w);
+      nflags = pairs;
+      sk.flags = flags;
+      sk.partials = reinterpret_cast<float*>(w + round256(sizeof(unsigned int) * pairs));
+    }
+  }
+  rc = launch_to_f16(grad_out, go_dtype, go_f16, M, N, flags, nflags, as_stream(stream));
+  if (rc != NF4_OK) return rc;
+  return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles),
+                                   sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream));
 }
 
 extern "C" size_t nf4_backward_a_batched_workspace(int count) {

@@ -1,6 +1,6 @@
 // nf4_trace.cuh -- optional timing probes, compiled in only with -DNF4_TRACE.
 //
-// The first two CTAs of a launch record clock64() at fixed points of each role
+// The first CTAs of a launch record clock64() at fixed points of each role
 // into a device buffer [cta][event][slot] set with nf4_debug_set_trace(); the
 // event numbers are listed at each kernel.  Without NF4_TRACE the probes expand
 // to nothing.
@@ -8,7 +8,7 @@
 
 namespace nf4 {
 // Pair kernel (bwd_a_kernel):
-// the two CTAs of cluster 0 record clock64() at fixed points of each role into
+// the CTAs of clusters 0 and 1 record clock64() at fixed points of each role into
 // a device buffer [cta][event][slot]; event kTraceEvents-1 slot 0 is the clock
 // right after the start-up cluster barrier, the common reference of both CTAs.
 // Events: 0-15 converter warp after its operand-slot wait, 16-31 converter warp
@@ -17,7 +17,9 @@ namespace nf4 {
 // 42 converter group leader sees raw data, 43 converter group leader starts,
 // 44 slot 0 kernel entry / slot 1 all roles done / slot 2 after the last
 // cluster barrier; pre-converted variant: 45 A producer issues the stage's A
-// copy, 46 watcher sees both A copies landed; 48-63 converter warp 0-15 has
+// copy, 46 watcher sees both A copies landed; epilogue: 34 slot k = item k's
+// partial sums written and counted, 37 slot k = item k's partner counts all
+// seen; 48-63 converter warp 0-15 has
 // stored its B^T chunks, 64-79 it has also passed the proxy fence.
 //
 // Few-token kernel (small_m_kernel), CTAs 0 and 1 (k-tile 0, cluster ranks 0
@@ -32,9 +34,10 @@ namespace nf4 {
 __device__ unsigned long long* g_trace = nullptr;
 constexpr int kTraceSlots = 512;
 constexpr int kTraceEvents = 88;
+constexpr unsigned kTraceCtas = 4;  // the first two pairs
 // Each kernel caches the buffer pointer once (NF4_TRACE_INIT), so a probe is a
 // clock read and one store.
-#define NF4_TRACE_INIT unsigned long long* const nf4_trace_buf = blockIdx.x < 2 ? g_trace : nullptr
+#define NF4_TRACE_INIT unsigned long long* const nf4_trace_buf = blockIdx.x < kTraceCtas ? g_trace : nullptr
 #define NF4_PROBE(ev, idx)                                                               \
   do {                                                                                   \
     if (nf4_trace_buf != nullptr && (idx) < kTraceSlots)                                 \

@@ -462,7 +462,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="q_proj", choices=sorted(workloads()))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--entry", default="plain", choices=["plain", "ws"],
+    ap.add_argument("--entry", default="ws", choices=["plain", "ws"],
                     help="single-problem entry point: nf4_backward_a_ex, or nf4_backward_a_ws "
                          "(f16 pre-pass into a workspace, then the GEMM)")
     ap.add_argument("--no-e2e", action="store_true")

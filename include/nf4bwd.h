@@ -105,9 +105,12 @@ int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float* scales,
                       const uint8_t* data, float* grad_A, int M, int N, int K, void* stream);
 
 /*
- * Bytes of device workspace nf4_backward_a_ws needs for an M x N grad_out: an
- * f16 copy with rows padded to a multiple of 8 elements, 2 * M * ((N + 7) & ~7)
- * bytes (0 when M or N is not positive).
+ * Bytes of device workspace nf4_backward_a_ws needs for an M x N grad_out on
+ * the current device: an f16 copy with rows padded to a multiple of 8 elements
+ * (2 * M * ((N + 7) & ~7) bytes, rounded up to 256), then room for the split
+ * of a last partial wave of tiles (nf4_split_plan): one flag word and one
+ * 256 KiB fp32 partial-sum tile per pair of CTAs the device runs at once.
+ * 0 when M or N is not positive.
  */
 size_t nf4_backward_a_ws_bytes(int M, int N);
 
@@ -116,14 +119,17 @@ size_t nf4_backward_a_ws_bytes(int M, int N);
  * grad_out to f16 (the rounding the GEMM applies to its A operand anyway: page
  * above, build_ptx "PHASE 1", cvt.rn.f16) into `workspace`, then the GEMM loads
  * its A operand from that copy with TMA instead of converting it in shared
- * memory.  The result equals nf4_backward_a_ex's bit for bit.  The pages have
+ * memory.  Without a split (nf4_split_plan) the result equals
+ * nf4_backward_a_ex's bit for bit; a split tile adds the pairs' fp32 partial
+ * sums in pair order, a different but fixed rounding.  The pages have
  * no counterpart of the split: it trades 6 (fp32) or 4 (bf16) bytes of HBM
  * traffic per grad_out element for shared-memory bandwidth inside the GEMM.
  *   workspace        caller-owned device memory, 256-byte aligned, at least
  *                    nf4_backward_a_ws_bytes(M, N) bytes; overwritten; must not
  *                    be used by anything else until the stream has run the call
- *   workspace_bytes  its size; too small, NULL or misaligned returns
- *                    NF4_ERR_WORKSPACE and enqueues nothing
+ *   workspace_bytes  its size; smaller than the f16 copy, NULL or misaligned
+ *                    returns NF4_ERR_WORKSPACE and enqueues nothing; room for
+ *                    the f16 copy only runs every tile whole (no split)
  * M at most the few-token limit (nf4_set_small_m_max), M == 0 and N == 0 take
  * the same paths as nf4_backward_a_ex and do not touch the workspace (it may
  * then be NULL).
@@ -131,6 +137,28 @@ size_t nf4_backward_a_ws_bytes(int M, int N);
 int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float* scales,
                       const uint8_t* data, float* grad_A, int M, int N, int K, void* workspace,
                       size_t workspace_bytes, void* stream);
+
+/*
+ * The split plan of nf4_backward_a_ws, as pure host computations (no device is
+ * touched), for `tiles` pair tiles (256 tokens x 256 output columns) of
+ * `stages` 64-wide stages of N each, run by `pairs` pairs of CTAs.  Whole waves
+ * of tiles stay whole (tiles [0, dp_tiles), round-robin); when splitting the
+ * last, partial wave saves every pair at least 40 stages (stages * (pairs -
+ * rem) >= 40 * pairs, rem = tiles % pairs), its sk_tiles = rem tiles are split
+ * by stages, one contiguous run of their stages per pair.  Returns -1 for a
+ * non-positive count or a NULL output.
+ */
+int nf4_split_plan(int tiles, int stages, int pairs, int* dp_tiles, int* sk_tiles);
+
+/*
+ * Item k (k = 0, 1, ...) of pair `pair` under that plan, in the order the pair
+ * runs them: item[0] the tile, [item[1], item[2]) its stages, and for the
+ * first stages of a split tile the range item[3] .. item[4] of pairs whose
+ * partial sums the pair adds before storing the tile: every pair of the range
+ * that holds stages of split tiles (item[4] < item[3]: none).  Returns 1, 0 when the pair has
+ * no item k, -1 for invalid arguments.
+ */
+int nf4_split_item(int tiles, int stages, int pairs, int pair, int k, int* item);
 
 /*
  * Few-token path.  A call of nf4_backward_a / nf4_backward_a_ex with M at most

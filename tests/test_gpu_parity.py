@@ -365,12 +365,17 @@ def test_full_size_sampled_rows(name, p):
 
 # ---------------------------------------------------------------- pre-converted entry point
 # nf4_backward_a_ws rounds grad_out to f16 in a pass of its own and feeds the
-# GEMM's A operand by TMA; the tile order, the MMAs and their order are those of
-# the plain entry point, so the two results agree bit for bit.
+# GEMM's A operand by TMA.  With a workspace that holds only the f16 copy, the
+# tiles, the MMAs and their order are those of the plain entry point, so the
+# two results agree bit for bit; with the full workspace a last partial wave of
+# tiles is split by stages over all pairs (nf4_split_plan) and the partial sums
+# are added in pair order.
 WS = SMALL + [
     Problem(300, 196, 640, F32, 1.0, 0.02, True, 40, "ws-pitch-pad"),   # f16 rows padded to 200
     Problem(200, 4, 192, F32, 1.0, 0.02, False, 41, "ws-n4"),            # one half group per row
     Problem(513, 1032, 768, BF16, 1e-2, 0.02, True, 42, "ws-bf16-3-row-pairs"),
+    Problem(512, 4096, 512, F32, 1e-2, 0.015, False, 44, "ws-4-tiles-of-64-stages"),  # ~19 pairs a tile
+    Problem(2560, 576, 2048, BF16, 1e-2, 0.02, True, 45, "ws-80-tiles"),  # one wave + 4 split tiles
 ]
 
 
@@ -381,18 +386,51 @@ def test_ws_full_check(p):
 
 
 @pytest.mark.parametrize("p", WS, ids=lambda p: p.name)
-def test_ws_equals_plain_bitwise(p):
+def test_ws_unsplit_equals_plain_bitwise(p):
     go = to_device_go(make_grad_out(p), p.go_dtype)
     w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
     with nb().small_m_max(0):
         plain = nb().backward_a(go, w)
-        pre = nb().backward_a_ws(go, w)
+        pre = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
     nb().check_error()
     assert torch.equal(plain, pre)
 
 
+def test_ws_split_is_deterministic_and_close_to_unsplit():
+    p = Problem(512, 4096, 512, F32, 1.0, 0.015, True, 46)
+    go = to_device_go(make_grad_out(p), p.go_dtype)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    ws = nb().ws_workspace(p.M, p.N)
+    runs = [nb().backward_a_ws(go, w, ws) for _ in range(3)]
+    whole = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
+    nb().check_error()
+    assert torch.equal(runs[0], runs[1]) and torch.equal(runs[0], runs[2])
+    # Same products, different fp32 summation order: equal up to rounding.
+    assert torch.allclose(runs[0], whole, rtol=1e-4, atol=1e-4)
+    # 4 tiles of 64 stages over every pair: each tile is split many ways, so
+    # some element rounds differently (this checks the split took place).
+    assert not torch.equal(runs[0], whole)
+
+
+def test_ws_whole_waves_plus_split_wave_sampled_rows():
+    """96 tiles of 64 stages on a 152-SM GB300 (76 pairs): one whole wave, then
+    20 tiles split by stages over all pairs (some pairs finish a split tile and
+    also wrote a partial sum for another)."""
+    p = Problem(2048, 4096, 3072, BF16, 1e-2, 0.02, True, 47, "ws-96-tiles")
+    run_problem(p, rows=sample_rows(p.M, 8, p.seed), check_codes=False, entry="ws")
+    go = to_device_go(make_grad_out(p), p.go_dtype)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    ws = nb().ws_workspace(p.M, p.N)
+    a = nb().backward_a_ws(go, w, ws)
+    b = nb().backward_a_ws(go, w, ws)
+    whole = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
+    nb().check_error()
+    assert torch.equal(a, b)
+    assert torch.allclose(a, whole, rtol=1e-4, atol=1e-5)
+
+
 @pytest.mark.parametrize("name,p", FULL, ids=[p.name for _, p in FULL])
-def test_ws_full_size_sampled_rows_and_bitwise(name, p):
+def test_ws_full_size_sampled_rows_and_deterministic(name, p):
     if p.M <= 64:
         pytest.skip("few-token shapes take the same path through both entry points")
     run_problem(p, rows=sample_rows(p.M, 6, p.seed + 1), check_codes=False, entry="ws")
@@ -401,10 +439,11 @@ def test_ws_full_size_sampled_rows_and_bitwise(name, p):
     ws = nb().ws_workspace(p.M, p.N)
     first = nb().backward_a_ws(go, w, ws)
     again = nb().backward_a_ws(go, w, ws)
+    unsplit = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
     plain = nb().backward_a(go, w)
     nb().check_error()
     assert torch.equal(first, again)
-    assert torch.equal(first, plain)
+    assert torch.equal(unsplit, plain)
 
 
 def test_ws_rejects_bad_workspace_without_launching():
@@ -415,7 +454,8 @@ def test_ws_rejects_bad_workspace_without_launching():
     go = to_device_go(make_grad_out(p), F32)
     w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
     need = int(L.nf4_backward_a_ws_bytes(p.M, p.N))
-    assert need == 2 * p.M * ((p.N + 7) // 8 * 8)
+    copy = 2 * p.M * ((p.N + 7) // 8 * 8)  # the f16 copy alone
+    assert need >= copy + 256 * 1024       # plus the split's flags and partial sums
     out = torch.full((p.M, p.K), 7.0, device="cuda")
     ws = torch.empty(need + 512, dtype=torch.uint8, device="cuda")
 
@@ -426,7 +466,7 @@ def test_ws_rejects_bad_workspace_without_launching():
 
     with nb().small_m_max(64):
         assert call(None, 0) == nb().NF4_ERR_WORKSPACE
-        assert call(C.c_void_p(ws.data_ptr()), need - 1) == nb().NF4_ERR_WORKSPACE
+        assert call(C.c_void_p(ws.data_ptr()), copy - 1) == nb().NF4_ERR_WORKSPACE
         assert call(C.c_void_p(ws.data_ptr() + 16), need) == nb().NF4_ERR_WORKSPACE
         torch.cuda.synchronize()
         assert bool((out == 7.0).all())
@@ -434,4 +474,6 @@ def test_ws_rejects_bad_workspace_without_launching():
         assert call(None, 0, M=16) == nb().NF4_OK
         nb().check_error()
         assert call(C.c_void_p(ws.data_ptr()), need) == nb().NF4_OK
+        nb().check_error()
+        assert call(C.c_void_p(ws.data_ptr()), copy) == nb().NF4_OK  # no room to split: whole tiles
         nb().check_error()
