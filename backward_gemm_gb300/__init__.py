@@ -27,6 +27,7 @@ NF4_ERR_TIMEOUT = 4
 NF4_ERR_WORKSPACE = 5
 NF4_F32 = 0
 NF4_BF16 = 1
+NF4_F16 = 2
 
 # Every function the header declares, with (restype, argtypes).
 _vp, _i, _sz = C.c_void_p, C.c_int, C.c_size_t
@@ -105,7 +106,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return NF4_F32
     if t.dtype == torch.bfloat16:
         return NF4_BF16
-    raise TypeError(f"grad_out must be float32 or bfloat16, got {t.dtype}")
+    if t.dtype == torch.float16:
+        return NF4_F16
+    raise TypeError(f"grad_out must be float32, bfloat16 or float16, got {t.dtype}")
 
 
 def _require_cuda_contig(name: str, t: torch.Tensor) -> None:

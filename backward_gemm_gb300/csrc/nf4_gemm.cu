@@ -1126,7 +1126,7 @@ static bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* ba
 // Argument rules shared by the single and grouped entry points.
 static int check_problem(const void* go, int dtype, const float* scales, const uint8_t* data,
                          const float* grad_A, int M, int N, int K) {
-  if (dtype != NF4_F32 && dtype != NF4_BF16) return NF4_ERR_INVALID;
+  if (dtype != NF4_F32 && dtype != NF4_BF16 && dtype != NF4_F16) return NF4_ERR_INVALID;
   if (M < 0 || N < 0 || K <= 0 || K % 64 != 0) return NF4_ERR_INVALID;
   if (M == 0) return NF4_OK;
   if (grad_A == nullptr) return NF4_ERR_INVALID;
@@ -1498,6 +1498,16 @@ extern "C" int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float
                ? NF4_OK
                : NF4_ERR_CUDA;
   }
+  if (go_dtype == NF4_F16) {
+    // Already the A operand's type: the pre-converted kernel reads it as is.
+    ProblemDesc d;
+    rc = fill_desc_pre(&d, static_cast<const uint16_t*>(grad_out), scales, data, grad_A, M, N, K);
+    if (rc != NF4_OK) return rc;
+    const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
+    if (tiles > INT_MAX) return NF4_ERR_INVALID;
+    return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles), nullptr,
+                                     as_stream(stream));
+  }
   if (M <= small_m::g_max_m.load())
     return small_m::run(grad_out, go_dtype, scales, data, grad_A, M, N, K, as_stream(stream));
   ProblemDesc d;
@@ -1595,11 +1605,14 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
                ? NF4_OK
                : NF4_ERR_CUDA;
   }
-  if (M <= small_m::g_max_m.load())
+  const bool f16_in = go_dtype == NF4_F16;
+  if (!f16_in && M <= small_m::g_max_m.load())
     return small_m::run(grad_out, go_dtype, scales, data, grad_A, M, N, K, as_stream(stream));
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < f16_bytes(M, N))
     return NF4_ERR_WORKSPACE;
-  uint16_t* go_f16 = static_cast<uint16_t*>(workspace);
+  // f16 grad_out is the A operand already (the copy region goes unused).
+  const uint16_t* go_f16 = f16_in ? static_cast<const uint16_t*>(grad_out)
+                                  : static_cast<uint16_t*>(workspace);
   ProblemDesc d;
   rc = fill_desc_pre(&d, go_f16, scales, data, grad_A, M, N, K);
   if (rc != NF4_OK) return rc;
@@ -1625,8 +1638,16 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
       sk.partials = reinterpret_cast<float*>(w + round256(sizeof(unsigned int) * pairs));
     }
   }
-  rc = launch_to_f16(grad_out, go_dtype, go_f16, M, N, flags, nflags, as_stream(stream));
-  if (rc != NF4_OK) return rc;
+  if (f16_in) {
+    // No pre-pass: zero the split flags on the stream instead.
+    if (nflags > 0 && cudaMemsetAsync(flags, 0, sizeof(unsigned int) * nflags,
+                                      as_stream(stream)) != cudaSuccess)
+      return NF4_ERR_CUDA;
+  } else {
+    rc = launch_to_f16(grad_out, go_dtype, static_cast<uint16_t*>(workspace), M, N, flags, nflags,
+                       as_stream(stream));
+    if (rc != NF4_OK) return rc;
+  }
   return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles),
                                    sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream));
 }
@@ -1641,6 +1662,7 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
   if (count < 0 || (count > 0 && problems == nullptr)) return NF4_ERR_INVALID;
   for (int i = 0; i < count; ++i) {
     const nf4_problem& p = problems[i];
+    if (p.go_dtype == NF4_F16) return NF4_ERR_INVALID;  // single calls only
     const int rc = check_problem(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
     if (rc != NF4_OK) return rc;
   }
@@ -1786,6 +1808,7 @@ extern "C" int nf4_backward_a_batched_noalloc(const nf4_problem* problems, int c
   if (count > kNoAllocMaxProblems) return NF4_ERR_WORKSPACE;
   for (int i = 0; i < count; ++i) {
     const nf4_problem& p = problems[i];
+    if (p.go_dtype == NF4_F16) return NF4_ERR_INVALID;  // single calls only
     const int rc = check_problem(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
     if (rc != NF4_OK) return rc;
   }

@@ -56,7 +56,9 @@ typedef enum nf4_status {
   NF4_ERR_WORKSPACE = 5 /* workspace missing, misaligned or too small */
 } nf4_status;
 
-typedef enum nf4_dtype { NF4_F32 = 0, NF4_BF16 = 1 } nf4_dtype;
+/* Type of grad_out.  NF4_F16 is already the GEMM's operand type (no rounding
+ * step); it is accepted by nf4_backward_a_ex and nf4_backward_a_ws only. */
+typedef enum nf4_dtype { NF4_F32 = 0, NF4_BF16 = 1, NF4_F16 = 2 } nf4_dtype;
 
 /* Version of this ABI (incremented on any incompatible change). */
 int nf4_abi_version(void);
@@ -99,8 +101,11 @@ int nf4_dequantize_f16(const float* scales, const uint8_t* data, int K, int N, u
 int nf4_backward_a(const float* grad_out, const float* scales, const uint8_t* data,
                    float* grad_A, int M, int N, int K, void* stream);
 
-/* As nf4_backward_a, with grad_out of type go_dtype (NF4_F32 or NF4_BF16;
- * bf16 needs N % 8 == 0). */
+/* As nf4_backward_a, with grad_out of type go_dtype (NF4_F32, NF4_BF16 or
+ * NF4_F16; bf16 and f16 need N % 8 == 0).  f16 grad_out feeds the pair kernel's
+ * TMA-loaded A operand as it is, whatever M (the few-token kernel takes fp32
+ * and bf16 only); its result equals nf4_backward_a_ws's without a split for
+ * the same values given in fp32 or bf16 (the rounding to f16 then happens first). */
 int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float* scales,
                       const uint8_t* data, float* grad_A, int M, int N, int K, void* stream);
 
@@ -132,7 +137,8 @@ size_t nf4_backward_a_ws_bytes(int M, int N);
  *                    the f16 copy only runs every tile whole (no split)
  * M at most the few-token limit (nf4_set_small_m_max), M == 0 and N == 0 take
  * the same paths as nf4_backward_a_ex and do not touch the workspace (it may
- * then be NULL).
+ * then be NULL).  With NF4_F16 grad_out there is no pre-pass: the GEMM reads
+ * grad_out directly and the workspace's copy region goes unused.
  */
 int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float* scales,
                       const uint8_t* data, float* grad_A, int M, int N, int K, void* workspace,
@@ -185,7 +191,7 @@ int nf4_small_m_split(int N, int K, int sms, int cta_slots, int* per_out);
 /* One projection of a grouped launch. */
 typedef struct nf4_problem {
   const void* grad_out; /* [M][N], type go_dtype */
-  int go_dtype;         /* NF4_F32 or NF4_BF16 */
+  int go_dtype;         /* NF4_F32 or NF4_BF16 (NF4_F16: NF4_ERR_INVALID) */
   const float* scales;  /* [N][K/64] */
   const uint8_t* data;  /* [N][K/2] */
   float* grad_A;        /* [M][K], overwritten */

@@ -477,3 +477,44 @@ def test_ws_rejects_bad_workspace_without_launching():
         nb().check_error()
         assert call(C.c_void_p(ws.data_ptr()), copy) == nb().NF4_OK  # no room to split: whole tiles
         nb().check_error()
+
+
+# ---------------------------------------------------------------- f16 grad_out
+# grad_out given in f16 is the A operand as is: the oracle's operand-level
+# product (f16 operands, exact products, fp64 sum) is the reference, and the
+# result equals that of the same values given in fp32 through the unsplit
+# pre-converted path (the conversion to f16 is then exact).
+F16_CASES = [
+    Problem(300, 200, 640, F32, 1.0, 0.02, True, 50, "f16-ragged"),
+    Problem(16, 1536, 1536, F32, 1e-2, 0.02, False, 51, "f16-m16"),
+    Problem(600, 4096, 512, F32, 1e-2, 0.015, False, 52, "f16-long-n"),
+]
+
+
+@pytest.mark.parametrize("p", F16_CASES, ids=lambda p: p.name)
+def test_f16_grad_out_matches_oracle_and_f32_path(p):
+    go32 = make_grad_out(p)
+    go16 = oracle.f32_to_f16(go32)                      # f16 bits, RNE
+    B = make_weight(p)
+    w = nb().quantize(torch.from_numpy(B).cuda())
+    go_dev = torch.from_numpy(go16.view(np.int16)).cuda().view(torch.float16)
+    got = nb().backward_a(go_dev, w)
+    nb().check_error()
+    data_o, scales_o = oracle.quantize(B)
+    bt = oracle.dequantize_f16(scales_o, data_o, p.K, p.N)
+    ref, bound = oracle.backward_a_rows(go16, bt, np.arange(p.M, dtype=np.int32))
+    assert_close(got.cpu().numpy(), ref, bound, f"{p}")
+    # The same values in fp32 (exactly representable) through the pre-pass.
+    go_back = torch.from_numpy(go16.view(np.float16).astype(np.float32)).cuda()
+    with nb().small_m_max(0):
+        via32 = nb().backward_a_ws(go_back, w, nb().ws_workspace(p.M, p.N, split=False))
+    nb().check_error()
+    assert torch.equal(got, via32)
+
+
+def test_f16_grad_out_rejected_by_grouped_launch():
+    p = Problem(300, 192, 640, F32, 1.0, 0.02, False, 53)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    go = torch.zeros((p.M, p.N), dtype=torch.float16, device="cuda")
+    with pytest.raises(nb().Nf4Error):
+        nb().backward_a_batched([(go, w, None)])
