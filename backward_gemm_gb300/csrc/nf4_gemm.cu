@@ -1328,6 +1328,15 @@ static int fill(SmallDesc* d, const void* go, int dtype, const float* scales, co
                  static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), SK / 2, SN,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
+  const int KB = K / 64;
+  d->scale_tma = 0;
+  if (KB % 4 == 0 && aligned(scales, 16)) {
+    if (!encode_2d(&d->tm_scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales,
+                   static_cast<uint64_t>(KB), static_cast<uint64_t>(N),
+                   static_cast<uint64_t>(KB) * 4, SK / 64, SN, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return NF4_ERR_CUDA;
+    d->scale_tma = 1;
+  }
   d->scales = scales;
   d->grad_A = grad_A;
   d->M = M;

@@ -19,7 +19,9 @@
 //
 //   CTA         MP tokens (MP in {16, 32, 64}, rows >= M are TMA zero fill) x 256
 //               output columns k, over the n-slice of its cluster rank, 64 n per
-//               stage (4 MMAs of M = 128, N = 256, K = 16; A rows >= MP are zero)
+//               stage (4 MMAs of M = 128, N = 256, K = 16; only A rows < MP are
+//               stored: the MMA's rows >= MP read the start of the slot's B
+//               operand, and their accumulator rows are never read)
 //   warps 0, 18 TMA producers of the even and odd stages.  The copies one
 //               thread issues are served one after another, so every (ring slot,
 //               box) pair has its own lane: grad_out (one or two boxes of MP rows
@@ -52,12 +54,12 @@ constexpr int kConvWarps = kConvGroups * kGroupWarps;
 constexpr int kProducer2Warp = kConvWarp0 + kConvWarps;   // 18
 constexpr int kThreads = (kProducer2Warp + 1) * 32;       // 608
 constexpr int kNf4Bytes = SN * (SK / 2);                  // 64 rows n x 128 bytes
-constexpr int kABytes = kMmaM * SN * 2;                   // 16 KB: 128 rows x 64 n, K-major
+constexpr int kABytes = kMmaM * SN * 2;                   // 16 KB: what an MMA's A reads
 constexpr int kBBytes = SK * SN * 2;                      // 32 KB: 256 k x 64 n, MN-major
-constexpr int kOpBytes = kABytes + kBBytes;
 constexpr uint32_t kBLbo = SN * 128;                      // 8 KB: one 64-k chunk of B
 constexpr uint32_t kSbo = 1024;
-constexpr int kBoxLanes = 3;     // producer lanes per ring slot: grad_out x2, NF4
+constexpr int kScaleBytes = SN * 16;                     // 64 rows n x the tile's 4 block scales
+constexpr int kBoxLanes = 4;     // producer lanes per ring slot: grad_out x2, NF4, scales
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kTmemCols = SK;
 constexpr int kPartStride = SK + 4;  // floats per partial-tile row (the pad spreads banks)
@@ -68,10 +70,17 @@ struct Config {
   static constexpr int kRawStages = RS;
   static constexpr int kOpStages = OS;
   // Raw stage: grad_out (two 32-column fp32 boxes, or one 64-column bf16 box,
-  // MP rows of 128 bytes each, 128-byte swizzle), then the NF4 bytes.
+  // MP rows of 128 bytes each, 128-byte swizzle), then the NF4 bytes, then the
+  // stage's block scales (when they travel by TMA).
   static constexpr int kGoBoxBytes = MP * 128;
   static constexpr int kGoBytes = 2 * kGoBoxBytes;
-  static constexpr int kRawBytes = kGoBytes + kNf4Bytes;
+  static constexpr int kScaleOff = kGoBytes + kNf4Bytes;
+  static constexpr int kRawBytes = kGoBytes + kNf4Bytes + kScaleBytes;
+  // Operand slot: the MP real rows of the K-major A operand (128 bytes each),
+  // then B.  The MMA reads 128 A rows (16 KB); rows >= MP fall on B's first
+  // bytes, which is harmless: accumulator rows >= MP are never read.
+  static constexpr int kAReal = MP * 128;
+  static constexpr int kOpBytes = kAReal + kBBytes;
   static constexpr int kRawOff = 0;
   static constexpr int kOpOff = RS * kRawBytes;
   static constexpr int kBarOff = kOpOff + OS * kOpBytes;
@@ -82,8 +91,10 @@ struct Config {
   // loop is done.
   static constexpr int kPartialBytes = MP * kPartStride * 4;
   static_assert(kPartialBytes <= RS * kRawBytes, "partial tile fits in the raw ring");
-  static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kGoBytes % 1024 == 0,
+  static_assert(kRawBytes % 1024 == 0 && kOpBytes % 1024 == 0 && kGoBytes % 1024 == 0 &&
+                    kAReal % 1024 == 0,
                 "stage alignment");
+  static_assert(kABytes <= kOpBytes, "an MMA's A reads stay inside the slot");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert((RS / 2) * kBoxLanes <= 32, "one producer lane per (slot, box)");
   // Each raw slot must always be consumed by the same converter group: a group
@@ -93,18 +104,25 @@ struct Config {
 };
 
 // Operand slots outnumber the converter groups, so that a group can fill its
-// next slot while the tensor core still reads the previous one.
-using Cfg16 = Config<16, 4, 3>;
-using Cfg32 = Config<32, 4, 3>;
-using Cfg64 = Config<64, 4, 2>;
+// next slot while the tensor core still reads the previous one.  The weight
+// stream is latency-bound (an NF4 box takes ~2-2.5 us from HBM), so the raw
+// ring is as deep as shared memory allows: bytes in flight per SM set the rate.
+using Cfg16 = Config<16, 6, 4>;
+using Cfg32 = Config<32, 4, 4>;
+using Cfg64 = Config<64, 4, 3>;
 
 struct SmallDesc {  // 64-byte aligned (CUtensorMap)
-  CUtensorMap tm_go;   // grad_out [M][N], box (32 fp32 | 64 bf16) columns x MP rows, 128B swizzle
-  CUtensorMap tm_nf4;  // codes [N][K/2] bytes, box 128 bytes x 64 rows, 128B swizzle
+  CUtensorMap tm_go;      // grad_out [M][N], box (32 fp32 | 64 bf16) columns x MP rows, 128B swizzle
+  CUtensorMap tm_nf4;     // codes [N][K/2] bytes, box 128 bytes x 64 rows, 128B swizzle
+  CUtensorMap tm_scales;  // scales [N][K/64] fp32, box 4 x 64 rows (if scale_tma)
   const float* scales;
   float* grad_A;
   int M, N, K, dtype;
   int n_per_cta;       // n-slice of one cluster rank, a multiple of SN
+  // 1: each stage's 64 rows x 4 block scales come as one more TMA box of the
+  // raw stage (K % 256 == 0 and 16-byte aligned scales); 0: each converter
+  // thread loads its scale from global memory well ahead of its use.
+  int scale_tma;
 };
 
 __device__ __forceinline__ uint32_t cluster_id_x() {
@@ -177,17 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  // A-operand rows MP..127 are zero in every slot and never written again (the
-  // rows of a 128-byte-swizzled K-major tile are contiguous 128-byte rows).
-  {
-    constexpr int kZeroChunks = (kMmaM - MP) * 128 / 16;
-    for (int i = threadIdx.x; i < OS * kZeroChunks; i += kThreads) {
-      const uint32_t slot = static_cast<uint32_t>(i / kZeroChunks);
-      const uint32_t c = static_cast<uint32_t>(i % kZeroChunks);
-      sts128(sbase + C::kOpOff + slot * kOpBytes + MP * 128 + c * 16, make_uint4(0, 0, 0, 0));
-    }
-    fence_proxy_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -201,20 +208,25 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     // warp waiting on different barriers would wake together), then the lanes
     // 3*i + b of the slot's index i issue its box b in one instruction: b = 0
     // grad_out columns 0-31 (fp32) or 0-63 (bf16) and the stage's byte count,
-    // b = 1 fp32 columns 32-63, b = 2 the NF4 bytes.  Boxes may land before the
-    // byte count is registered: the phase cannot complete while that arrival
-    // is pending.
+    // b = 1 fp32 columns 32-63, b = 2 the NF4 bytes, b = 3 the block scales.
+    // Boxes may land before the byte count is registered: the phase cannot
+    // complete while that arrival is pending.
     const int p = warp == kProducerWarp ? 0 : 1;
     const int my_slot = p + 2 * (lane / kBoxLanes), box = lane % kBoxLanes;
-    const bool my_box = lane < (RS / 2) * kBoxLanes && (box != 1 || f32);
-    const CUtensorMap* my_map = box == 2 ? &d.tm_nf4 : &d.tm_go;
-    const uint32_t my_dst = sbase + C::kRawOff + static_cast<uint32_t>(my_slot) * C::kRawBytes +
-                            (box == 0 ? 0u : (box == 1 ? C::kGoBoxBytes : C::kGoBytes));
+    const bool my_box = lane < (RS / 2) * kBoxLanes &&
+                        (box == 3 ? d.scale_tma != 0 : (box != 1 || f32));
+    const CUtensorMap* my_map = box == 3 ? &d.tm_scales : (box == 2 ? &d.tm_nf4 : &d.tm_go);
+    const uint32_t my_dst =
+        sbase + C::kRawOff + static_cast<uint32_t>(my_slot) * C::kRawBytes +
+        (box == 0 ? 0u : (box == 1 ? C::kGoBoxBytes : (box == 2 ? C::kGoBytes : C::kScaleOff)));
+    // x of the NF4 box: the tile's 128 bytes; of the scale box: its 4 blocks.
+    const int my_x = box == 3 ? kt * (SK / 64) : kt * (SK / 2);
     if (lane == 0) {
       tma_prefetch_desc(&d.tm_go);
       tma_prefetch_desc(&d.tm_nf4);
     }
-    const uint32_t bytes = static_cast<uint32_t>((f32 ? 2 : 1) * C::kGoBoxBytes + kNf4Bytes);
+    const uint32_t bytes = static_cast<uint32_t>((f32 ? 2 : 1) * C::kGoBoxBytes + kNf4Bytes +
+                                                 (d.scale_tma ? kScaleBytes : 0));
     int s = p;
     for (; s < ns; s += 2) {
       const uint32_t slot = s % RS;
@@ -225,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         const uint32_t fb = full_raw(slot);
         const int n0 = n_begin + s * SN;
         if (box == 0) mbar_arrive_expect_tx(fb, bytes);
-        tma_load_2d(my_dst, my_map, box == 2 ? kt * (SK / 2) : n0 + 32 * box, box == 2 ? n0 : 0, fb);
+        tma_load_2d(my_dst, my_map, box >= 2 ? my_x : n0 + 32 * box, box >= 2 ? n0 : 0, fb);
         if (box == 2) NF4_PROBE(0, s);
       }
       __syncwarp();
@@ -237,39 +249,46 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop and one elected lane issues (a converged
+    // issuer keeps the MMA operands in uniform registers, see elect_one).
+    {
       constexpr uint32_t idesc = idesc_f16_f32(kMmaM, SK, /*A K-major*/ 0, /*B MN-major*/ 1);
       const uint64_t a_desc0 = smem_desc_sw128(sbase + C::kOpOff, 16, kSbo);
-      const uint64_t b_desc0 = smem_desc_sw128(sbase + C::kOpOff + kABytes, kBLbo, kSbo);
+      const uint64_t b_desc0 = smem_desc_sw128(sbase + C::kOpOff + C::kAReal, kBLbo, kSbo);
       constexpr uint32_t kBStep = (2u * kSbo) >> 4;  // +2 n-groups per MMA K-step
       int s = 0;
       for (; s < ns; ++s) {
         const uint32_t slot = s % OS;
-        if (!mbar_wait(full_op(slot), (s / OS) & 1, abort_flag)) break;
-        NF4_PROBE(5, s);
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_op(slot), (s / OS) & 1, abort_flag))) break;
+        if (lane == 0) NF4_PROBE(5, s);
         // No tcgen05 fence here: the converters handed the operands to the
         // async proxy (fence.proxy.async before their arrive) and this thread
         // acquired the barrier; a fence per stage would keep the MMAs of
         // consecutive stages from overlapping.
-        const uint64_t off = static_cast<uint64_t>((slot * kOpBytes) >> 4);
+        const uint64_t off = static_cast<uint64_t>((slot * C::kOpBytes) >> 4);
         const uint64_t a = a_desc0 + off, b = b_desc0 + off;
-        // A: +32 bytes along the swizzled 128-byte row; B: +2 n-groups (2 KB).
-        tc_mma_f16(tmem_base, a, b, idesc, s != 0 ? 1u : 0u);
-        tc_mma_f16(tmem_base, a + 2u, b + kBStep, idesc, 1u);
-        tc_mma_f16(tmem_base, a + 4u, b + 2u * kBStep, idesc, 1u);
-        tc_mma_f16(tmem_base, a + 6u, b + 3u * kBStep, idesc, 1u);
-        tc_commit(empty_op(slot));
-        NF4_PROBE(6, s);
+        if (elect_one()) {
+          // A: +32 bytes along the swizzled 128-byte row; B: +2 n-groups (2 KB).
+          tc_mma_f16(tmem_base, a, b, idesc, s != 0 ? 1u : 0u);
+          tc_mma_f16(tmem_base, a + 2u, b + kBStep, idesc, 1u);
+          tc_mma_f16(tmem_base, a + 4u, b + 2u * kBStep, idesc, 1u);
+          tc_mma_f16(tmem_base, a + 6u, b + 3u * kBStep, idesc, 1u);
+          tc_commit(empty_op(slot));
+        }
+        __syncwarp();
+        if (lane == 0) NF4_PROBE(6, s);
       }
       if (s > 0) {
         // Also after giving up: no MMA may still run when TMEM is released.
-        tc_commit(acc_full);
+        if (elect_one()) tc_commit(acc_full);
+        __syncwarp();
         mbar_wait(acc_full, 0, nullptr);
         // The commits into the last operand slots are not waited for by anyone
         // else: they must have arrived before the CTA exits.
-        for (int i = (s > OS ? s - OS : 0); i < s; ++i)
-          mbar_wait(empty_op(i % OS), (i / OS) & 1, nullptr);
-      } else {
+        if (lane == 0)
+          for (int i = (s > OS ? s - OS : 0); i < s; ++i)
+            mbar_wait(empty_op(i % OS), (i / OS) & 1, nullptr);
+      } else if (lane == 0) {
         mbar_arrive(acc_full);  // nothing was issued (empty slice, or gave up at once)
       }
     }
@@ -286,9 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
     constexpr int kGoUnits = MP * 8;               // (row m, 8 n) units of grad_out per stage
     constexpr int kGoIters = (kGoUnits + 255) / 256;
 
-    // Block scales are loaded four group turns (eight stages) before their use.
+    // Block scales come with the raw stage (scale_tma), or are loaded four
+    // group turns (eight stages) before their use.
+    const bool stma = d.scale_tma != 0;
     auto scale_of = [&](int st) {
-      return st < ns ? block_scale(d, n_begin + st * SN + bn, kt * (SK / 64) + bj) : 0.0f;
+      return !stma && st < ns ? block_scale(d, n_begin + st * SN + bn, kt * (SK / 64) + bj) : 0.0f;
     };
     float sc0 = scale_of(group), sc1 = scale_of(group + kConvGroups);
     float sc2 = scale_of(group + 2 * kConvGroups), sc3 = scale_of(group + 3 * kConvGroups);
@@ -312,6 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       // NF4 block j of row n: 32 bytes, chunks 2j and 2j+1 of the 128-byte row.
       const uint4 q0 = lds128(raw + q_off + (((2u * bj) ^ bswz) << 4));
       const uint4 q1 = lds128(raw + q_off + (((2u * bj + 1u) ^ bswz) << 4));
+      const float scale_v =
+          stma ? __uint_as_float(lds32(raw + C::kScaleOff + bn * 16 + bj * 4)) : scale;
       uint4 g[kGoIters][2];
 #pragma unroll
       for (int u = 0; u < kGoIters; ++u) {
@@ -340,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
         break;
       }
       if (lead) NF4_PROBE(3, s);
-      const uint32_t a_op = sbase + C::kOpOff + oslot * kOpBytes;
-      const uint32_t b_op = a_op + kABytes;
+      const uint32_t a_op = sbase + C::kOpOff + oslot * C::kOpBytes;
+      const uint32_t b_op = a_op + C::kAReal;
       // grad_out -> f16 A operand (K-major, 128B swizzle: chunk c8 of row m at c8 ^ (m % 8)).
 #pragma unroll
       for (int u = 0; u < kGoIters; ++u) {
@@ -368,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       // One NF4 block (row n = bn, k = 64*bj .. +63) -> one 128-byte swizzle row
       // of the MN-major B operand.
       {
-        const BlockTable tb = make_block_table(scale);
+        const BlockTable tb = make_block_table(scale_v);
         const uint32_t dst = b_op + bj * kBLbo + (bn >> 3) * kSbo + bswz * 128;
         const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
