@@ -399,6 +399,15 @@ __global__ void __launch_bounds__(L::kThreads, 1)
   const int lane = threadIdx.x & 31;
   NF4_TRACE_INIT;
   if (threadIdx.x == 0) NF4_PROBE(44, 0);
+  // Start the first reads of the problem's descriptor (tensor maps and the
+  // fields every role reads) now, so that their latency overlaps the set-up
+  // below instead of delaying each role's first stage.
+  if (count == 1 && threadIdx.x == 32) {
+    tma_prefetch_desc(&descs[0].tm_go);
+    tma_prefetch_desc(&descs[0].tm_nf4);
+    tma_prefetch_desc(&descs[0].tm_out);
+    if (descs[0].scale_tma) tma_prefetch_desc(&descs[0].tm_scales);
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
@@ -453,10 +462,6 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     // that arrival is pending.
     const int my_slot = lane / L::kBoxes;
     const int box = L::kPreA ? 2 + (lane & 1) : (lane & 3);
-    if (lane == 0 && count == 1) {
-      tma_prefetch_desc(&descs[0].tm_go);
-      tma_prefetch_desc(&descs[0].tm_nf4);
-    }
     uint32_t it = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -646,6 +651,9 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     // Lane `slot` issues the copies of that slot (a thread's bulk copies are
     // served one after another); lane 0 alone waits.
     const uint32_t full_a_leader0 = mapa_shared(full_a(0), 0);
+    // The A operand is the pre-pass's output: wait for that kernel (a launch
+    // that may overlap it) before the first copy.
+    griddep_wait();
     uint32_t it = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -827,6 +835,8 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     // later stages of a split tile are left as a partial sum in this pair's
     // workspace slot, followed by a count-up of the pair's flag.
     const uint32_t tmem_empty_leader0 = mapa_shared(tmem_empty(0), 0);
+    // The split flags are zeroed by the preceding pre-pass kernel.
+    if constexpr (L::kPreA) griddep_wait();
     constexpr int kEpiCols = L::kEpiCols;
     constexpr int kEpiBufBytes = L::kEpiBufBytes;
     constexpr int kPieces = kEpiCols / 4;  // 16-byte pieces per staged row
@@ -1055,6 +1065,9 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const void* __restrict__ sr
                                                      uint16_t* __restrict__ dst, int M, int N,
                                                      int ldh, unsigned int* __restrict__ flags,
                                                      int nflags) {
+  // The GEMM that follows may be scheduled now (it waits for this kernel's
+  // results before it reads them).
+  griddep_launch_dependents();
   // The split-tile flags of the GEMM that follows start from zero.
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < nflags; i += blockDim.x) flags[i] = 0u;
@@ -1271,9 +1284,12 @@ static int max_clusters(int* out) {
 
 // Launch over `total_tiles` tiles; sk == nullptr: all tiles whole, else the
 // split described by *sk (planned for this device's pair count).
+// pdl: the launch directly follows to_f16_kernel on the stream and may start
+// while that kernel finishes (programmatic stream serialization).
 template <class L>
 static int launch_layout(const ProblemDesc& single, const ProblemDesc* batch, int count,
-                         int total_tiles, const SkArgs* sk_in, cudaStream_t stream) {
+                         int total_tiles, const SkArgs* sk_in, cudaStream_t stream,
+                         bool pdl = false) {
   int maxc = 0;
   const int rc = max_clusters<L>(&maxc);
   if (rc != NF4_OK) return rc;
@@ -1286,17 +1302,19 @@ static int launch_layout(const ProblemDesc& single, const ProblemDesc* batch, in
     clusters = maxc;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   cfg.blockDim = dim3(L::kThreads, 1, 1);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, bwd_a_kernel<L>, single, batch, count, sk) != cudaSuccess)
     return NF4_ERR_CUDA;
   return launch_status();
@@ -1658,7 +1676,8 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
     if (rc != NF4_OK) return rc;
   }
   return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles),
-                                   sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream));
+                                   sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream),
+                                   /*pdl=*/!f16_in);
 }
 
 extern "C" size_t nf4_backward_a_batched_workspace(int count) {

@@ -170,6 +170,20 @@ __device__ __forceinline__ bool flag_wait_global_ge(const unsigned int* p, unsig
   }
 }
 
+// Programmatic dependent launch: a kernel launched right after another with
+// programmatic stream serialization may start before that one ends.
+// griddep_wait() returns once the preceding kernel has completed and its memory
+// operations are visible (at once when there is no such kernel);
+// griddep_launch_dependents() lets the dependent kernel be scheduled once every
+// block of this kernel has executed it or exited.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
