@@ -51,6 +51,8 @@ SIGNATURES = {
     "nf4_split_plan": (_i, [_i, _i, _i, C.POINTER(_i), C.POINTER(_i)]),
     "nf4_split_item": (_i, [_i, _i, _i, _i, _i, C.POINTER(_i)]),
     "nf4_backward_a_batched_workspace": (_sz, [_i]),
+    "nf4_backward_a_batched_ws_bytes": (_sz, [C.POINTER(Nf4Problem), _i]),
+    "nf4_backward_a_batched_ws": (_i, [C.POINTER(Nf4Problem), _i, _vp, _sz, _vp]),
     "nf4_backward_a_batched": (_i, [C.POINTER(Nf4Problem), _i, _vp, _sz, _vp]),
     "nf4_check_error": (_i, [_vp]),
     "nf4_check_error_site": (_i, [_vp, C.POINTER(C.c_uint)]),
@@ -250,6 +252,55 @@ def backward_a_batched(items, workspace: torch.Tensor | None = None):
         workspace = batched_workspace(len(items), items[0][0].device if items else None)
     _check(lib().nf4_backward_a_batched(arr, len(items), _ptr(workspace), workspace.numel(),
                                         _stream()), "nf4_backward_a_batched")
+    return outs
+
+
+def _problem_array(items, make_out: bool):
+    arr = (Nf4Problem * max(len(items), 1))()
+    outs = []
+    for i, (go, w, out) in enumerate(items):
+        _require_cuda_contig("grad_out", go)
+        M, N = go.shape
+        if out is None:
+            if not make_out:
+                raise ValueError("every output must be given")
+            out = torch.empty((M, w.K), dtype=torch.float32, device=go.device)
+        _require_cuda_contig("out", out)
+        outs.append(out)
+        arr[i] = Nf4Problem(go.data_ptr(), _dtype_code(go), w.scales.data_ptr(), w.data.data_ptr(),
+                            out.data_ptr(), M, N, w.K)
+    return arr, outs
+
+
+def batched_ws_bytes(items) -> int:
+    """Bytes of workspace :func:`backward_a_batched_ws` needs for ``items``
+    (only the grad_out tensors' shapes and types and the weights' K matter)."""
+    items = list(items)
+    arr = (Nf4Problem * max(len(items), 1))()
+    for i, (go, w, _) in enumerate(items):
+        M, N = go.shape
+        arr[i] = Nf4Problem(0, _dtype_code(go), 0, 0, 0, M, N, w.K)
+    return int(lib().nf4_backward_a_batched_ws_bytes(arr, len(items)))
+
+
+def batched_ws_workspace(items, device=None) -> torch.Tensor:
+    """Workspace for :func:`backward_a_batched_ws` (descriptors and f16 copies)."""
+    items = list(items)
+    dev = device or (items[0][0].device if items else "cuda")
+    return torch.empty(max(batched_ws_bytes(items), 256), dtype=torch.uint8, device=dev)
+
+
+def backward_a_batched_ws(items, workspace: torch.Tensor | None = None):
+    """Grouped launch of the pre-converted path (``nf4_backward_a_batched_ws``):
+    f16 copies of every fp32/bf16 grad_out, then one pair-kernel launch over all
+    problems.  ``items`` as for :func:`backward_a_batched`; returns the outputs."""
+    items = list(items)
+    arr, outs = _problem_array(items, make_out=True)
+    if workspace is None:
+        workspace = batched_ws_workspace(items)
+    _require_cuda_contig("workspace", workspace)
+    _check(lib().nf4_backward_a_batched_ws(arr, len(items), _ptr(workspace), workspace.numel(),
+                                           _stream()), "nf4_backward_a_batched_ws")
     return outs
 
 

@@ -1061,6 +1061,34 @@ __device__ __forceinline__ uint4 bf16x8_to_f16(const uint4 w) {
   return h;
 }
 
+// One 16-element group (row m, columns c .. c+15) of the copy.
+__device__ __forceinline__ void convert_group(const void* __restrict__ src, int f32,
+                                              uint16_t* __restrict__ dst, int N, int ldh,
+                                              int64_t m, int c) {
+  uint16_t* out = dst + m * ldh + c;
+  const bool second = c + 8 < ldh;  // the group's second 8 columns exist in the copy
+  if (f32) {
+    // N % 4 == 0: each 4-column piece is either inside the row or past N.
+    const float4* row = reinterpret_cast<const float4*>(static_cast<const float*>(src) + m * N);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int q = c >> 2;
+    const float4 a0 = c < N ? __ldcs(row + q) : z;
+    const float4 a1 = c + 4 < N ? __ldcs(row + q + 1) : z;
+    const float4 a2 = c + 8 < N ? __ldcs(row + q + 2) : z;
+    const float4 a3 = c + 12 < N ? __ldcs(row + q + 3) : z;
+    *reinterpret_cast<uint4*>(out) = f32x8_to_f16(a0, a1);
+    if (second) *reinterpret_cast<uint4*>(out + 8) = f32x8_to_f16(a2, a3);
+  } else {
+    // N % 8 == 0 and ldh == N: whole 8-column pieces only.
+    const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + m * N);
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const uint4 w0 = __ldcs(row + (c >> 3));
+    const uint4 w1 = second ? __ldcs(row + (c >> 3) + 1) : z;
+    *reinterpret_cast<uint4*>(out) = bf16x8_to_f16(w0);
+    if (second) *reinterpret_cast<uint4*>(out + 8) = bf16x8_to_f16(w1);
+  }
+}
+
 __global__ void __launch_bounds__(256) to_f16_kernel(const void* __restrict__ src, int f32,
                                                      uint16_t* __restrict__ dst, int M, int N,
                                                      int ldh, unsigned int* __restrict__ flags,
@@ -1076,29 +1104,40 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const void* __restrict__ sr
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t m = i / groups;
-    const int c = static_cast<int>(i - m * groups) << 4;
-    uint16_t* out = dst + m * ldh + c;
-    const bool second = c + 8 < ldh;  // the group's second 8 columns exist in the copy
-    if (f32) {
-      // N % 4 == 0: each 4-column piece is either inside the row or past N.
-      const float4* row = reinterpret_cast<const float4*>(static_cast<const float*>(src) + m * N);
-      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int q = c >> 2;
-      const float4 a0 = c < N ? __ldcs(row + q) : z;
-      const float4 a1 = c + 4 < N ? __ldcs(row + q + 1) : z;
-      const float4 a2 = c + 8 < N ? __ldcs(row + q + 2) : z;
-      const float4 a3 = c + 12 < N ? __ldcs(row + q + 3) : z;
-      *reinterpret_cast<uint4*>(out) = f32x8_to_f16(a0, a1);
-      if (second) *reinterpret_cast<uint4*>(out + 8) = f32x8_to_f16(a2, a3);
-    } else {
-      // N % 8 == 0 and ldh == N: whole 8-column pieces only.
-      const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + m * N);
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      const uint4 w0 = __ldcs(row + (c >> 3));
-      const uint4 w1 = second ? __ldcs(row + (c >> 3) + 1) : z;
-      *reinterpret_cast<uint4*>(out) = bf16x8_to_f16(w0);
-      if (second) *reinterpret_cast<uint4*>(out + 8) = bf16x8_to_f16(w1);
+    convert_group(src, f32, dst, N, ldh, m, static_cast<int>(i - m * groups) << 4);
+  }
+}
+
+// The same pass over several problems of a grouped launch: job j owns the
+// 16-element groups [begin[j], begin[j+1]) of the concatenated list.
+constexpr int kF16JobsPerLaunch = 64;
+struct F16Job {
+  const void* src;
+  uint16_t* dst;
+  int f32, N, ldh, groups_per_row;
+  int64_t begin;
+};
+struct F16Jobs {
+  F16Job job[kF16JobsPerLaunch];
+  int64_t end;  // total groups
+  int n;
+};
+static_assert(sizeof(F16Jobs) <= 4096, "kernel parameter size");
+
+__global__ void __launch_bounds__(256) to_f16_group_kernel(const __grid_constant__ F16Jobs jobs) {
+  griddep_launch_dependents();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < jobs.end;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int lo = 0, hi = jobs.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (jobs.job[mid].begin <= i) lo = mid; else hi = mid - 1;
     }
+    const F16Job& j = jobs.job[lo];
+    const int64_t local = i - j.begin;
+    const int64_t m = local / j.groups_per_row;
+    convert_group(j.src, j.f32, j.dst, j.N, j.ldh, m,
+                  static_cast<int>(local - m * j.groups_per_row) << 4);
   }
 }
 
@@ -1750,6 +1789,140 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
   for (const ProblemDesc& d : descs) all_bf16 = all_bf16 && d.dtype == NF4_BF16;
   return launch(unused, static_cast<const ProblemDesc*>(workspace), static_cast<int>(descs.size()),
                 static_cast<int>(total), all_bf16, st);
+}
+
+// ------------------------------------------------------------------ grouped, pre-converted
+namespace nf4 {
+// Problems of a grouped pre-converted launch whose grad_out needs the f16 copy
+// (fp32 or bf16, M above the few-token limit or not), in problem order.
+static size_t group_copy_bytes(const nf4_problem* problems, int count) {
+  size_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    if (p.M > 0 && p.N > 0 && p.go_dtype != NF4_F16) total += round256(f16_bytes(p.M, p.N));
+  }
+  return total;
+}
+
+static int launch_f16_jobs(const F16Jobs& jobs, cudaStream_t stream) {
+  int sms = 0;
+  const int rc = sm_count(&sms);
+  if (rc != NF4_OK) return rc;
+  const int64_t blocks = std::min<int64_t>((jobs.end + 255) / 256, static_cast<int64_t>(sms) * 64);
+  to_f16_group_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, stream>>>(jobs);
+  return cudaGetLastError() == cudaSuccess ? NF4_OK : NF4_ERR_CUDA;
+}
+}  // namespace nf4
+
+extern "C" size_t nf4_backward_a_batched_ws_bytes(const nf4_problem* problems, int count) {
+  if (count <= 0 || problems == nullptr) return 0;
+  return round256(sizeof(ProblemDesc) * static_cast<size_t>(count)) +
+         group_copy_bytes(problems, count);
+}
+
+extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (count < 0 || (count > 0 && problems == nullptr)) return NF4_ERR_INVALID;
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    const int rc = check_problem(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
+    if (rc != NF4_OK) return rc;
+  }
+  cudaStream_t st = as_stream(stream);
+  const size_t desc_bytes = round256(sizeof(ProblemDesc) * static_cast<size_t>(count));
+  // Nothing is enqueued before the workspace is known to be big enough.
+  bool any_gemm = false;
+  const int small_max = small_m::g_max_m.load();
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    if (p.M > 0 && p.N > 0 && (p.M > small_max || p.go_dtype == NF4_F16)) any_gemm = true;
+  }
+  if (any_gemm && (workspace == nullptr || !aligned(workspace, 256) ||
+                   workspace_bytes < desc_bytes + group_copy_bytes(problems, count)))
+    return NF4_ERR_WORKSPACE;
+  std::vector<ProblemDesc> descs;
+  descs.reserve(count);
+  std::vector<F16Job> jobs;
+  uint8_t* copy = static_cast<uint8_t*>(workspace) + desc_bytes;
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    if (p.M == 0) continue;
+    if (p.N == 0) {
+      if (cudaMemsetAsync(p.grad_A, 0, sizeof(float) * static_cast<size_t>(p.M) * p.K, st) !=
+          cudaSuccess)
+        return NF4_ERR_CUDA;
+      continue;
+    }
+    const bool f16_in = p.go_dtype == NF4_F16;
+    uint16_t* dst = nullptr;
+    if (!f16_in) {
+      dst = reinterpret_cast<uint16_t*>(copy);
+      copy += round256(f16_bytes(p.M, p.N));
+    }
+    if (!f16_in && p.M <= small_max) {
+      // Few tokens: the problem's own launch of the few-token kernel.
+      const int rc = small_m::run(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N,
+                                  p.K, st);
+      if (rc != NF4_OK) return rc;
+      continue;
+    }
+    descs.emplace_back();
+    const uint16_t* a = f16_in ? static_cast<const uint16_t*>(p.grad_out) : dst;
+    const int rc = fill_desc_pre(&descs.back(), a, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
+    if (rc != NF4_OK) return rc;
+    if (!f16_in) {
+      F16Job j;
+      j.src = p.grad_out;
+      j.dst = dst;
+      j.f32 = p.go_dtype == NF4_F32 ? 1 : 0;
+      j.N = p.N;
+      j.ldh = f16_pitch(p.N);
+      j.groups_per_row = (j.ldh + 15) >> 4;
+      j.begin = static_cast<int64_t>(p.M) * j.groups_per_row;  // size for now
+      jobs.push_back(j);
+    }
+  }
+  if (descs.empty()) return NF4_OK;
+  // Longest tiles first (stable), as the grouped entry point orders them.
+  std::stable_sort(descs.begin(), descs.end(), [](const ProblemDesc& a, const ProblemDesc& b) {
+    return a.n_stages > b.n_stages;
+  });
+  int64_t total = 0;
+  for (ProblemDesc& d : descs) {
+    d.tile_begin = static_cast<int>(total);
+    total += static_cast<int64_t>(d.tiles_m) * d.tiles_k;
+    if (total > INT_MAX) return NF4_ERR_INVALID;
+  }
+  ProblemDesc* ws = static_cast<ProblemDesc*>(workspace);
+  for (size_t i = 0; i < descs.size(); i += kDescsPerUpload) {
+    const int n = static_cast<int>(std::min<size_t>(kDescsPerUpload, descs.size() - i));
+    DescChunk chunk;
+    std::memset(&chunk, 0, sizeof(chunk));
+    std::memcpy(chunk.d, descs.data() + i, sizeof(ProblemDesc) * n);
+    upload_descs_kernel<<<1, 256, 0, st>>>(chunk, ws + i, n);
+    if (cudaGetLastError() != cudaSuccess) return NF4_ERR_CUDA;
+  }
+  // The f16 copies, kF16JobsPerLaunch problems per launch; the GEMM follows
+  // the last of them as a programmatic dependent.
+  for (size_t i = 0; i < jobs.size(); i += kF16JobsPerLaunch) {
+    F16Jobs batch;
+    std::memset(&batch, 0, sizeof(batch));
+    batch.n = static_cast<int>(std::min<size_t>(kF16JobsPerLaunch, jobs.size() - i));
+    int64_t at = 0;
+    for (int j = 0; j < batch.n; ++j) {
+      batch.job[j] = jobs[i + j];
+      const int64_t size = batch.job[j].begin;
+      batch.job[j].begin = at;
+      at += size;
+    }
+    batch.end = at;
+    const int rc = launch_f16_jobs(batch, st);
+    if (rc != NF4_OK) return rc;
+  }
+  ProblemDesc unused;
+  std::memset(&unused, 0, sizeof(unused));
+  return launch_layout<LayoutPreA>(unused, ws, static_cast<int>(descs.size()),
+                                   static_cast<int>(total), nullptr, st, /*pdl=*/!jobs.empty());
 }
 
 #ifdef NF4_PROGRESS

@@ -143,7 +143,8 @@ def make_input_sets(probs, copies, dev, entry="plain"):
             out = torch.empty((p.M, p.K), dtype=torch.float32, device=dev)
             items.append((go_t, w, out))
         if len(items) > 1:
-            ws = nb.batched_workspace(len(items), dev)
+            ws = (nb.batched_ws_workspace(items, dev) if entry == "ws"
+                  else nb.batched_workspace(len(items), dev))
         elif entry == "ws":
             ws = nb.ws_workspace(probs[0].M, probs[0].N, dev)
         else:
@@ -153,9 +154,13 @@ def make_input_sets(probs, copies, dev, entry="plain"):
     return sets, base_go
 
 
+RUN_ENTRY = {"entry": "plain"}  # the entry point run_step uses (set by bench_ours)
+
+
 def run_step(items, ws):
-    """One step through the public API.  A single problem with a workspace runs
-    nf4_backward_a_ws (f16 pre-pass, then the GEMM), without one nf4_backward_a_ex."""
+    """One step through the public API.  With the ws entry a single problem runs
+    nf4_backward_a_ws and a group nf4_backward_a_batched_ws (f16 pre-passes, then
+    the GEMM); otherwise nf4_backward_a_ex / nf4_backward_a_batched."""
     import backward_gemm_gb300 as nb
 
     if len(items) == 1:
@@ -164,6 +169,8 @@ def run_step(items, ws):
             nb.backward_a(go, w, out=out)
         else:
             nb.backward_a_ws(go, w, ws, out=out)
+    elif RUN_ENTRY["entry"] == "ws":
+        nb.backward_a_batched_ws(items, ws)
     else:
         nb.backward_a_batched(items, ws)
 
@@ -182,7 +189,8 @@ def bench_ours(args, rank, world, dev):
     probs = workloads()[args.workload]
     flops = sum(p.flops for p in probs)
     alg_bytes = sum(p.algorithmic_bytes for p in probs)
-    entry = args.entry if len(probs) == 1 and probs[0].M > SMALL_M_MAX else "plain"
+    entry = args.entry if len(probs) > 1 or probs[0].M > SMALL_M_MAX else "plain"
+    RUN_ENTRY["entry"] = entry
     per_set = sum(p.go_bytes + 4 * p.M * p.K + p.K * p.N // 2
                   + (2 * p.M * p.N if entry == "ws" else 0) for p in probs)
     copies = max(2, min(16, -(-2 * L2_BYTES // per_set)))
@@ -238,7 +246,7 @@ def bench_ours(args, rank, world, dev):
     # the steps left in each set's workspace (the f16 grad_out entry skips the
     # pre-pass), over the same rotating sets.
     kernel_ms = None
-    if entry == "ws" and probs[0].N % 8 == 0:
+    if entry == "ws" and len(probs) == 1 and probs[0].N % 8 == 0:
         kernel_ms = time_gemm_only(sets, probs[0], stream, dev, K)
 
     peaks, peak_kind = load_peaks()
@@ -273,7 +281,8 @@ def bench_ours(args, rank, world, dev):
                    "gflop_per_step": flops / 1e9, "algorithmic_mb_per_step": alg_bytes / 1e6,
                    "l2": f"rotating {copies} input sets, {copies * per_set / 2**20:.0f} MiB > L2",
                    "timing": f"CUDA graph of {copies} steps, CUDA events",
-                   "entry": "nf4_backward_a_ws" if entry == "ws" else (
+                   "entry": ("nf4_backward_a_ws" if len(probs) == 1 else "nf4_backward_a_batched_ws")
+                            if entry == "ws" else (
                        "nf4_backward_a_ex" if len(probs) == 1 else "nf4_backward_a_batched"),
                    "parallelism": f"dp{world} (M-sharded replicas, no collective)"},
         "e2e": e2e,
@@ -288,6 +297,7 @@ def bench_ours(args, rank, world, dev):
 
 SMALL_M_MAX = 64      # the library's default few-token limit (nf4_set_small_m_max)
 DESCS_PER_UPLOAD = 48  # descriptors per upload kernel of a grouped launch
+F16_JOBS_PER_LAUNCH = 64  # problems per grouped f16 pass (nf4_backward_a_batched_ws)
 
 
 def time_gemm_only(sets, p, stream, dev, steps):
@@ -326,7 +336,7 @@ def kernel_names(probs, entry="plain") -> str:
     if any(p.M > SMALL_M_MAX for p in probs):
         names.append("bwd_a_kernel")
         if entry == "ws":
-            names.insert(0, "to_f16_kernel")
+            names.insert(0, "to_f16_kernel" if len(probs) == 1 else "to_f16_group_kernel")
     return " + ".join(names)
 
 
@@ -339,7 +349,11 @@ def launches_per_step(probs, entry="plain") -> int:
         return 2 if entry == "ws" and probs[0].M > SMALL_M_MAX else 1
     few = sum(1 for p in probs if p.M <= SMALL_M_MAX)
     rest = len(probs) - few
-    return few + ((-(-rest // DESCS_PER_UPLOAD) + 1) if rest else 0)
+    if not rest:
+        return few
+    # grouped ws entry: + the f16 passes, F16_JOBS_PER_LAUNCH problems each
+    passes = -(-rest // F16_JOBS_PER_LAUNCH) if entry == "ws" else 0
+    return few + -(-rest // DESCS_PER_UPLOAD) + passes + 1
 
 
 def bench_e2e(args, probs, host_go, set0, stream, dev, flops, world):

@@ -191,7 +191,7 @@ int nf4_small_m_split(int N, int K, int sms, int cta_slots, int* per_out);
 /* One projection of a grouped launch. */
 typedef struct nf4_problem {
   const void* grad_out; /* [M][N], type go_dtype */
-  int go_dtype;         /* NF4_F32 or NF4_BF16 (NF4_F16: NF4_ERR_INVALID) */
+  int go_dtype;         /* NF4_F32 or NF4_BF16; NF4_F16 in nf4_backward_a_batched_ws only */
   const float* scales;  /* [N][K/64] */
   const uint8_t* data;  /* [N][K/2] */
   float* grad_A;        /* [M][K], overwritten */
@@ -219,6 +219,33 @@ size_t nf4_backward_a_batched_workspace(int count);
  */
 int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace nf4_backward_a_batched_ws needs for these problems: the
+ * descriptors (the same as nf4_backward_a_batched's, rounded up to 256) plus
+ * an f16 copy of every fp32 or bf16 grad_out (2 * M * ((N + 7) & ~7) bytes
+ * each, rounded up to 256).  `problems` is a host array; 0 for count <= 0.
+ */
+size_t nf4_backward_a_batched_ws_bytes(const nf4_problem* problems, int count);
+
+/*
+ * The grouped launch of the pre-converted path (see nf4_backward_a_ws): every
+ * fp32 or bf16 grad_out is rounded to f16 into the workspace by grouped
+ * streaming passes, then one persistent launch of the pair kernel with
+ * TMA-loaded A operands runs all problems' tiles (longest first), as a
+ * programmatic dependent of the last pass.  NF4_F16 grad_out is accepted and
+ * read in place.  Few-token problems (M at most nf4_set_small_m_max, fp32 or
+ * bf16) run as their own launches of the few-token kernel, as in
+ * nf4_backward_a_batched.  Each problem's grad_A equals, bit for bit, what
+ * nf4_backward_a_ws gives for it without a split (tiles are never split
+ * here).  No counterpart on the pages.
+ *   workspace  caller-owned device memory, 256-byte aligned, at least
+ *              nf4_backward_a_batched_ws_bytes(problems, count) bytes; too
+ *              small, NULL or misaligned returns NF4_ERR_WORKSPACE and enqueues
+ *              nothing; must not be reused until the stream has run the call
+ */
+int nf4_backward_a_batched_ws(const nf4_problem* problems, int count, void* workspace,
+                              size_t workspace_bytes, void* stream);
 
 /*
  * Grouped backward-A that allocates nothing.  The pages have no counterpart of

@@ -518,3 +518,90 @@ def test_f16_grad_out_rejected_by_grouped_launch():
     go = torch.zeros((p.M, p.N), dtype=torch.float16, device="cuda")
     with pytest.raises(nb().Nf4Error):
         nb().backward_a_batched([(go, w, None)])
+
+
+# ---------------------------------------------------------------- grouped, pre-converted
+def test_batched_ws_matches_single_ws_and_oracle():
+    """nf4_backward_a_batched_ws: one f16 copy per fp32/bf16 problem, f16 input
+    read in place, few-token problems on their own kernel; every result equals
+    the single pre-converted call without a split (or the few-token call) bit
+    for bit, and the oracle within tolerance."""
+    probs = [Problem(300, 192, 640, F32, 1.0, 0.02, True, 61),
+             Problem(129, 256, 1536, BF16, 1e-2, 0.02, False, 62),
+             Problem(16, 1536, 1536, F32, 1e-2, 0.02, False, 63),     # few tokens
+             Problem(1000, 64, 256, F32, 1.0, 0.02, False, 64),
+             Problem(520, 196, 384, F32, 1.0, 0.02, True, 65)]        # f16 rows padded
+    items, gos, Bs = [], [], []
+    for p in probs:
+        go = make_grad_out(p)
+        B = make_weight(p)
+        items.append((to_device_go(go, p.go_dtype), nb().quantize(torch.from_numpy(B).cuda()), None))
+        gos.append(go)
+        Bs.append(B)
+    # One more problem given in f16 (read in place).
+    pf = Problem(400, 320, 512, F32, 1.0, 0.02, False, 66)
+    go16 = oracle.f32_to_f16(make_grad_out(pf))
+    Bf = make_weight(pf)
+    items.append((torch.from_numpy(go16.view(np.int16)).cuda().view(torch.float16),
+                  nb().quantize(torch.from_numpy(Bf).cuda()), None))
+    outs = nb().backward_a_batched_ws(items)
+    nb().check_error()
+    for p, go, B, (go_t, w, _), out in zip(probs, gos, Bs, items, outs):
+        single = nb().backward_a_ws(go_t, w, nb().ws_workspace(p.M, p.N, split=False))
+        assert torch.equal(out, single), p
+        data_o, scales_o = oracle.quantize(B)
+        ref, bound = oracle.backward_a(go, p.go_dtype, scales_o, data_o, p.K)
+        assert_close(out.cpu().numpy(), ref, bound, str(p))
+    go_t, w, _ = items[-1]
+    assert torch.equal(outs[-1], nb().backward_a(go_t, w))
+    data_o, scales_o = oracle.quantize(Bf)
+    bt = oracle.dequantize_f16(scales_o, data_o, pf.K, pf.N)
+    ref, bound = oracle.backward_a_rows(go16, bt, np.arange(pf.M, dtype=np.int32))
+    assert_close(outs[-1].cpu().numpy(), ref, bound, "f16 input")
+
+
+def test_batched_ws_full_step_one_layer_and_repeatable():
+    full = CONFIGS["full_step"][:7]
+    probs = [Problem(512, p.N, p.K, p.go_dtype, p.go_std, p.b_std, p.outliers, p.seed, p.name)
+             for p in full]
+    items, refs = [], []
+    for p in probs:
+        go = make_grad_out(p)
+        B = make_weight(p)
+        items.append((to_device_go(go, p.go_dtype), nb().quantize(torch.from_numpy(B).cuda()), None))
+        data_o, scales_o = oracle.quantize(B)
+        go16 = oracle.round_operand(go, p.go_dtype)
+        bt = oracle.dequantize_f16(scales_o, data_o, p.K, p.N)
+        rows = sample_rows(p.M, 6, p.seed)
+        refs.append((rows,) + oracle.backward_a_rows(go16, bt, rows))
+    ws = nb().batched_ws_workspace(items)
+    outs = nb().backward_a_batched_ws(items, ws)
+    again = nb().backward_a_batched_ws([(g, w, None) for g, w, _ in items], ws)
+    nb().check_error()
+    for p, out, out2, (rows, ref, bound) in zip(probs, outs, again, refs):
+        assert_close(out.cpu().numpy()[rows], ref, bound, p.name)
+        assert torch.equal(out, out2)
+
+
+def test_batched_ws_rejects_small_workspace_without_launching():
+    import ctypes as C
+
+    p = Problem(300, 192, 640, F32, 1.0, 0.02, False, 67)
+    go = to_device_go(make_grad_out(p), F32)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    out = torch.full((p.M, p.K), 3.0, device="cuda")
+    items = [(go, w, out)]
+    need = nb().batched_ws_bytes(items)
+    assert need >= 2 * p.M * p.N
+    arr = (nb().Nf4Problem * 1)()
+    arr[0] = nb().Nf4Problem(go.data_ptr(), F32, w.scales.data_ptr(), w.data.data_ptr(),
+                             out.data_ptr(), p.M, p.N, p.K)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    L = nb().lib()
+    assert L.nf4_backward_a_batched_ws(arr, 1, C.c_void_p(ws.data_ptr()), need - 1, None) == \
+        nb().NF4_ERR_WORKSPACE
+    assert L.nf4_backward_a_batched_ws(arr, 1, None, 0, None) == nb().NF4_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((out == 3.0).all())
+    assert L.nf4_backward_a_batched_ws(arr, 1, C.c_void_p(ws.data_ptr()), need, None) == nb().NF4_OK
+    nb().check_error()
