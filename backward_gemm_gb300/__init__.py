@@ -48,6 +48,8 @@ SIGNATURES = {
     "nf4_backward_a_ex": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "nf4_backward_a_ws_bytes": (_sz, [_i, _i]),
     "nf4_backward_a_ws": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+    "nf4_tile_rows": (_i, [_i, _i, _i, _i, _i]),
+    "nf4_set_tile_rows": (_i, [_i]),
     "nf4_split_plan": (_i, [_i, _i, _i, C.POINTER(_i), C.POINTER(_i)]),
     "nf4_split_item": (_i, [_i, _i, _i, _i, _i, C.POINTER(_i)]),
     "nf4_backward_a_batched_workspace": (_sz, [_i]),
@@ -176,6 +178,33 @@ def ws_workspace(M: int, N: int, device=None, split: bool = True) -> torch.Tenso
     else:
         n = 2 * M * ((N + 7) // 8 * 8)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def tile_rows(M: int, N: int, K: int, pairs: int, can_split: bool = True) -> int:
+    """Tokens per pair tile (256 or 512) the pre-converted path picks (host only)."""
+    r = int(lib().nf4_tile_rows(M, N, K, pairs, 1 if can_split else 0))
+    if r < 0:
+        raise ValueError("invalid tile-rows arguments")
+    return r
+
+
+class tile_rows_forced:
+    """Context manager forcing the pre-converted kernel's tile (256 or 512
+    tokens; 0 = automatic) within the block."""
+
+    def __init__(self, rows: int):
+        self.rows = rows
+
+    def __enter__(self):
+        prev = int(lib().nf4_set_tile_rows(int(self.rows)))
+        if prev < 0:
+            raise ValueError("tile rows must be 0, 256 or 512")
+        self.prev = prev
+        return self
+
+    def __exit__(self, *exc):
+        lib().nf4_set_tile_rows(self.prev)
+        return False
 
 
 def split_plan(tiles: int, stages: int, pairs: int) -> tuple[int, int]:

@@ -95,9 +95,18 @@ constexpr uint32_t kTmemCols = 2 * BK;
 // separate pass, and a TMA copy writes each stage's A operand straight into a
 // ring of RA A slots (no raw grad_out, no converter work on A); the operand
 // slots then hold B^T only.
-template <int RS, int OS, int GOB, int RA = 0, int EC = 16>
+template <int RS, int OS, int GOB, int RA = 0, int EC = 16, int MB = 1>
 struct Layout {
   static constexpr bool kPreA = RA > 0;
+  // M-blocks of 256 tokens per pair tile.  MB = 2 (pre-converted variant
+  // only): each stage's dequantised B^T serves two M = 256 MMA blocks, which
+  // halves the dequantisation per MMA; the two accumulators fill the 512 TMEM
+  // columns, so they are single-buffered (the epilogue of a tile does not
+  // overlap the next tile's MMAs).
+  static constexpr int kMBlocks = MB;
+  static constexpr int kRowsPerTile = 256 * MB;
+  static constexpr int kAccBufs = 2 / MB;
+  static constexpr int kASlotBytes = MB * kABytes;
   // Epilogue chunk: EC fp32 columns of a warp's 32 rows per TMEM load and per
   // TMA store (EC = 16: 64-byte rows, 64-byte swizzle; 32: 128-byte rows,
   // 128-byte swizzle; fewer, larger chunks cost less per column).
@@ -113,7 +122,7 @@ struct Layout {
   static constexpr int kBInOp = kPreA ? 0 : kABytes;  // offset of B^T in an operand slot
   static constexpr int kRawOff = 0;
   static constexpr int kAOff = kRawOff + RS * kRawBytes;
-  static constexpr int kOpOff = kAOff + RA * kABytes;
+  static constexpr int kOpOff = kAOff + RA * MB * kABytes;
   static constexpr int kEpiOff = kOpOff + OS * kOpSlotBytes;
   static constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufs * kEpiBufBytes;
   // ... + one barrier per epilogue warp for reading other pairs' partial sums
@@ -142,10 +151,12 @@ struct Layout {
   // operand slots, whose release the groups also wait for by parity.
   static_assert(RS % kConvGroups == 0 && OS % kConvGroups == 0,
                 "ring slots are not shared between converter groups");
+  static_assert(MB == 1 || (MB == 2 && kPreA), "two M-blocks only with the pre-converted A");
 };
 using LayoutF32 = Layout<2, 4, 2 * kGoBoxBytes>;  // any fp32 grad_out in the launch
 using LayoutBF16 = Layout<2, 4, kGoBoxBytes>;     // bf16 grad_out only
 using LayoutPreA = Layout<6, 4, 0, 6, 32>;        // grad_out pre-converted to f16
+using LayoutPreA2 = Layout<4, 4, 0, 3, 32, 2>;    // pre-converted, 512-token pair tiles
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
 // 8 rows n per 1024-byte atom; atoms along k are kBLbo apart, atoms along n 1 KB.
@@ -352,6 +363,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
   // A-ring depth, 1 (never used) in the variants without an A ring so that the
   // slot arithmetic below stays well defined.
   constexpr int kAStages = L::kPreA ? L::kAStages : 1;
+  constexpr int kMBlocks = L::kMBlocks;
+  constexpr int kRowsPerTile = L::kRowsPerTile;
+  constexpr uint32_t kAccBufs = L::kAccBufs;
+  constexpr uint32_t kASlotBytes = L::kASlotBytes;
   constexpr int kAOff = L::kAOff;
   constexpr int kOpOff = L::kOpOff;
   constexpr int kOpSlotBytes = L::kOpSlotBytes;
@@ -529,7 +544,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       // ready counter is read only when the warp has caught up with it.
       // Descriptors of slot 0 are built once; a slot's are those plus its
       // offset in the 16-byte address field.
-      constexpr uint32_t idesc = idesc_f16_f32(BMP, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
+      constexpr uint32_t idesc = idesc_f16_f32(2 * BM, BK, /*A K-major*/ 0, /*B MN-major*/ 1);
       const uint64_t a_desc0 = smem_desc_sw128(sbase + (L::kPreA ? kAOff : kOpOff), 16, kSbo);
       const uint64_t b_desc0 = smem_desc_sw128(sbase + kOpOff + L::kBInOp, kBLbo, kSbo);
       constexpr uint32_t kBStep = (2u * kSbo) >> 4;  // +2 n-groups per MMA K-step
@@ -542,14 +557,14 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         if (w.t < 0) break;
         const Tile tl = tile_at(descs, count, w.t);
         const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
-        const uint32_t acc = lt & 1u;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(tmem_empty(acc), ((lt >> 1) & 1u) ^ 1u,
-                                                       abort_flag))) {
+        const uint32_t acc = lt % kAccBufs;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(tmem_empty(acc),
+                                                       ((lt / kAccBufs) & 1u) ^ 1u, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BK;
+        const uint32_t d_tmem = tmem_base + acc * BK;  // M-block b: + b * BK
         for (int s = w.s0; s < s1; ++s) {
           if (lane == 0) NF4_PROBE(32, it);
           // The watcher publishes, in order, how many stages' operand barriers
@@ -574,14 +589,19 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           if (lane == 0) NF4_PROBE(33, it);
           const uint64_t off = static_cast<uint64_t>((slot * kOpSlotBytes) >> 4);
           const uint64_t a =
-              a_desc0 + (L::kPreA ? static_cast<uint64_t>((aslot * kABytes) >> 4) : off);
+              a_desc0 + (L::kPreA ? static_cast<uint64_t>((aslot * kASlotBytes) >> 4) : off);
           const uint64_t b = b_desc0 + off;
           if (elect_one()) {
             // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
-            tc_mma_f16_pair(d_tmem, a, b, idesc, s != w.s0 ? 1u : 0u);
-            tc_mma_f16_pair(d_tmem, a + 2u, b + kBStep, idesc, 1u);
-            tc_mma_f16_pair(d_tmem, a + 4u, b + 2u * kBStep, idesc, 1u);
-            tc_mma_f16_pair(d_tmem, a + 6u, b + 3u * kBStep, idesc, 1u);
+#pragma unroll
+            for (int mb = 0; mb < kMBlocks; ++mb) {
+              const uint32_t dm = d_tmem + static_cast<uint32_t>(mb * BK);
+              const uint64_t am = a + static_cast<uint64_t>((mb * kABytes) >> 4);
+              tc_mma_f16_pair(dm, am, b, idesc, s != w.s0 ? 1u : 0u);
+              tc_mma_f16_pair(dm, am + 2u, b + kBStep, idesc, 1u);
+              tc_mma_f16_pair(dm, am + 4u, b + 2u * kBStep, idesc, 1u);
+              tc_mma_f16_pair(dm, am + 6u, b + 3u * kBStep, idesc, 1u);
+            }
             tc_commit_pair(empty_op(slot), 0x3);
             if constexpr (L::kPreA) tc_commit_pair(empty_a(aslot), 0x3);
           }
@@ -605,8 +625,8 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       // The epilogues' arrivals for the last two tiles are not needed by any MMA,
       // but the CTA may not exit while one from the other CTA is still in flight.
       if (ok) {
-        for (uint32_t l = (lt > 2 ? lt - 2 : 0u); l < lt; ++l)
-          mbar_wait_cluster(tmem_empty(l & 1u), (l >> 1) & 1u, nullptr);
+        for (uint32_t l = (lt > kAccBufs ? lt - kAccBufs : 0u); l < lt; ++l)
+          mbar_wait_cluster(tmem_empty(l % kAccBufs), (l / kAccBufs) & 1u, nullptr);
       }
     }
     __syncwarp();
@@ -661,7 +681,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       if (w.t < 0) break;
       const Tile tl = tile_at(descs, count, w.t);
       const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
-      const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM;
+      const int row0 = tl.mt * kRowsPerTile + static_cast<int>(rank) * BM;
       for (int s = w.s0; s < s1; ++s, ++it) {
         const uint32_t slot = it % kAStages;
         bool free_slot = true;
@@ -671,10 +691,13 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           ok = false;
           break;
         }
-        if (lane == static_cast<int>(slot)) {
-          if (rank == 0) mbar_arrive_expect_tx(full_a(slot), 2u * kABytes);
-          tma_load_2d_pair(sbase + kAOff + slot * kABytes, &tl.p->tm_go, s * BN, row0,
-                           full_a_leader0 + 8u * slot);
+        // Lane kMBlocks*slot + b issues M-block b's box of the slot.
+        if (lane / kMBlocks == static_cast<int>(slot)) {
+          const int b = lane % kMBlocks;
+          if (rank == 0 && b == 0)
+            mbar_arrive_expect_tx(full_a(slot), 2u * kMBlocks * kABytes);
+          tma_load_2d_pair(sbase + kAOff + slot * kASlotBytes + b * kABytes, &tl.p->tm_go, s * BN,
+                           row0 + b * 256, full_a_leader0 + 8u * slot);
           NF4_PROBE(45, it);
         }
         __syncwarp();
@@ -855,8 +878,8 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         const int64_t x_last = static_cast<int64_t>(w.t - sk.dp_tiles) * sk.stages + sk.stages - 1;
         q_last = sk_owner(sk, x_last, nclusters);
       }
-      const uint32_t acc = lt & 1u;
-      const bool got = mbar_wait_cluster(tmem_full(acc), (lt >> 1) & 1u, abort_flag);
+      const uint32_t acc = lt % kAccBufs;
+      const bool got = mbar_wait_cluster(tmem_full(acc), (lt / kAccBufs) & 1u, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       if (threadIdx.x == 0) NF4_PROBE(35, lt);
       tc_fence_after();
@@ -871,7 +894,8 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         if (!__shfl_sync(0xFFFFFFFFu, ready, 0)) break;
         if (threadIdx.x == 0) NF4_PROBE(37, k);
       }
-      const int row0 = tl.mt * BMP + static_cast<int>(rank) * BM + warp * 32;
+      // M-block 0's rows and accumulator (block b: + 256 rows, + b * BK columns).
+      const int row0 = tl.mt * kRowsPerTile + static_cast<int>(rank) * BM + warp * 32;
       const uint32_t taddr = tmem_base + acc * BK + (static_cast<uint32_t>(warp * 32) << 16);
       // Partial sums move as this warp's 16 staging-layout chunks (2 KB each,
       // 32 KB per warp) between its slot in the workspace and shared memory.
@@ -893,10 +917,12 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       };
       // One 16-column chunk in r: through a staging buffer to grad_A (TMA
       // store) or, for the later stages of a split tile, to this pair's slot.
-      auto emit_chunk = [&](int c, const uint32_t (&r)[kEpiCols]) {
+      // c: column chunk of the M-block; seq: running chunk count of the item
+      // (selects the staging buffer).
+      auto emit_chunk = [&](int c, int seq, const uint32_t (&r)[kEpiCols], int rows) {
         // Two staging buffers: at most one copy may still be reading, so the
         // one that last used this buffer is done with it.
-        uint8_t* const buf = buf0 + (c & 1) * kEpiBufBytes;
+        uint8_t* const buf = buf0 + (seq & 1) * kEpiBufBytes;
         if (threadIdx.x == 0) NF4_PROBE(80, lt * 16 + c);
         if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
         __syncwarp();
@@ -908,19 +934,22 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           if (partial)
             bulk_store_s2g(warp_slot(cluster) + c * kEpiBufBytes, smem_addr(buf), kEpiBufBytes);
           else
-            tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * kEpiCols, row0, smem_addr(buf));
+            tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * kEpiCols, rows, smem_addr(buf));
           bulk_commit();
         }
         if (threadIdx.x == 0) NF4_PROBE(82, lt * 16 + c);
       };
       if (!finish) {
 #pragma unroll 1
-        for (int c = 0; c < BK / kEpiCols; ++c) {
-          uint32_t r[kEpiCols];
-          if (threadIdx.x == 0) NF4_PROBE(83, lt * 16 + c);
-          tmem_ld_cols<kEpiCols>(taddr + c * kEpiCols, r);
-          tmem_wait_ld();
-          emit_chunk(c, r);
+        for (int mb = 0; mb < kMBlocks; ++mb) {
+#pragma unroll 1
+          for (int c = 0; c < BK / kEpiCols; ++c) {
+            uint32_t r[kEpiCols];
+            if (threadIdx.x == 0) NF4_PROBE(83, lt * 16 + c);
+            tmem_ld_cols<kEpiCols>(taddr + mb * BK + c * kEpiCols, r);
+            tmem_wait_ld();
+            emit_chunk(c, mb * (BK / kEpiCols) + c, r, row0 + mb * 256);
+          }
         }
       } else {
         // First stages of a split tile, this pair's last item: its MMAs are
@@ -963,7 +992,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
             if (more) {
               tmem_st_cols<kEpiCols>(taddr + c * kEpiCols, r);
             } else {
-              emit_chunk(c, r);
+              emit_chunk(c, c, r, row0);
             }
           }
           if (more) tmem_wait_st();
@@ -1192,7 +1221,8 @@ static int check_problem(const void* go, int dtype, const float* scales, const u
 
 // Everything of a descriptor but the grad_out map.
 static int fill_desc_rest(ProblemDesc* d, int dtype, const float* scales, const uint8_t* data,
-                          float* grad_A, int M, int N, int K, int epi_cols) {
+                          float* grad_A, int M, int N, int K, int epi_cols,
+                          int rows_per_tile = BMP) {
   const int KB = K / 64;
   d->scale_tma = 0;
   if (KB % 4 == 0 && aligned(scales, 16)) {
@@ -1217,7 +1247,7 @@ static int fill_desc_rest(ProblemDesc* d, int dtype, const float* scales, const 
   d->N = N;
   d->K = K;
   d->dtype = dtype;
-  d->tiles_m = (M + BMP - 1) / BMP;
+  d->tiles_m = (M + rows_per_tile - 1) / rows_per_tile;
   d->tiles_k = (K + BK - 1) / BK;
   d->n_stages = (N + BN - 1) / BN;
   d->tile_begin = 0;
@@ -1245,14 +1275,17 @@ static inline size_t f16_bytes(int M, int N) {
 // Descriptor of the pre-converted variant: the A map reads the f16 copy (box
 // 64 columns x 128 rows, 128-byte swizzle = the K-major A operand layout).
 static int fill_desc_pre(ProblemDesc* d, const uint16_t* go_f16, const float* scales,
-                         const uint8_t* data, float* grad_A, int M, int N, int K) {
+                         const uint8_t* data, float* grad_A, int M, int N, int K,
+                         int rows_per_tile = LayoutPreA::kRowsPerTile) {
   std::memset(d, 0, sizeof(*d));
   if (!encode_2d(&d->tm_go, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, go_f16, static_cast<uint64_t>(N),
                  static_cast<uint64_t>(M), static_cast<uint64_t>(f16_pitch(N)) * 2, BN, BM,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   // dtype is not read by this variant (its A operand is f16 already).
-  return fill_desc_rest(d, NF4_BF16, scales, data, grad_A, M, N, K, LayoutPreA::kEpiCols);
+  static_assert(LayoutPreA::kEpiCols == LayoutPreA2::kEpiCols, "one tm_out box for both");
+  return fill_desc_rest(d, NF4_BF16, scales, data, grad_A, M, N, K, LayoutPreA::kEpiCols,
+                        rows_per_tile);
 }
 
 static int sm_count(int* out) {
@@ -1522,6 +1555,75 @@ static int run(const void* go, int dtype, const float* scales, const uint8_t* da
 
 using namespace nf4;
 
+namespace nf4 {
+// Workspace of nf4_backward_a_ws: the f16 copy of grad_out, then (optional)
+// the split-tile flags and partial sums for `pairs` pairs of CTAs.
+constexpr size_t kPartialBytes = static_cast<size_t>(2) * BM * BK * sizeof(float);  // 256 KiB
+static inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+static inline size_t sk_bytes(int pairs) {
+  return round256(sizeof(unsigned int) * static_cast<size_t>(pairs)) +
+         kPartialBytes * static_cast<size_t>(pairs);
+}
+
+// Split plan for T tiles of S stages over `pairs` pairs: whole waves stay whole;
+// the last, partial wave is split by stages when that saves every pair at
+// least kSplitMinSaving stages of the wave (S - rem * S / pairs).  A split
+// tile costs an extra partial-sum epilogue and a dependent finishing epilogue
+// (measured on GB300: worth roughly 30 stages of 64 on the critical path), so
+// smaller savings are not taken.
+constexpr int kSplitMinSaving = 40;
+static void plan_split(int T, int S, int pairs, SkArgs* sk) {
+  sk->dp_tiles = T;
+  sk->sk_tiles = 0;
+  sk->stages = S;
+  if (pairs <= 1 || S <= 1) return;
+  const int rem = T % pairs;
+  if (rem == 0) return;
+  if (static_cast<int64_t>(S) * (pairs - rem) < static_cast<int64_t>(kSplitMinSaving) * pairs)
+    return;
+  sk->dp_tiles = T - rem;
+  sk->sk_tiles = rem;
+}
+}  // namespace nf4
+
+namespace nf4 {
+// Work estimates (in units of a 256-token tile's stage) that choose between
+// 256- and 512-token pair tiles for the pre-converted kernel.  Measured on
+// GB300: a 512-token stage (8 MMAs against one dequantised B^T) takes ~1.3x a
+// 256-token stage, and a 512-token tile's epilogue, which does not overlap the
+// next tile, costs ~16 such stages.
+constexpr int kStage2Tenths = 13;
+constexpr int kEpi2Stages = 16;
+constexpr int kSplitCostStages = 16;
+
+static int64_t est_tiles256(int M, int tiles_k, int S, int pairs, bool can_split) {
+  const int64_t T = static_cast<int64_t>((M + 255) / 256) * tiles_k;
+  SkArgs sk;
+  std::memset(&sk, 0, sizeof(sk));
+  if (can_split && T <= INT_MAX) plan_split(static_cast<int>(T), S, pairs, &sk);
+  if (sk.sk_tiles > 0)
+    return static_cast<int64_t>(sk.dp_tiles / pairs) * S +
+           (static_cast<int64_t>(sk.sk_tiles) * S + pairs - 1) / pairs + kSplitCostStages;
+  return (T + pairs - 1) / pairs * S;
+}
+
+static int64_t est_tiles512(int M, int tiles_k, int S, int pairs) {
+  const int64_t T = static_cast<int64_t>((M + 511) / 512) * tiles_k;
+  return (T + pairs - 1) / pairs * ((static_cast<int64_t>(S) * kStage2Tenths + 9) / 10 + kEpi2Stages);
+}
+
+// 0: choose by the estimates; 256 or 512: always that (nf4_set_tile_rows).
+static std::atomic<int> g_tile_rows{0};
+
+static bool use_tiles512(int M, int N, int K, int pairs, bool can_split) {
+  const int forced = g_tile_rows.load();
+  if (forced != 0) return forced == 512;
+  if (pairs <= 0 || M <= 256) return false;
+  const int tiles_k = (K + BK - 1) / BK, S = (N + BN - 1) / BN;
+  return est_tiles512(M, tiles_k, S, pairs) < est_tiles256(M, tiles_k, S, pairs, can_split);
+}
+}  // namespace nf4
+
 extern "C" int nf4_abi_version(void) { return 1; }
 
 extern "C" int nf4_set_small_m_max(int m_max) {
@@ -1566,11 +1668,19 @@ extern "C" int nf4_backward_a_ex(const void* grad_out, int go_dtype, const float
   }
   if (go_dtype == NF4_F16) {
     // Already the A operand's type: the pre-converted kernel reads it as is.
+    int pairs = 0;
+    rc = max_clusters<LayoutPreA>(&pairs);
+    if (rc != NF4_OK) return rc;
+    const bool tiles512 = use_tiles512(M, N, K, pairs, /*can_split=*/false);
     ProblemDesc d;
-    rc = fill_desc_pre(&d, static_cast<const uint16_t*>(grad_out), scales, data, grad_A, M, N, K);
+    rc = fill_desc_pre(&d, static_cast<const uint16_t*>(grad_out), scales, data, grad_A, M, N, K,
+                       tiles512 ? LayoutPreA2::kRowsPerTile : LayoutPreA::kRowsPerTile);
     if (rc != NF4_OK) return rc;
     const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
     if (tiles > INT_MAX) return NF4_ERR_INVALID;
+    if (tiles512)
+      return launch_layout<LayoutPreA2>(d, nullptr, 1, static_cast<int>(tiles), nullptr,
+                                        as_stream(stream));
     return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles), nullptr,
                                      as_stream(stream));
   }
@@ -1589,36 +1699,16 @@ extern "C" int nf4_backward_a(const float* grad_out, const float* scales, const 
   return nf4_backward_a_ex(grad_out, NF4_F32, scales, data, grad_A, M, N, K, stream);
 }
 
-namespace nf4 {
-// Workspace of nf4_backward_a_ws: the f16 copy of grad_out, then (optional)
-// the split-tile flags and partial sums for `pairs` pairs of CTAs.
-constexpr size_t kPartialBytes = static_cast<size_t>(2) * BM * BK * sizeof(float);  // 256 KiB
-static inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-static inline size_t sk_bytes(int pairs) {
-  return round256(sizeof(unsigned int) * static_cast<size_t>(pairs)) +
-         kPartialBytes * static_cast<size_t>(pairs);
+
+extern "C" int nf4_set_tile_rows(int rows) {
+  if (rows != 0 && rows != 256 && rows != 512) return -1;
+  return g_tile_rows.exchange(rows);
 }
 
-// Split plan for T tiles of S stages over `pairs` pairs: whole waves stay whole;
-// the last, partial wave is split by stages when that saves every pair at
-// least kSplitMinSaving stages of the wave (S - rem * S / pairs).  A split
-// tile costs an extra partial-sum epilogue and a dependent finishing epilogue
-// (measured on GB300: worth roughly 30 stages of 64 on the critical path), so
-// smaller savings are not taken.
-constexpr int kSplitMinSaving = 40;
-static void plan_split(int T, int S, int pairs, SkArgs* sk) {
-  sk->dp_tiles = T;
-  sk->sk_tiles = 0;
-  sk->stages = S;
-  if (pairs <= 1 || S <= 1) return;
-  const int rem = T % pairs;
-  if (rem == 0) return;
-  if (static_cast<int64_t>(S) * (pairs - rem) < static_cast<int64_t>(kSplitMinSaving) * pairs)
-    return;
-  sk->dp_tiles = T - rem;
-  sk->sk_tiles = rem;
+extern "C" int nf4_tile_rows(int M, int N, int K, int pairs, int can_split) {
+  if (M <= 0 || N <= 0 || K <= 0 || pairs <= 0) return -1;
+  return use_tiles512(M, N, K, pairs, can_split != 0) ? 512 : 256;
 }
-}  // namespace nf4
 
 extern "C" int nf4_split_plan(int tiles, int stages, int pairs, int* dp_tiles, int* sk_tiles) {
   if (tiles <= 0 || stages <= 0 || pairs <= 0 || dp_tiles == nullptr || sk_tiles == nullptr)
@@ -1679,22 +1769,25 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
   // f16 grad_out is the A operand already (the copy region goes unused).
   const uint16_t* go_f16 = f16_in ? static_cast<const uint16_t*>(grad_out)
                                   : static_cast<uint16_t*>(workspace);
-  ProblemDesc d;
-  rc = fill_desc_pre(&d, go_f16, scales, data, grad_A, M, N, K);
-  if (rc != NF4_OK) return rc;
-  const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
-  if (tiles > INT_MAX) return NF4_ERR_INVALID;
   int pairs = 0;
   rc = max_clusters<LayoutPreA>(&pairs);
   if (rc != NF4_OK) return rc;
+  const size_t base = round256(f16_bytes(M, N));
+  const bool can_split = workspace_bytes >= base + sk_bytes(pairs);
+  const bool tiles512 = use_tiles512(M, N, K, pairs, can_split);
+  ProblemDesc d;
+  rc = fill_desc_pre(&d, go_f16, scales, data, grad_A, M, N, K,
+                     tiles512 ? LayoutPreA2::kRowsPerTile : LayoutPreA::kRowsPerTile);
+  if (rc != NF4_OK) return rc;
+  const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
+  if (tiles > INT_MAX) return NF4_ERR_INVALID;
   // The split needs its flags and partial sums after the f16 copy; a workspace
-  // holding only the copy runs every tile whole.
+  // holding only the copy runs every tile whole.  512-token tiles are never split.
   SkArgs sk;
   std::memset(&sk, 0, sizeof(sk));
-  const size_t base = round256(f16_bytes(M, N));
   unsigned int* flags = nullptr;
   int nflags = 0;
-  if (workspace_bytes >= base + sk_bytes(pairs)) {
+  if (can_split && !tiles512) {
     plan_split(static_cast<int>(tiles), d.n_stages, pairs, &sk);
     if (sk.sk_tiles > 0) {
       uint8_t* w = static_cast<uint8_t*>(workspace) + base;
@@ -1714,6 +1807,9 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
                        as_stream(stream));
     if (rc != NF4_OK) return rc;
   }
+  if (tiles512)
+    return launch_layout<LayoutPreA2>(d, nullptr, 1, static_cast<int>(tiles), nullptr,
+                                      as_stream(stream), /*pdl=*/!f16_in);
   return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles),
                                    sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream),
                                    /*pdl=*/!f16_in);

@@ -145,6 +145,25 @@ int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float* scales,
                       size_t workspace_bytes, void* stream);
 
 /*
+ * Tokens per pair tile, 256 or 512, that the pre-converted kernel uses for an
+ * M x N x K problem run by `pairs` pairs of CTAs (pure host computation).  A
+ * 512-token tile issues two M = 256 MMA blocks against each dequantised B^T
+ * stage, halving the dequantisation per MMA, but its two accumulators fill
+ * tensor memory, so its epilogue does not overlap the next tile and its tiles
+ * are never split.  The choice compares estimated stage counts of both
+ * (including the split when can_split != 0).  -1 for a non-positive argument.
+ */
+int nf4_tile_rows(int M, int N, int K, int pairs, int can_split);
+
+/*
+ * Force the pre-converted kernel's tile (256 or 512 tokens) for calls made
+ * after this returns, or 0 to choose by nf4_tile_rows (the default).  Returns
+ * the previous setting, or -1 (nothing changed) for another value.
+ * Process-wide.  Both tiles give the same results bit for bit.
+ */
+int nf4_set_tile_rows(int rows);
+
+/*
  * The split plan of nf4_backward_a_ws, as pure host computations (no device is
  * touched), for `tiles` pair tiles (256 tokens x 256 output columns) of
  * `stages` 64-wide stages of N each, run by `pairs` pairs of CTAs.  Whole waves

@@ -605,3 +605,49 @@ def test_batched_ws_rejects_small_workspace_without_launching():
     assert bool((out == 3.0).all())
     assert L.nf4_backward_a_batched_ws(arr, 1, C.c_void_p(ws.data_ptr()), need, None) == nb().NF4_OK
     nb().check_error()
+
+
+# ---------------------------------------------------------------- 512-token pair tiles
+# The pre-converted kernel's second variant issues two M = 256 MMA blocks per
+# dequantised B^T stage.  Each output element still sums the same products in
+# the same stage and K-step order, so the result equals the 256-token kernel's.
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_ws_512_token_tiles_match_plain_and_oracle(dtype):
+    p = Problem(2048, 4096, 4096, dtype, 1e-2, 0.015, True, 70 + dtype, "ws-512-rows")
+    assert nb().tile_rows(p.M, p.N, p.K, 76) == 512
+    run_problem(p, rows=sample_rows(p.M, 8, p.seed), check_codes=False, entry="ws")
+    go = to_device_go(make_grad_out(p), p.go_dtype)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    a = nb().backward_a_ws(go, w)
+    b = nb().backward_a_ws(go, w)
+    plain = nb().backward_a(go, w)
+    nb().check_error()
+    assert torch.equal(a, b)
+    assert torch.equal(a, plain)
+
+
+def test_ws_512_token_tiles_ragged_rows():
+    """M = 1300: the last 512-token tile has 276 rows, its second M-block only
+    20 (TMA zero fill above M, stores clipped)."""
+    p = Problem(1300, 2048, 4608, F32, 1.0, 0.02, False, 72, "ws-512-ragged")
+    run_problem(p, rows=sample_rows(p.M, 10, p.seed), check_codes=False, entry="ws")
+    go = to_device_go(make_grad_out(p), p.go_dtype)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    assert torch.equal(nb().backward_a_ws(go, w), nb().backward_a(go, w))
+    nb().check_error()
+
+
+@pytest.mark.parametrize("p", [Problem(512, 64, 256, F32, 1.0, 0.02, False, 73, "one-512-tile"),
+                               Problem(700, 136, 768, BF16, 1.0, 0.02, True, 74, "ragged-512"),
+                               Problem(300, 4, 192, F32, 1.0, 0.02, False, 75, "n4-512")],
+                         ids=lambda p: p.name)
+def test_forced_512_token_tiles_equal_256_and_oracle(p):
+    go = to_device_go(make_grad_out(p), p.go_dtype)
+    w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+    with nb().tile_rows_forced(512), nb().small_m_max(0):
+        a = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
+        run_problem(p, entry="ws")
+    with nb().tile_rows_forced(256), nb().small_m_max(0):
+        b = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
+    nb().check_error()
+    assert torch.equal(a, b)
