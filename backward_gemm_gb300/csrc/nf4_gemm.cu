@@ -156,7 +156,7 @@ struct Layout {
 using LayoutF32 = Layout<2, 4, 2 * kGoBoxBytes>;  // any fp32 grad_out in the launch
 using LayoutBF16 = Layout<2, 4, kGoBoxBytes>;     // bf16 grad_out only
 using LayoutPreA = Layout<6, 4, 0, 6, 32>;        // grad_out pre-converted to f16
-using LayoutPreA2 = Layout<4, 4, 0, 3, 32, 2>;    // pre-converted, 512-token pair tiles
+using LayoutPreA2 = Layout<2, 4, 0, 4, 16, 2>;    // pre-converted, 512-token pair tiles
 
 // B^T operand (MN-major, 128-byte swizzle): 64 output columns k per swizzle row,
 // 8 rows n per 1024-byte atom; atoms along k are kBLbo apart, atoms along n 1 KB.
@@ -1283,8 +1283,9 @@ static int fill_desc_pre(ProblemDesc* d, const uint16_t* go_f16, const float* sc
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return NF4_ERR_CUDA;
   // dtype is not read by this variant (its A operand is f16 already).
-  static_assert(LayoutPreA::kEpiCols == LayoutPreA2::kEpiCols, "one tm_out box for both");
-  return fill_desc_rest(d, NF4_BF16, scales, data, grad_A, M, N, K, LayoutPreA::kEpiCols,
+  return fill_desc_rest(d, NF4_BF16, scales, data, grad_A, M, N, K,
+                        rows_per_tile == LayoutPreA2::kRowsPerTile ? LayoutPreA2::kEpiCols
+                                                                   : LayoutPreA::kEpiCols,
                         rows_per_tile);
 }
 
