@@ -1588,40 +1588,26 @@ static void plan_split(int T, int S, int pairs, SkArgs* sk) {
 }  // namespace nf4
 
 namespace nf4 {
-// Work estimates (in units of a 256-token tile's stage) that choose between
-// 256- and 512-token pair tiles for the pre-converted kernel.  Measured on
-// GB300: a 512-token stage (8 MMAs against one dequantised B^T) takes ~1.3x a
-// 256-token stage, and a 512-token tile's epilogue, which does not overlap the
-// next tile, costs ~16 such stages.
-constexpr int kStage2Tenths = 13;
-constexpr int kEpi2Stages = 16;
-constexpr int kSplitCostStages = 16;
+// 256- or 512-token pair tiles for the pre-converted kernel.  A 512-token
+// stage issues 8 MMAs against one dequantised B^T stage; measured on GB300 it
+// takes ~1.4-1.5x a 256-token stage, and a 512-token tile's epilogue does not
+// overlap the next tile.  512-token tiles were faster on every measured shape
+// with at least 8 stages and at least half a wave of them (down/up/o/gate at
+// M = 4096, 2048 x 4096 x 4096, the 8191-token shapes, also against the split
+// 256-token schedule); slower on q_proj (24 such tiles for 76 pairs) and on
+// N = 256 (4 stages).
+static std::atomic<int> g_tile_rows{0};  // 0: by the rule below; 256 or 512: forced
 
-static int64_t est_tiles256(int M, int tiles_k, int S, int pairs, bool can_split) {
-  const int64_t T = static_cast<int64_t>((M + 255) / 256) * tiles_k;
-  SkArgs sk;
-  std::memset(&sk, 0, sizeof(sk));
-  if (can_split && T <= INT_MAX) plan_split(static_cast<int>(T), S, pairs, &sk);
-  if (sk.sk_tiles > 0)
-    return static_cast<int64_t>(sk.dp_tiles / pairs) * S +
-           (static_cast<int64_t>(sk.sk_tiles) * S + pairs - 1) / pairs + kSplitCostStages;
-  return (T + pairs - 1) / pairs * S;
+static bool tiles512_rule(int64_t tiles512, int S, int pairs) {
+  return S >= 8 && pairs > 0 && 2 * tiles512 >= pairs;
 }
 
-static int64_t est_tiles512(int M, int tiles_k, int S, int pairs) {
-  const int64_t T = static_cast<int64_t>((M + 511) / 512) * tiles_k;
-  return (T + pairs - 1) / pairs * ((static_cast<int64_t>(S) * kStage2Tenths + 9) / 10 + kEpi2Stages);
-}
-
-// 0: choose by the estimates; 256 or 512: always that (nf4_set_tile_rows).
-static std::atomic<int> g_tile_rows{0};
-
-static bool use_tiles512(int M, int N, int K, int pairs, bool can_split) {
+static bool use_tiles512(int M, int N, int K, int pairs, bool /*can_split*/) {
   const int forced = g_tile_rows.load();
   if (forced != 0) return forced == 512;
-  if (pairs <= 0 || M <= 256) return false;
-  const int tiles_k = (K + BK - 1) / BK, S = (N + BN - 1) / BN;
-  return est_tiles512(M, tiles_k, S, pairs) < est_tiles256(M, tiles_k, S, pairs, can_split);
+  if (M <= 256) return false;
+  const int64_t T2 = static_cast<int64_t>((M + 511) / 512) * ((K + BK - 1) / BK);
+  return tiles512_rule(T2, (N + BN - 1) / BN, pairs);
 }
 }  // namespace nf4
 
@@ -1937,6 +1923,29 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
   if (any_gemm && (workspace == nullptr || !aligned(workspace, 256) ||
                    workspace_bytes < desc_bytes + group_copy_bytes(problems, count)))
     return NF4_ERR_WORKSPACE;
+  // Tile size for the whole group: 512 tokens when every GEMM problem has more
+  // than 256 tokens, there are at least half a wave of 512-token tiles and the
+  // tiles average at least 8 stages (the single-problem rule, on the group).
+  int pairs = 0;
+  if (any_gemm) {
+    const int rc = max_clusters<LayoutPreA>(&pairs);
+    if (rc != NF4_OK) return rc;
+  }
+  int64_t t2 = 0, t2_stages = 0;
+  bool all_tall = true;
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    if (p.M == 0 || p.N == 0 || (p.go_dtype != NF4_F16 && p.M <= small_max)) continue;
+    const int64_t tiles = static_cast<int64_t>((p.M + 511) / 512) * ((p.K + BK - 1) / BK);
+    t2 += tiles;
+    t2_stages += tiles * ((p.N + BN - 1) / BN);
+    all_tall = all_tall && p.M > 256;
+  }
+  const int forced = g_tile_rows.load();
+  const bool tiles512 =
+      forced != 0 ? forced == 512
+                  : (all_tall && t2 > 0 && tiles512_rule(t2, static_cast<int>(t2_stages / t2), pairs));
+  const int rows_per_tile = tiles512 ? LayoutPreA2::kRowsPerTile : LayoutPreA::kRowsPerTile;
   std::vector<ProblemDesc> descs;
   descs.reserve(count);
   std::vector<F16Job> jobs;
@@ -1965,7 +1974,8 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
     }
     descs.emplace_back();
     const uint16_t* a = f16_in ? static_cast<const uint16_t*>(p.grad_out) : dst;
-    const int rc = fill_desc_pre(&descs.back(), a, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
+    const int rc = fill_desc_pre(&descs.back(), a, p.scales, p.data, p.grad_A, p.M, p.N, p.K,
+                                 rows_per_tile);
     if (rc != NF4_OK) return rc;
     if (!f16_in) {
       F16Job j;
@@ -2018,6 +2028,9 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
   }
   ProblemDesc unused;
   std::memset(&unused, 0, sizeof(unused));
+  if (tiles512)
+    return launch_layout<LayoutPreA2>(unused, ws, static_cast<int>(descs.size()),
+                                      static_cast<int>(total), nullptr, st, /*pdl=*/!jobs.empty());
   return launch_layout<LayoutPreA>(unused, ws, static_cast<int>(descs.size()),
                                    static_cast<int>(total), nullptr, st, /*pdl=*/!jobs.empty());
 }

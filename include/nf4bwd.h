@@ -150,8 +150,10 @@ int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float* scales,
  * 512-token tile issues two M = 256 MMA blocks against each dequantised B^T
  * stage, halving the dequantisation per MMA, but its two accumulators fill
  * tensor memory, so its epilogue does not overlap the next tile and its tiles
- * are never split.  The choice compares estimated stage counts of both
- * (including the split when can_split != 0).  -1 for a non-positive argument.
+ * are never split.  512 when the problem has at least 8 stages (N >= 449) and
+ * at least pairs / 2 such tiles; 256 otherwise (a rule from measurements;
+ * can_split is accepted for the split-aware choice and currently unused).
+ * -1 for a non-positive argument.
  */
 int nf4_tile_rows(int M, int N, int K, int pairs, int can_split);
 

@@ -91,13 +91,17 @@ def test_split_plan_rejects_bad_arguments():
 
 
 def test_tile_rows_choice_for_the_workloads():
-    """Large problems take 512-token tiles; q_proj (48 tiles of 256) and
-    up_proj (whose last wave is split) keep 256."""
+    """512-token tiles need >= 8 stages and >= pairs / 2 tiles: q_proj (24 such
+    tiles for 76 pairs) and N = 256 (4 stages) keep 256."""
     P = 76
     assert nb.tile_rows(2048, 1536, 1536, P) == 256          # q_proj
-    assert nb.tile_rows(4096, 8960, 1536, P) == 256          # up_proj
+    assert nb.tile_rows(4096, 256, 1536, P) == 256           # k_proj / v_proj
+    assert nb.tile_rows(4096, 8960, 1536, P) == 512          # up_proj
+    assert nb.tile_rows(4096, 1536, 8960, P) == 512          # down_proj
     assert nb.tile_rows(8191, 4096, 14336, P) == 512         # large_b
     assert nb.tile_rows(8191, 14336, 4096, P) == 512         # large_a
     assert nb.tile_rows(256, 4096, 4096, P) == 256           # one 256-token block
+    assert nb.tile_rows(4096, 448, 4096, P) == 256           # 7 stages
+    assert nb.tile_rows(4096, 512, 4096, P) == 512           # 8 stages
     with pytest.raises(ValueError):
         nb.tile_rows(0, 64, 64, P)
