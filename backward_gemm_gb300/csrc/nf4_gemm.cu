@@ -900,9 +900,11 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       // Partial sums move as this warp's 16 staging-layout chunks (2 KB each,
       // 32 KB per warp) between its slot in the workspace and shared memory.
       constexpr uint32_t kWarpPartBytes = (BK / kEpiCols) * kEpiBufBytes;  // 32 KB
-      auto warp_slot = [&](int q) {
+      // Pair q's slot: [q][M-block][rank][epilogue warp] x kWarpPartBytes.
+      auto warp_slot = [&](int q, int mb) {
         return reinterpret_cast<uint8_t*>(sk.partials) +
-               ((static_cast<size_t>(q) * 2 + rank) * kEpiWarps + warp) * kWarpPartBytes;
+               (((static_cast<size_t>(q) * kMBlocks + mb) * 2 + rank) * kEpiWarps + warp) *
+                   kWarpPartBytes;
       };
       // Row `lane` of a 32-row chunk, swizzled as the TMA stores to grad_A
       // read it (16-byte piece q of row r at q ^ ((r / 2) % 4) for 64-byte
@@ -919,7 +921,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       // store) or, for the later stages of a split tile, to this pair's slot.
       // c: column chunk of the M-block; seq: running chunk count of the item
       // (selects the staging buffer).
-      auto emit_chunk = [&](int c, int seq, const uint32_t (&r)[kEpiCols], int rows) {
+      auto emit_chunk = [&](int c, int seq, const uint32_t (&r)[kEpiCols], int mb) {
         // Two staging buffers: at most one copy may still be reading, so the
         // one that last used this buffer is done with it.
         uint8_t* const buf = buf0 + (seq & 1) * kEpiBufBytes;
@@ -932,9 +934,9 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           if (partial)
-            bulk_store_s2g(warp_slot(cluster) + c * kEpiBufBytes, smem_addr(buf), kEpiBufBytes);
+            bulk_store_s2g(warp_slot(cluster, mb) + c * kEpiBufBytes, smem_addr(buf), kEpiBufBytes);
           else
-            tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * kEpiCols, rows, smem_addr(buf));
+            tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * kEpiCols, row0 + mb * 256, smem_addr(buf));
           bulk_commit();
         }
         if (threadIdx.x == 0) NF4_PROBE(82, lt * 16 + c);
@@ -948,7 +950,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
             if (threadIdx.x == 0) NF4_PROBE(83, lt * 16 + c);
             tmem_ld_cols<kEpiCols>(taddr + mb * BK + c * kEpiCols, r);
             tmem_wait_ld();
-            emit_chunk(c, mb * (BK / kEpiCols) + c, r, row0 + mb * 256);
+            emit_chunk(c, mb * (BK / kEpiCols) + c, r, mb);
           }
         }
       } else {
@@ -959,8 +961,9 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         // with the result, the earlier ones back into TMEM.
         const uint32_t region = sbase + kRawOff + static_cast<uint32_t>(warp) * kWarpPartBytes;
         const uint8_t* const region_ptr = smem + kRawOff + warp * kWarpPartBytes;
-        uint32_t j = 0;
+        uint32_t j = 0;  // loads so far: the parity of part_bar
         bool ok_load = true;
+        for (int mb = 0; ok_load && mb < kMBlocks; ++mb)
         for (int q = cluster + 1; ok_load && q <= q_last; ++q) {
           if (!sk_has_stages(sk, q, nclusters)) continue;
           bool more = false;  // another contributor after q
@@ -971,14 +974,14 @@ __global__ void __launch_bounds__(L::kThreads, 1)
             fence_proxy_async_smem();
             fence_proxy_async_global();
             mbar_arrive_expect_tx(part_bar(warp), kWarpPartBytes);
-            bulk_load_g2s(region, warp_slot(q), kWarpPartBytes, part_bar(warp));
+            bulk_load_g2s(region, warp_slot(q, mb), kWarpPartBytes, part_bar(warp));
           }
           ok_load = __all_sync(0xFFFFFFFFu, mbar_wait(part_bar(warp), j & 1u, abort_flag));
           if (!ok_load) break;
 #pragma unroll 1
           for (int c = 0; c < BK / kEpiCols; ++c) {
             uint32_t r[kEpiCols];
-            tmem_ld_cols<kEpiCols>(taddr + c * kEpiCols, r);
+            tmem_ld_cols<kEpiCols>(taddr + mb * BK + c * kEpiCols, r);
             tmem_wait_ld();
             const uint8_t* src = region_ptr + c * kEpiBufBytes + lane * (kEpiCols * 4);
 #pragma unroll
@@ -990,9 +993,9 @@ __global__ void __launch_bounds__(L::kThreads, 1)
               r[4 * q4 + 3] = __float_as_uint(__uint_as_float(r[4 * q4 + 3]) + v.w);
             }
             if (more) {
-              tmem_st_cols<kEpiCols>(taddr + c * kEpiCols, r);
+              tmem_st_cols<kEpiCols>(taddr + mb * BK + c * kEpiCols, r);
             } else {
-              emit_chunk(c, c, r, row0);
+              emit_chunk(c, mb * (BK / kEpiCols) + c, r, mb);
             }
           }
           if (more) tmem_wait_st();
@@ -1559,7 +1562,8 @@ using namespace nf4;
 namespace nf4 {
 // Workspace of nf4_backward_a_ws: the f16 copy of grad_out, then (optional)
 // the split-tile flags and partial sums for `pairs` pairs of CTAs.
-constexpr size_t kPartialBytes = static_cast<size_t>(2) * BM * BK * sizeof(float);  // 256 KiB
+// Per pair: 2 CTAs x up to 2 M-blocks x 128 x 256 fp32.
+constexpr size_t kPartialBytes = static_cast<size_t>(2) * 2 * BM * BK * sizeof(float);  // 512 KiB
 static inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 static inline size_t sk_bytes(int pairs) {
   return round256(sizeof(unsigned int) * static_cast<size_t>(pairs)) +
@@ -1769,12 +1773,17 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
   const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
   if (tiles > INT_MAX) return NF4_ERR_INVALID;
   // The split needs its flags and partial sums after the f16 copy; a workspace
-  // holding only the copy runs every tile whole.  512-token tiles are never split.
+  // holding only the copy runs every tile whole.  The plan is made for the
+  // number of pairs the chosen kernel runs at once (its launch uses them all).
+  if (tiles512) {
+    rc = max_clusters<LayoutPreA2>(&pairs);
+    if (rc != NF4_OK) return rc;
+  }
   SkArgs sk;
   std::memset(&sk, 0, sizeof(sk));
   unsigned int* flags = nullptr;
   int nflags = 0;
-  if (can_split && !tiles512) {
+  if (can_split && workspace_bytes >= base + sk_bytes(pairs)) {
     plan_split(static_cast<int>(tiles), d.n_stages, pairs, &sk);
     if (sk.sk_tiles > 0) {
       uint8_t* w = static_cast<uint8_t*>(workspace) + base;
@@ -1795,8 +1804,9 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
     if (rc != NF4_OK) return rc;
   }
   if (tiles512)
-    return launch_layout<LayoutPreA2>(d, nullptr, 1, static_cast<int>(tiles), nullptr,
-                                      as_stream(stream), /*pdl=*/!f16_in);
+    return launch_layout<LayoutPreA2>(d, nullptr, 1, static_cast<int>(tiles),
+                                      sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream),
+                                      /*pdl=*/!f16_in);
   return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles),
                                    sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream),
                                    /*pdl=*/!f16_in);

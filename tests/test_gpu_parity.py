@@ -651,3 +651,39 @@ def test_forced_512_token_tiles_equal_256_and_oracle(p):
         b = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
     nb().check_error()
     assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- split with 512-token tiles
+def test_split_with_512_token_tiles_matches_oracle_and_is_deterministic():
+    """4 tiles of 512 x 256 and 64 stages over every pair: each tile split ~19
+    ways, partial sums of both M-blocks added in pair order."""
+    p = Problem(1024, 4096, 512, F32, 1.0, 0.015, True, 80, "split-512")
+    with nb().tile_rows_forced(512):
+        run_problem(p, entry="ws")
+        go = to_device_go(make_grad_out(p), p.go_dtype)
+        w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+        ws = nb().ws_workspace(p.M, p.N)
+        a = nb().backward_a_ws(go, w, ws)
+        b = nb().backward_a_ws(go, w, ws)
+        whole = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
+    nb().check_error()
+    assert torch.equal(a, b)
+    assert torch.allclose(a, whole, rtol=1e-4, atol=1e-4)
+    assert not torch.equal(a, whole)  # the split took place
+
+
+def test_whole_waves_plus_split_wave_with_512_token_tiles():
+    """90 tiles of 512 x 256 on a 152-SM GB300 (76 pairs): one whole wave, then
+    14 tiles split over all pairs."""
+    p = Problem(5120, 4096, 2304, BF16, 1e-2, 0.02, True, 81, "split-512-mixed")
+    with nb().tile_rows_forced(512):
+        run_problem(p, rows=sample_rows(p.M, 8, p.seed), check_codes=False, entry="ws")
+        go = to_device_go(make_grad_out(p), p.go_dtype)
+        w = nb().quantize(torch.from_numpy(make_weight(p)).cuda())
+        ws = nb().ws_workspace(p.M, p.N)
+        a = nb().backward_a_ws(go, w, ws)
+        b = nb().backward_a_ws(go, w, ws)
+        whole = nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
+    nb().check_error()
+    assert torch.equal(a, b)
+    assert torch.allclose(a, whole, rtol=1e-4, atol=1e-5)
