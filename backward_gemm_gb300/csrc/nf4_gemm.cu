@@ -126,7 +126,7 @@ struct Layout {
   static constexpr int kEpiOff = kOpOff + OS * kOpSlotBytes;
   static constexpr int kBarOff = kEpiOff + kEpiWarps * kEpiBufs * kEpiBufBytes;
   // ... + one barrier per epilogue warp for reading other pairs' partial sums
-  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1 + 2 * RA + kEpiWarps;
+  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1 + 2 * RA + kEpiWarps + 1;
   // misc: TMEM address, abort flag, the ready counter (and spare words), then the
   // 16-byte signal words: in CTA 0 one destination per (operand slot,
   // converter warp of a group), and one source.
@@ -141,6 +141,14 @@ struct Layout {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kRawBytes % 1024 == 0 && kOpSlotBytes % 1024 == 0 && kABytes % 1024 == 0, "align");
   static_assert(kSigOff % 16 == 0 && kSigSrcOff % 16 == 0, "bulk-copy addresses are 16-byte aligned");
+  // A pair's last item stages each epilogue warp's M-block (and a finishing
+  // pair loads partial sums) in the idle rings: 32 KB per warp.
+  static_assert(kEpiWarps * (BK / EC) * kEpiBufBytes <= kEpiOff - kRawOff,
+                "the rings hold every epilogue warp's M-block");
+  // Two M-blocks: every tile's epilogue stages in the A ring (see kEpiInARing).
+  static constexpr bool kEpiInARing = MB == 2;
+  static_assert(!kEpiInARing || kEpiWarps * (BK / EC) * kEpiBufBytes <= RA * MB * kABytes,
+                "the A ring holds every epilogue warp's M-block");
   static_assert(kReadyOff + 4 * OS <= kSigOff, "ready counter fits before the signal area");
   static_assert(RS * kBoxes <= 32 && RA <= 32, "one producer lane per (ring slot, box)");
   // Each raw slot must always be consumed by the same converter group.  A group
@@ -187,34 +195,44 @@ static_assert(sizeof(ProblemDesc) == 640, "descriptor size (the no-allocation ar
 // registers (the inline-asm memory clobbers would otherwise force reloads).
 struct Tile {
   const ProblemDesc* p;
+  const float* scales;
   int M, N, K, dtype;
   int mt, kt, ns, stma;
 };
 
-__device__ __forceinline__ Tile tile_at(const ProblemDesc* descs, int count, int t) {
-  int lo = 0, hi = count - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (descs[mid].tile_begin <= t) lo = mid; else hi = mid - 1;
-  }
+__device__ __forceinline__ Tile tile_fields(const ProblemDesc& d, const ProblemDesc* p, int t) {
   Tile r;
-  const ProblemDesc* p = descs + lo;
   r.p = p;
-  r.M = p->M;
-  r.N = p->N;
-  r.K = p->K;
-  r.dtype = p->dtype;
+  r.scales = d.scales;
+  r.M = d.M;
+  r.N = d.N;
+  r.K = d.K;
+  r.dtype = d.dtype;
   // Output-column tiles vary fastest: the pairs running at the same time then
   // share a few 256-row blocks of grad_out, which stay in L2 while every column
   // tile of them is computed (row-block-fastest order made them stream grad_out
   // from DRAM once per column tile when it does not fit in L2).
-  const int local = t - p->tile_begin;
-  const int tk = p->tiles_k;
+  const int local = t - d.tile_begin;
+  const int tk = d.tiles_k;
   r.mt = local / tk;
   r.kt = local % tk;
-  r.ns = p->n_stages;
-  r.stma = p->scale_tma;
+  r.ns = d.n_stages;
+  r.stma = d.scale_tma;
   return r;
+}
+
+// Tile t of the launch: of the single problem passed by value (its fields are
+// read from the kernel's parameters, no global-memory round trip before the
+// first copies), or of the grouped launch's descriptor array.
+__device__ __forceinline__ Tile tile_at(const ProblemDesc& single, const ProblemDesc* batch,
+                                        int count, int t) {
+  if (batch == nullptr) return tile_fields(single, &single, t);
+  int lo = 0, hi = count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (batch[mid].tile_begin <= t) lo = mid; else hi = mid - 1;
+  }
+  return tile_fields(batch[lo], batch + lo, t);
 }
 
 // ------------------------------------------------------------------ work schedule
@@ -297,11 +315,11 @@ struct ConvCursor {
 };
 
 __device__ __forceinline__ void cc_load(ConvCursor& c, const SkArgs& sk, int cluster, int pairs,
-                                        const ProblemDesc* descs, int count) {
+                                        const ProblemDesc& single, const ProblemDesc* batch, int count) {
   const Item w = item_at(sk, cluster, pairs, c.k);
   c.t = w.t;
   if (w.t >= 0) {
-    const Tile tl = tile_at(descs, count, w.t);
+    const Tile tl = tile_at(single, batch, count, w.t);
     c.s = w.s0;
     c.s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
     c.kt = tl.kt;
@@ -309,12 +327,12 @@ __device__ __forceinline__ void cc_load(ConvCursor& c, const SkArgs& sk, int clu
     c.KB = tl.K >> 6;
     c.f32 = tl.dtype == NF4_F32;
     c.stma = tl.stma != 0;
-    c.scales = tl.p->scales;
+    c.scales = tl.scales;
   }
 }
 
 __device__ __forceinline__ void cc_start(ConvCursor& c, const SkArgs& sk, int cluster, int pairs,
-                                         const ProblemDesc* descs, int count) {
+                                         const ProblemDesc& single, const ProblemDesc* batch, int count) {
   c.k = 0;
   c.s = 0;
   c.s1 = 1;
@@ -324,15 +342,15 @@ __device__ __forceinline__ void cc_start(ConvCursor& c, const SkArgs& sk, int cl
   c.f32 = true;
   c.stma = false;
   c.scales = nullptr;
-  cc_load(c, sk, cluster, pairs, descs, count);
+  cc_load(c, sk, cluster, pairs, single, batch, count);
 }
 
 __device__ __forceinline__ void cc_next(ConvCursor& c, const SkArgs& sk, int cluster, int pairs,
-                                        const ProblemDesc* descs, int count) {
+                                        const ProblemDesc& single, const ProblemDesc* batch, int count) {
   if (c.t < 0) return;
   if (++c.s >= c.s1) {
     ++c.k;
-    cc_load(c, sk, cluster, pairs, descs, count);
+    cc_load(c, sk, cluster, pairs, single, batch, count);
   }
 }
 
@@ -407,6 +425,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
   auto part_bar = [&](uint32_t w) {
     return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + 2 * L::kAStages + w);
   };
+  // Two M-blocks: the epilogue warps hand the A ring back after each item (one
+  // phase per item, kEpiWarps arrivals).
+  const uint32_t epi_release =
+      bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + 2 * L::kAStages + kEpiWarps);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -447,6 +469,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       mbar_init(empty_a(i), 1);
     }
     for (int i = 0; i < kEpiWarps; ++i) mbar_init(part_bar(i), 1);
+    mbar_init(epi_release, kEpiWarps);
     for (int i = 0; i < kOpStages; ++i)
       reinterpret_cast<volatile uint32_t*>(smem + kReadyOff)[i] = 0u;
     *abort_flag = 0;
@@ -458,7 +481,11 @@ __global__ void __launch_bounds__(L::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+  // Barriers of both CTAs are initialised before any remote arrive: every role
+  // waits for the peer CTA here, except the raw producer, whose copies complete
+  // on this CTA's own barriers; it issues its first stages first.
+  cluster_arrive();
+  if (warp != kProducerWarp) cluster_wait();
   if (threadIdx.x == 0) NF4_PROBE(39, 0);
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -479,10 +506,11 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     const int box = L::kPreA ? 2 + (lane & 1) : (lane & 3);
     uint32_t it = 0;
     bool ok = true;
+    bool peer_ready = false;  // this warp's cluster_wait done
     for (int k = 0; ok; ++k) {
       const Item w = item_at(sk, cluster, nclusters, k);
       if (w.t < 0) break;
-      const Tile tl = tile_at(descs, count, w.t);
+      const Tile tl = tile_at(single, batch, count, w.t);
       const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
       const bool f32 = tl.dtype == NF4_F32;
       const uint32_t bytes = (L::kPreA ? 0u : (f32 ? 2u * kGoBoxBytes : kGoBoxBytes)) +
@@ -497,6 +525,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       const bool my_box = box == 3 ? tl.stma != 0 : (box != 1 || f32);
       const bool registers = L::kPreA ? box == 2 : box == 0;
       for (int s = w.s0; s < s1; ++s, ++it) {
+        if (!peer_ready && it == static_cast<uint32_t>(kRawStages)) {  // the ring's first fill is out
+          cluster_wait();
+          peer_ready = true;
+        }
         const uint32_t slot = it % kRawStages;
         bool free_slot = true;
         if (lane == 0) free_slot = mbar_wait(empty_raw(slot), ((it / kRawStages) & 1u) ^ 1u, abort_flag);
@@ -522,6 +554,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         __syncwarp();
       }
     }
+    if (!peer_ready) cluster_wait();  // no more stages than slots
     if (lane == 0) {
       // Every issued copy must land before the CTA may exit.
       for (uint32_t i = (it > kRawStages ? it - kRawStages : 0u); i < it; ++i)
@@ -555,7 +588,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       for (int k = 0; ok; ++k, ++lt) {
         const Item w = item_at(sk, cluster, nclusters, k);
         if (w.t < 0) break;
-        const Tile tl = tile_at(descs, count, w.t);
+        const Tile tl = tile_at(single, batch, count, w.t);
         const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
         const uint32_t acc = lt % kAccBufs;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(tmem_empty(acc),
@@ -641,7 +674,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       for (int k = 0; ok; ++k) {
         const Item w = item_at(sk, cluster, nclusters, k);
         if (w.t < 0) break;
-        const Tile tl = tile_at(descs, count, w.t);
+        const Tile tl = tile_at(single, batch, count, w.t);
         const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
         for (int s = w.s0; s < s1; ++s, ++it) {
           const uint32_t slot = it % kOpStages;
@@ -679,9 +712,21 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     for (int k = 0; ok; ++k) {
       const Item w = item_at(sk, cluster, nclusters, k);
       if (w.t < 0) break;
-      const Tile tl = tile_at(descs, count, w.t);
+      const Tile tl = tile_at(single, batch, count, w.t);
       const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
       const int row0 = tl.mt * kRowsPerTile + static_cast<int>(rank) * BM;
+      if constexpr (L::kEpiInARing) {
+        // The previous item's epilogue stages its result in the A ring: wait
+        // until its stores have read it.
+        if (k > 0) {
+          bool released = true;
+          if (lane == 0) released = mbar_wait(epi_release, static_cast<uint32_t>(k - 1) & 1u, abort_flag);
+          if (!__shfl_sync(0xFFFFFFFFu, released, 0)) {
+            ok = false;
+            break;
+          }
+        }
+      }
       for (int s = w.s0; s < s1; ++s, ++it) {
         const uint32_t slot = it % kAStages;
         bool free_slot = true;
@@ -731,15 +776,15 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     // `nxt` runs two stages (one group turn) ahead of the stage being converted,
     // so the block scale it needs is loaded a whole turn before its use.
     ConvCursor nxt;
-    cc_start(nxt, sk, cluster, nclusters, descs, count);
-    for (int i = 0; i < group; ++i) cc_next(nxt, sk, cluster, nclusters, descs, count);
+    cc_start(nxt, sk, cluster, nclusters, single, batch, count);
+    for (int i = 0; i < group; ++i) cc_next(nxt, sk, cluster, nclusters, single, batch, count);
     // (Scales that travel with the raw stage are read from it instead.)
     bool cur_valid = nxt.t >= 0;
     bool cur_f32 = nxt.f32;
     bool cur_stma = nxt.stma;
     float scale_cur = cur_valid && !cur_stma ? cc_scale(nxt, rank, bj, bn) : 0.0f;
-    cc_next(nxt, sk, cluster, nclusters, descs, count);
-    cc_next(nxt, sk, cluster, nclusters, descs, count);
+    cc_next(nxt, sk, cluster, nclusters, single, batch, count);
+    cc_next(nxt, sk, cluster, nclusters, single, batch, count);
     // This thread's scale within a raw slot's scale box (row bn, 16 bytes per row).
     const uint32_t scale_off = L::kScaleOff + bn * 16 + (2u * rank + bj) * 4u;
 
@@ -752,8 +797,8 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       cur_f32 = nxt.f32;
       cur_stma = nxt.stma;
       scale_cur = cur_valid && !cur_stma ? cc_scale(nxt, rank, bj, bn) : 0.0f;
-      cc_next(nxt, sk, cluster, nclusters, descs, count);
-      cc_next(nxt, sk, cluster, nclusters, descs, count);
+      cc_next(nxt, sk, cluster, nclusters, single, batch, count);
+      cc_next(nxt, sk, cluster, nclusters, single, batch, count);
 
       const uint32_t rslot = it % kRawStages;
       const uint32_t oslot = it % kOpStages;
@@ -868,10 +913,16 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     for (int k = 0;; ++k, ++lt) {
       const Item w = item_at(sk, cluster, nclusters, k);
       if (w.t < 0) break;
-      const Tile tl = tile_at(descs, count, w.t);
+      const Tile tl = tile_at(single, batch, count, w.t);
       const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
       const bool partial = w.s0 > 0;                // later stages of a split tile
       const bool finish = !partial && s1 < tl.ns;  // first stages of a split tile
+      // The pair's last item: once its accumulator is full every stage has been
+      // consumed, so the operand rings are idle and serve as deep staging (a
+      // warp's whole M-block of chunks, no wait for a staging buffer).
+      // With two M-blocks every item does so in the A ring, which the A producer
+      // refills for the next item only after the epilogue has released it.
+      const bool deep = L::kEpiInARing || item_at(sk, cluster, nclusters, k + 1).t < 0;
       // Pairs whose partial sums complete this tile: cluster+1 .. q_last.
       int q_last = cluster;
       if (finish) {
@@ -901,6 +952,12 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       // 32 KB per warp) between its slot in the workspace and shared memory.
       constexpr uint32_t kWarpPartBytes = (BK / kEpiCols) * kEpiBufBytes;  // 32 KB
       // Pair q's slot: [q][M-block][rank][epilogue warp] x kWarpPartBytes.
+      // This warp's 32 KB of the rings (deep staging; a finishing pair's
+      // partial-sum loads): in the A ring with two M-blocks, else from the
+      // start of the rings (idle during a pair's last item).
+      constexpr int kRegionOff = L::kEpiInARing ? L::kAOff : kRawOff;
+      const uint32_t region = sbase + kRegionOff + static_cast<uint32_t>(warp) * kWarpPartBytes;
+      uint8_t* const region_ptr = smem + kRegionOff + warp * kWarpPartBytes;
       auto warp_slot = [&](int q, int mb) {
         return reinterpret_cast<uint8_t*>(sk.partials) +
                (((static_cast<size_t>(q) * kMBlocks + mb) * 2 + rank) * kEpiWarps + warp) *
@@ -922,11 +979,12 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       // c: column chunk of the M-block; seq: running chunk count of the item
       // (selects the staging buffer).
       auto emit_chunk = [&](int c, int seq, const uint32_t (&r)[kEpiCols], int mb) {
-        // Two staging buffers: at most one copy may still be reading, so the
-        // one that last used this buffer is done with it.
-        uint8_t* const buf = buf0 + (seq & 1) * kEpiBufBytes;
+        // Deep staging: chunk c of the M-block has its own place in the rings.
+        // Otherwise two staging buffers: at most one copy may still be
+        // reading, so the one that last used this buffer is done with it.
+        uint8_t* const buf = deep ? region_ptr + c * kEpiBufBytes : buf0 + (seq & 1) * kEpiBufBytes;
         if (threadIdx.x == 0) NF4_PROBE(80, lt * 16 + c);
-        if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
+        if (!deep && lane == 0) bulk_wait_read<kEpiBufs - 1>();
         __syncwarp();
         if (threadIdx.x == 0) NF4_PROBE(81, lt * 16 + c);
         stage_chunk(buf, r);
@@ -941,16 +999,65 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         }
         if (threadIdx.x == 0) NF4_PROBE(82, lt * 16 + c);
       };
-      if (!finish) {
+      if (!finish && deep) {
+        // The pair's last item: the warp stages its whole M-block in the
+        // region (chunk c at c x kEpiBufBytes, the staging layout), then
+        // one proxy fence and all of the M-block's stores.
 #pragma unroll 1
         for (int mb = 0; mb < kMBlocks; ++mb) {
+          if (mb > 0) {  // the previous M-block's stores must have read the region
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+          }
 #pragma unroll 1
           for (int c = 0; c < BK / kEpiCols; ++c) {
             uint32_t r[kEpiCols];
-            if (threadIdx.x == 0) NF4_PROBE(83, lt * 16 + c);
             tmem_ld_cols<kEpiCols>(taddr + mb * BK + c * kEpiCols, r);
             tmem_wait_ld();
-            emit_chunk(c, mb * (BK / kEpiCols) + c, r, mb);
+            if (threadIdx.x == 0) NF4_PROBE(83, mb * 16 + c);
+            stage_chunk(region_ptr + c * kEpiBufBytes, r);
+            if (threadIdx.x == 0) NF4_PROBE(80, mb * 16 + c);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (threadIdx.x == 0) NF4_PROBE(81, mb);
+          if (lane == 0) {
+            if (partial) {
+              bulk_store_s2g(warp_slot(cluster, mb), region, kWarpPartBytes);
+            } else {
+#pragma unroll 1
+              for (int c = 0; c < BK / kEpiCols; ++c)
+                tma_store_2d(&tl.p->tm_out, tl.kt * BK + c * kEpiCols, row0 + mb * 256,
+                             region + c * kEpiBufBytes);
+            }
+            bulk_commit();
+          }
+          if (threadIdx.x == 0) NF4_PROBE(82, mb);
+        }
+      } else if (!finish) {
+#pragma unroll 1
+        for (int mb = 0; mb < kMBlocks; ++mb) {
+          if constexpr (kEpiCols == 16) {
+            // Two 16-column chunks per TMEM wait: one load latency per pair.
+#pragma unroll 1
+            for (int c = 0; c < BK / kEpiCols; c += 2) {
+              uint32_t r[kEpiCols], r2[kEpiCols];
+              if (threadIdx.x == 0) NF4_PROBE(83, lt * 16 + c);
+              tmem_ld_cols<kEpiCols>(taddr + mb * BK + c * kEpiCols, r);
+              tmem_ld_cols<kEpiCols>(taddr + mb * BK + (c + 1) * kEpiCols, r2);
+              tmem_wait_ld();
+              emit_chunk(c, mb * (BK / kEpiCols) + c, r, mb);
+              emit_chunk(c + 1, mb * (BK / kEpiCols) + c + 1, r2, mb);
+            }
+          } else {
+#pragma unroll 1
+            for (int c = 0; c < BK / kEpiCols; ++c) {
+              uint32_t r[kEpiCols];
+              if (threadIdx.x == 0) NF4_PROBE(83, lt * 16 + c);
+              tmem_ld_cols<kEpiCols>(taddr + mb * BK + c * kEpiCols, r);
+              tmem_wait_ld();
+              emit_chunk(c, mb * (BK / kEpiCols) + c, r, mb);
+            }
           }
         }
       } else {
@@ -959,8 +1066,6 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         // partial sums (32 KB for this warp) are bulk-loaded into the rings
         // and added to the accumulator in pair order; the last one goes out
         // with the result, the earlier ones back into TMEM.
-        const uint32_t region = sbase + kRawOff + static_cast<uint32_t>(warp) * kWarpPartBytes;
-        const uint8_t* const region_ptr = smem + kRawOff + warp * kWarpPartBytes;
         uint32_t j = 0;  // loads so far: the parity of part_bar
         bool ok_load = true;
         for (int mb = 0; ok_load && mb < kMBlocks; ++mb)
@@ -969,8 +1074,11 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           bool more = false;  // another contributor after q
           for (int q2 = q + 1; q2 <= q_last; ++q2) more = more || sk_has_stages(sk, q2, nclusters);
           if (lane == 0) {
-            // Generic reads of this region (previous contributor) and the
-            // acquire of the counts come before the async-proxy copy.
+            // Stores of the previous M-block's result (deep staging in this
+            // region) must have read it; generic reads of the region (previous
+            // contributor) and the acquire of the counts come before the
+            // async-proxy copy.
+            bulk_wait_read<0>();
             fence_proxy_async_smem();
             fence_proxy_async_global();
             mbar_arrive_expect_tx(part_bar(warp), kWarpPartBytes);
@@ -1009,6 +1117,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       if (lane == 0) {
         if (rank == 0) mbar_arrive(tmem_empty(acc));
         else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
+        if constexpr (L::kEpiInARing) {
+          bulk_wait_read<0>();  // the stores have read the staged result
+          mbar_arrive(epi_release);
+        }
         if (partial) {
           // The warp's partial sums are in global memory once its copies have
           // completed; then they are made visible to generic-proxy readers and
@@ -1025,6 +1137,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
+    if (threadIdx.x == 0) NF4_PROBE(84, 0);
   }
 
   tc_fence_before();

@@ -20,7 +20,10 @@ namespace nf4 {
 // copy, 46 watcher sees both A copies landed; epilogue: 34 slot k = item k's
 // partial sums written and counted, 37 slot k = item k's partner counts all
 // seen; 48-63 converter warp 0-15 has
-// stored its B^T chunks, 64-79 it has also passed the proxy fence.
+// stored its B^T chunks, 64-79 it has also passed the proxy fence; epilogue
+// warp 0, a pair's last item (slot 16 * M-block + chunk): 83 chunk loaded from
+// TMEM, 80 chunk staged, 81 (slot M-block) proxy fence passed, 82 stores
+// issued; 84 slot 0: the epilogue's stores have completed.
 //
 // Few-token kernel (small_m_kernel), CTAs 0 and 1 (k-tile 0, cluster ranks 0
 // and 1 when S > 1): slot s of events 0-6 and 8 is stage s.  0 producer issues
