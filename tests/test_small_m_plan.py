@@ -33,12 +33,21 @@ def test_every_rank_gets_work_and_all_of_n_is_covered(nb, N, K, sms, slots):
 @pytest.mark.parametrize("N,K,slots", [(14336, 4096, 456), (4096, 14336, 456),
                                        (14336, 4096, 304)])
 def test_few_tiles_are_split_to_fill_the_gpu(nb, N, K, slots):
-    """With fewer 128-column tiles than SMs, the split puts at least one CTA on
-    most SMs, and all of them fit at once."""
+    """With fewer 256-column tiles than SMs, the split puts a CTA on most SMs
+    (at least 70%), and all of them fit at once."""
     S, _ = nb.small_m_split(N, K, 152, slots)
     T = -(-K // 256)
-    assert T * S >= 0.8 * 152
+    assert T * S >= 0.7 * 152
     assert T * S <= slots
+
+
+@pytest.mark.parametrize("slots", [304, 456])
+def test_long_n_prefers_fewer_longer_slices(nb, slots):
+    """M = 16, N = 4096, K = 14336 (56 k-tiles of 64 stages): on GB300 clusters
+    of 2 (one CTA per SM, 32 stages each) took 28.5 us, clusters of 5 (two CTAs
+    on most SMs, 13 stages each) 31.0 us; the rule's fixed cost per CTA makes it
+    take the former."""
+    assert nb.small_m_split(4096, 14336, 152, slots) == (2, 32)
 
 
 def test_one_stage_means_no_split(nb):
