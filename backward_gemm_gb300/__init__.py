@@ -48,6 +48,8 @@ SIGNATURES = {
     "nf4_backward_a_ex": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "nf4_backward_a_ws_bytes": (_sz, [_i, _i]),
     "nf4_backward_a_ws": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
+    "nf4_forward_ws_bytes": (_sz, [_i, _i]),
+    "nf4_forward_ws": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
     "nf4_tile_rows": (_i, [_i, _i, _i, _i, _i]),
     "nf4_set_tile_rows": (_i, [_i]),
     "nf4_split_plan": (_i, [_i, _i, _i, C.POINTER(_i), C.POINTER(_i)]),
@@ -255,6 +257,38 @@ def backward_a_ws(grad_out: torch.Tensor, w: NF4Weight, workspace: torch.Tensor 
                                    _stream()),
            "nf4_backward_a_ws")
     return out
+
+
+def forward_ws(A: torch.Tensor, w: NF4Weight, workspace: torch.Tensor | None = None,
+               out: torch.Tensor | None = None):
+    """C[M, N] = A[M, K] @ dequant(B)[K, N] through ``nf4_forward_ws`` (the
+    forward counterpart: contracted over K; A rounded to f16, the same
+    dequantised operand values as the backward, f32 accumulation).  A is
+    float32, bfloat16 or float16 [M, K]; returns C float32 [M, N]."""
+    _require_cuda_contig("A", A)
+    M, K = A.shape
+    if K != w.K:
+        raise ValueError(f"A has K={K}, weight has K={w.K}")
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.float32, device=A.device)
+    _require_cuda_contig("out", out)
+    if out.dtype != torch.float32 or tuple(out.shape) != (M, w.N):
+        raise ValueError("out must be float32 [M, N]")
+    if workspace is None:
+        n = int(lib().nf4_forward_ws_bytes(M, K))
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=A.device)
+    _require_cuda_contig("workspace", workspace)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().nf4_forward_ws(_ptr(A), _dtype_code(A), _ptr(w.scales), _ptr(w.data), _ptr(out),
+                                M, w.N, K, _ptr(workspace), nbytes, _stream()),
+           "nf4_forward_ws")
+    return out
+
+
+def fwd_workspace(M: int, K: int, device=None) -> torch.Tensor:
+    """Workspace for :func:`forward_ws` (f16 copy of A plus the split area)."""
+    n = int(lib().nf4_forward_ws_bytes(M, K))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
 
 
 def batched_workspace(count: int, device=None) -> torch.Tensor:

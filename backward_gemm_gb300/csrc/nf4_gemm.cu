@@ -186,6 +186,12 @@ struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
   // are 16-byte strided); 0: each converter thread loads its scale from global
   // memory a turn ahead of its use.
   int scale_tma;
+  // 1: the forward product C[M x N] = A[M x K] @ dequant(B_nf4[K x N]) (the
+  // shared dimension is K): tm_go holds A (f16), tm_nf4 boxes are 128 rows n x
+  // 32 bytes (one 64-k block per row, no swizzle), tm_out is C, M/N/K keep
+  // their forward meaning, tiles_k counts 256-column tiles of N and n_stages
+  // the 64-wide stages of K.  Pre-converted variant only; scale_tma is 0.
+  int fwd;
 };
 
 static_assert(sizeof(ProblemDesc) % 16 == 0, "descriptor copy granularity");
@@ -197,7 +203,7 @@ struct Tile {
   const ProblemDesc* p;
   const float* scales;
   int M, N, K, dtype;
-  int mt, kt, ns, stma;
+  int mt, kt, ns, stma, fwd;
 };
 
 __device__ __forceinline__ Tile tile_fields(const ProblemDesc& d, const ProblemDesc* p, int t) {
@@ -218,6 +224,7 @@ __device__ __forceinline__ Tile tile_fields(const ProblemDesc& d, const ProblemD
   r.kt = local % tk;
   r.ns = d.n_stages;
   r.stma = d.scale_tma;
+  r.fwd = d.fwd;
   return r;
 }
 
@@ -310,7 +317,7 @@ __host__ __device__ __forceinline__ int sk_owner(const SkArgs& sk, int64_t x, in
 // with the fields of that tile's problem needed for the scale loads.
 struct ConvCursor {
   int k, t, s, s1, kt, N, KB;
-  bool f32, stma;
+  bool f32, stma, fwd;
   const float* scales;
 };
 
@@ -327,6 +334,7 @@ __device__ __forceinline__ void cc_load(ConvCursor& c, const SkArgs& sk, int clu
     c.KB = tl.K >> 6;
     c.f32 = tl.dtype == NF4_F32;
     c.stma = tl.stma != 0;
+    c.fwd = tl.fwd != 0;
     c.scales = tl.scales;
   }
 }
@@ -341,6 +349,7 @@ __device__ __forceinline__ void cc_start(ConvCursor& c, const SkArgs& sk, int cl
   c.KB = 0;
   c.f32 = true;
   c.stma = false;
+  c.fwd = false;
   c.scales = nullptr;
   cc_load(c, sk, cluster, pairs, single, batch, count);
 }
@@ -361,6 +370,14 @@ __device__ __forceinline__ float cc_scale(const ConvCursor& c, uint32_t rank, in
   const int b = c.kt * 4 + 2 * static_cast<int>(rank) + j;
   if (n >= c.N || b >= c.KB) return 0.0f;
   return __ldg(c.scales + static_cast<int64_t>(n) * c.KB + b);
+}
+
+// Forward orientation: scale of output column n = kt*256 + 128*rank + r and
+// K-block s (the stage); 0 outside the weight.
+__device__ __forceinline__ float cc_scale_fwd(const ConvCursor& c, uint32_t rank, int r) {
+  const int n = c.kt * BK + static_cast<int>(rank) * BKC + r;
+  if (n >= c.N || c.s >= c.KB) return 0.0f;
+  return __ldg(c.scales + static_cast<int64_t>(n) * c.KB + c.s);
 }
 
 
@@ -548,7 +565,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
             mbar_arrive_expect_tx(fb, bytes);
             NF4_PROBE(40, it);
           }
-          tma_load_2d(dst, map, box >= 2 ? x_box : s * BN + x_box, box >= 2 ? s * BN : row0, fb);
+          if (tl.fwd && box == 2)  // 128 rows n of this CTA's columns, the stage's 32 bytes
+            tma_load_2d(dst, map, s * (BN / 2), tl.kt * BK + static_cast<int>(rank) * BKC, fb);
+          else
+            tma_load_2d(dst, map, box >= 2 ? x_box : s * BN + x_box, box >= 2 ? s * BN : row0, fb);
         }
         if (lane == 0) NF4_PROGRESS_SET(0, it + 1);
         __syncwarp();
@@ -581,6 +601,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       const uint64_t a_desc0 = smem_desc_sw128(sbase + (L::kPreA ? kAOff : kOpOff), 16, kSbo);
       const uint64_t b_desc0 = smem_desc_sw128(sbase + kOpOff + L::kBInOp, kBLbo, kSbo);
       constexpr uint32_t kBStep = (2u * kSbo) >> 4;  // +2 n-groups per MMA K-step
+      // Forward tiles: B is K-major like A (128 rows n per CTA, 128-byte
+      // swizzle), +32 bytes per MMA K-step.
+      constexpr uint32_t idesc_fwd = idesc_f16_f32(2 * BM, BK, 0, /*B K-major*/ 0);
+      const uint64_t b_desc0_fwd = smem_desc_sw128(sbase + kOpOff + L::kBInOp, 16, kSbo);
       const uint32_t ready0 = sbase + kReadyOff;
       uint32_t it = 0, lt = 0, slot = 0, aslot = 0;
       uint32_t avail = 0;  // stages the watcher has published as ready
@@ -591,6 +615,9 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         const Tile tl = tile_at(single, batch, count, w.t);
         const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
         const uint32_t acc = lt % kAccBufs;
+        const uint32_t id = tl.fwd ? idesc_fwd : idesc;
+        const uint64_t bdesc = tl.fwd ? b_desc0_fwd : b_desc0;
+        const uint32_t bstep = tl.fwd ? 2u : kBStep;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(tmem_empty(acc),
                                                        ((lt / kAccBufs) & 1u) ^ 1u, abort_flag))) {
           ok = false;
@@ -623,17 +650,17 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           const uint64_t off = static_cast<uint64_t>((slot * kOpSlotBytes) >> 4);
           const uint64_t a =
               a_desc0 + (L::kPreA ? static_cast<uint64_t>((aslot * kASlotBytes) >> 4) : off);
-          const uint64_t b = b_desc0 + off;
+          const uint64_t b = bdesc + off;
           if (elect_one()) {
             // A: +32 bytes per 16 f16 along the swizzled row; B: +2 n-groups.
 #pragma unroll
             for (int mb = 0; mb < kMBlocks; ++mb) {
               const uint32_t dm = d_tmem + static_cast<uint32_t>(mb * BK);
               const uint64_t am = a + static_cast<uint64_t>((mb * kABytes) >> 4);
-              tc_mma_f16_pair(dm, am, b, idesc, s != w.s0 ? 1u : 0u);
-              tc_mma_f16_pair(dm, am + 2u, b + kBStep, idesc, 1u);
-              tc_mma_f16_pair(dm, am + 4u, b + 2u * kBStep, idesc, 1u);
-              tc_mma_f16_pair(dm, am + 6u, b + 3u * kBStep, idesc, 1u);
+              tc_mma_f16_pair(dm, am, b, id, s != w.s0 ? 1u : 0u);
+              tc_mma_f16_pair(dm, am + 2u, b + bstep, id, 1u);
+              tc_mma_f16_pair(dm, am + 4u, b + 2u * bstep, id, 1u);
+              tc_mma_f16_pair(dm, am + 6u, b + 3u * bstep, id, 1u);
             }
             tc_commit_pair(empty_op(slot), 0x3);
             if constexpr (L::kPreA) tc_commit_pair(empty_a(aslot), 0x3);
@@ -768,6 +795,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     const uint32_t aswz = static_cast<uint32_t>(ar & 7);
     const uint32_t bswz = static_cast<uint32_t>(bn & 7);
     const uint32_t qchunk = ((2u * bj + bh) ^ ((static_cast<uint32_t>(bn) >> 1) & 3u)) << 4;
+    // Forward orientation: thread (row fr of the CTA's 128 columns n, half fh
+    // of the stage's 64 k) -> 16-byte chunks 4*fh .. +3 of the K-major row fr.
+    const int fr = ct & (BKC - 1);
+    const int fh = ct >> 7;
     // CTA 1: where this warp's stage-completion copy goes in CTA 0.
     const uint32_t gw = static_cast<uint32_t>(ct >> 5);  // warp within the group
     const uint32_t full_op_leader0 = mapa_shared(full_op(0), 0);
@@ -782,7 +813,9 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     bool cur_valid = nxt.t >= 0;
     bool cur_f32 = nxt.f32;
     bool cur_stma = nxt.stma;
-    float scale_cur = cur_valid && !cur_stma ? cc_scale(nxt, rank, bj, bn) : 0.0f;
+    bool cur_fwd = nxt.fwd;
+    float scale_cur = !cur_valid || cur_stma ? 0.0f
+                      : (cur_fwd ? cc_scale_fwd(nxt, rank, fr) : cc_scale(nxt, rank, bj, bn));
     cc_next(nxt, sk, cluster, nclusters, single, batch, count);
     cc_next(nxt, sk, cluster, nclusters, single, batch, count);
     // This thread's scale within a raw slot's scale box (row bn, 16 bytes per row).
@@ -793,10 +826,13 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       const float scale_pre = scale_cur;
       const bool f32 = cur_f32;
       const bool stma = cur_stma;
+      const bool fwd = cur_fwd;
       cur_valid = nxt.t >= 0;
       cur_f32 = nxt.f32;
       cur_stma = nxt.stma;
-      scale_cur = cur_valid && !cur_stma ? cc_scale(nxt, rank, bj, bn) : 0.0f;
+      cur_fwd = nxt.fwd;
+      scale_cur = !cur_valid || cur_stma ? 0.0f
+                  : (cur_fwd ? cc_scale_fwd(nxt, rank, fr) : cc_scale(nxt, rank, bj, bn));
       cc_next(nxt, sk, cluster, nclusters, single, batch, count);
       cc_next(nxt, sk, cluster, nclusters, single, batch, count);
 
@@ -827,7 +863,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         for (int i = 0; i < 4; ++i)
           g[i] = *reinterpret_cast<const uint4*>(src + (((4u * ahalf + i) ^ aswz) << 4));
       }
-      const uint4 q = *reinterpret_cast<const uint4*>(raw + kGoBytes + bn * (BKC / 2) + qchunk);
+      // NF4 bytes: backward, 64-byte swizzled rows n of the tile's 128 k; forward,
+      // plain 32-byte rows (one 64-k block) of the CTA's 128 columns n.
+      const uint4 q = *reinterpret_cast<const uint4*>(
+          raw + kGoBytes + (fwd ? static_cast<uint32_t>(fr * 32 + fh * 16) : bn * (BKC / 2) + qchunk));
       const float scale = stma ? *reinterpret_cast<const float*>(raw + scale_off) : scale_pre;
       // The slot is refilled by TMA (async proxy) once released: order these
       // generic-proxy reads before that write.
@@ -864,14 +903,17 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       }
 
       // Half an NF4 block (row n = bn, k = 64*bj + 32*bh .. +31) -> four 16-byte
-      // chunks of one 128-byte swizzle row of B^T.
+      // chunks of one 128-byte swizzle row of the MN-major B^T; forward: (row n
+      // = fr, k = 32*fh .. +31) -> chunks 4*fh .. +3 of the K-major row fr.
       {
         const BlockTable tb = make_block_table(scale);
-        uint8_t* dst = b_op + bj * kBLbo + (bn >> 3) * kSbo + bswz * 128;
+        const uint32_t sw = fwd ? static_cast<uint32_t>(fr & 7) : bswz;
+        const uint32_t hh = fwd ? static_cast<uint32_t>(fh) : static_cast<uint32_t>(bh);
+        uint8_t* dst = b_op + (fwd ? (fr >> 3) * kSbo : bj * kBLbo + (bn >> 3) * kSbo) + sw * 128;
         const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<uint4*>(dst + (((4u * bh + e) ^ bswz) << 4)) =
+          *reinterpret_cast<uint4*>(dst + (((4u * hh + e) ^ sw) << 4)) =
               dequant_word(words[e], tb);
       }
       if (probe) NF4_PROBE(48 + cw, it);
@@ -1405,6 +1447,41 @@ static int fill_desc_pre(ProblemDesc* d, const uint16_t* go_f16, const float* sc
                         rows_per_tile);
 }
 
+// Descriptor of the forward product C[M x N] = A[M x K] @ dequant(B_nf4[K x N])
+// on the pre-converted kernel: the A map reads the f16 copy of A (box 64
+// columns k x 128 rows), the NF4 map boxes 128 rows n x 32 bytes (one 64-k
+// block), the output map is C.  The block scales are loaded by the converters.
+static int fill_desc_fwd(ProblemDesc* d, const uint16_t* a_f16, const float* scales,
+                         const uint8_t* data, float* C, int M, int N, int K, int rows_per_tile) {
+  std::memset(d, 0, sizeof(*d));
+  const int epi_cols = rows_per_tile == LayoutPreA2::kRowsPerTile ? LayoutPreA2::kEpiCols
+                                                                  : LayoutPreA::kEpiCols;
+  if (!encode_2d(&d->tm_go, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a_f16, static_cast<uint64_t>(K),
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(f16_pitch(K)) * 2, BN, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&d->tm_nf4, CU_TENSOR_MAP_DATA_TYPE_UINT8, data, static_cast<uint64_t>(K / 2),
+                 static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), BN / 2, BKC,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&d->tm_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, static_cast<uint64_t>(N),
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(N) * 4,
+                 static_cast<uint32_t>(epi_cols), 32,
+                 epi_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+    return NF4_ERR_CUDA;
+  d->scales = scales;
+  d->grad_A = C;
+  d->M = M;
+  d->N = N;
+  d->K = K;
+  d->dtype = NF4_BF16;  // not read by this variant
+  d->tiles_m = (M + rows_per_tile - 1) / rows_per_tile;
+  d->tiles_k = (N + BK - 1) / BK;
+  d->n_stages = K / BN;
+  d->tile_begin = 0;
+  d->scale_tma = 0;
+  d->fwd = 1;
+  return NF4_OK;
+}
+
 static int sm_count(int* out) {
   static int cached[64] = {};
   int dev = 0;
@@ -1850,6 +1927,56 @@ extern "C" int nf4_split_item(int tiles, int stages, int pairs, int pair, int k,
   return 1;
 }
 
+namespace nf4 {
+// One problem on the pre-converted kernel, its descriptor d filled: the split
+// plan of a last partial wave (when the workspace holds its flags and partial
+// sums), the f16 pre-pass of the A operand a (M rows x R, R the shared
+// dimension) into the workspace unless it is f16 already, and the launch.
+static int launch_pre_single(ProblemDesc& d, const void* a, int a_dtype, int M, int R,
+                             void* workspace, size_t workspace_bytes, bool tiles512,
+                             cudaStream_t stream) {
+  const bool f16_in = a_dtype == NF4_F16;
+  const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
+  if (tiles > INT_MAX) return NF4_ERR_INVALID;
+  // The split needs its flags and partial sums after the f16 copy; a workspace
+  // holding only the copy runs every tile whole.  The plan is made for the
+  // number of pairs the chosen kernel runs at once (its launch uses them all).
+  int pairs = 0;
+  int rc = tiles512 ? max_clusters<LayoutPreA2>(&pairs) : max_clusters<LayoutPreA>(&pairs);
+  if (rc != NF4_OK) return rc;
+  const size_t base = round256(f16_bytes(M, R));
+  SkArgs sk;
+  std::memset(&sk, 0, sizeof(sk));
+  unsigned int* flags = nullptr;
+  int nflags = 0;
+  if (workspace_bytes >= base + sk_bytes(pairs)) {
+    plan_split(static_cast<int>(tiles), d.n_stages, pairs, &sk);
+    if (sk.sk_tiles > 0) {
+      uint8_t* w = static_cast<uint8_t*>(workspace) + base;
+      flags = reinterpret_cast<unsigned int*>(w);
+      nflags = pairs;
+      sk.flags = flags;
+      sk.partials = reinterpret_cast<float*>(w + round256(sizeof(unsigned int) * pairs));
+    }
+  }
+  if (f16_in) {
+    // No pre-pass: zero the split flags on the stream instead.
+    if (nflags > 0 &&
+        cudaMemsetAsync(flags, 0, sizeof(unsigned int) * nflags, stream) != cudaSuccess)
+      return NF4_ERR_CUDA;
+  } else {
+    rc = launch_to_f16(a, a_dtype, static_cast<uint16_t*>(workspace), M, R, flags, nflags, stream);
+    if (rc != NF4_OK) return rc;
+  }
+  const SkArgs* skp = sk.sk_tiles > 0 ? &sk : nullptr;
+  if (tiles512)
+    return launch_layout<LayoutPreA2>(d, nullptr, 1, static_cast<int>(tiles), skp, stream,
+                                      /*pdl=*/!f16_in);
+  return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles), skp, stream,
+                                   /*pdl=*/!f16_in);
+}
+}  // namespace nf4
+
 extern "C" size_t nf4_backward_a_ws_bytes(int M, int N) {
   if (M <= 0 || N <= 0) return 0;
   int pairs = 0;
@@ -1879,53 +2006,44 @@ extern "C" int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float
   int pairs = 0;
   rc = max_clusters<LayoutPreA>(&pairs);
   if (rc != NF4_OK) return rc;
-  const size_t base = round256(f16_bytes(M, N));
-  const bool can_split = workspace_bytes >= base + sk_bytes(pairs);
+  const bool can_split = workspace_bytes >= round256(f16_bytes(M, N)) + sk_bytes(pairs);
   const bool tiles512 = use_tiles512(M, N, K, pairs, can_split);
   ProblemDesc d;
   rc = fill_desc_pre(&d, go_f16, scales, data, grad_A, M, N, K,
                      tiles512 ? LayoutPreA2::kRowsPerTile : LayoutPreA::kRowsPerTile);
   if (rc != NF4_OK) return rc;
-  const int64_t tiles = static_cast<int64_t>(d.tiles_m) * d.tiles_k;
-  if (tiles > INT_MAX) return NF4_ERR_INVALID;
-  // The split needs its flags and partial sums after the f16 copy; a workspace
-  // holding only the copy runs every tile whole.  The plan is made for the
-  // number of pairs the chosen kernel runs at once (its launch uses them all).
-  if (tiles512) {
-    rc = max_clusters<LayoutPreA2>(&pairs);
-    if (rc != NF4_OK) return rc;
-  }
-  SkArgs sk;
-  std::memset(&sk, 0, sizeof(sk));
-  unsigned int* flags = nullptr;
-  int nflags = 0;
-  if (can_split && workspace_bytes >= base + sk_bytes(pairs)) {
-    plan_split(static_cast<int>(tiles), d.n_stages, pairs, &sk);
-    if (sk.sk_tiles > 0) {
-      uint8_t* w = static_cast<uint8_t*>(workspace) + base;
-      flags = reinterpret_cast<unsigned int*>(w);
-      nflags = pairs;
-      sk.flags = flags;
-      sk.partials = reinterpret_cast<float*>(w + round256(sizeof(unsigned int) * pairs));
-    }
-  }
-  if (f16_in) {
-    // No pre-pass: zero the split flags on the stream instead.
-    if (nflags > 0 && cudaMemsetAsync(flags, 0, sizeof(unsigned int) * nflags,
-                                      as_stream(stream)) != cudaSuccess)
-      return NF4_ERR_CUDA;
-  } else {
-    rc = launch_to_f16(grad_out, go_dtype, static_cast<uint16_t*>(workspace), M, N, flags, nflags,
-                       as_stream(stream));
-    if (rc != NF4_OK) return rc;
-  }
-  if (tiles512)
-    return launch_layout<LayoutPreA2>(d, nullptr, 1, static_cast<int>(tiles),
-                                      sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream),
-                                      /*pdl=*/!f16_in);
-  return launch_layout<LayoutPreA>(d, nullptr, 1, static_cast<int>(tiles),
-                                   sk.sk_tiles > 0 ? &sk : nullptr, as_stream(stream),
-                                   /*pdl=*/!f16_in);
+  return launch_pre_single(d, grad_out, go_dtype, M, N, workspace, workspace_bytes, tiles512,
+                           as_stream(stream));
+}
+
+extern "C" size_t nf4_forward_ws_bytes(int M, int K) { return nf4_backward_a_ws_bytes(M, K); }
+
+extern "C" int nf4_forward_ws(const void* A, int a_dtype, const float* scales, const uint8_t* data,
+                              float* C, int M, int N, int K, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (a_dtype != NF4_F32 && a_dtype != NF4_BF16 && a_dtype != NF4_F16) return NF4_ERR_INVALID;
+  if (M < 0 || N < 0 || K <= 0 || K % 64 != 0) return NF4_ERR_INVALID;
+  if (M == 0 || N == 0) return NF4_OK;
+  if (A == nullptr || scales == nullptr || data == nullptr || C == nullptr) return NF4_ERR_INVALID;
+  if (N % 4 != 0) return NF4_ERR_INVALID;  // C rows are 16-byte strided for the TMA stores
+  if (!aligned(A, 16) || !aligned(data, 16) || !aligned(scales, 4) || !aligned(C, 16))
+    return NF4_ERR_ALIGN;
+  const bool f16_in = a_dtype == NF4_F16;
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < f16_bytes(M, K))
+    return NF4_ERR_WORKSPACE;
+  const uint16_t* a_f16 = f16_in ? static_cast<const uint16_t*>(A) : static_cast<uint16_t*>(workspace);
+  int pairs = 0;
+  int rc = max_clusters<LayoutPreA>(&pairs);
+  if (rc != NF4_OK) return rc;
+  const bool can_split = workspace_bytes >= round256(f16_bytes(M, K)) + sk_bytes(pairs);
+  // The shared dimension is K and the output columns are N.
+  const bool tiles512 = use_tiles512(M, K, N, pairs, can_split);
+  ProblemDesc d;
+  rc = fill_desc_fwd(&d, a_f16, scales, data, C, M, N, K,
+                     tiles512 ? LayoutPreA2::kRowsPerTile : LayoutPreA::kRowsPerTile);
+  if (rc != NF4_OK) return rc;
+  return launch_pre_single(d, A, a_dtype, M, K, workspace, workspace_bytes, tiles512,
+                           as_stream(stream));
 }
 
 extern "C" size_t nf4_backward_a_batched_workspace(int count) {

@@ -145,6 +145,31 @@ int nf4_backward_a_ws(const void* grad_out, int go_dtype, const float* scales,
                       size_t workspace_bytes, void* stream);
 
 /*
+ * The forward product C[M x N] = A[M x K] @ dequant(B_nf4[K x N]), contracted
+ * over K (page above, module header: the backward kernel is described there as
+ * the transposed counterpart of a forward NF4 tensor-core GEMM over the same
+ * NF4 layout: data [N][K/2], scales [N][K/64]).  Same arithmetic as
+ * the backward: A rounded to f16 (RNE), dequant(B)[k,n] =
+ * f16(f32(scale[n][k/64] * codebook[code])), f32 accumulation, C overwritten.
+ * Two launches on `stream`, as nf4_backward_a_ws: an f16 pre-pass of A into
+ * `workspace` (none for NF4_F16 A), then the pair kernel with the dequantised
+ * weight as its K-major B operand (256 columns n per pair tile, 64 k per
+ * stage).  No counterpart kernel on the pages.
+ *   A       [M*K] of type a_dtype (NF4_F32, NF4_BF16 or NF4_F16), 16-byte aligned
+ *   data    [N][K/2] bytes, 16-byte aligned; scales [N][K/64] fp32, 4-byte aligned
+ *   C       [M*N] fp32, 16-byte aligned, N % 4 == 0 (its rows are TMA-stored)
+ *   K       positive multiple of 64; M == 0 or N == 0 enqueue nothing
+ *   workspace, workspace_bytes: as nf4_backward_a_ws, at least
+ *           nf4_forward_ws_bytes(M, K) bytes for the split of a last partial
+ *           wave, at least the f16 copy (2 * M * K bytes) in any case
+ * Returns NF4_ERR_INVALID, NF4_ERR_ALIGN or NF4_ERR_WORKSPACE (nothing
+ * enqueued) for arguments outside these rules.
+ */
+size_t nf4_forward_ws_bytes(int M, int K);
+int nf4_forward_ws(const void* A, int a_dtype, const float* scales, const uint8_t* data, float* C,
+                   int M, int N, int K, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Tokens per pair tile, 256 or 512, that the pre-converted kernel uses for an
  * M x N x K problem run by `pairs` pairs of CTAs (pure host computation).  A
  * 512-token tile issues two M = 256 MMA blocks against each dequantised B^T

@@ -49,6 +49,8 @@ def lib():
                                            C.c_int, vp, vp]
         L.nf4o_backward_a.argtypes = [vp, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int,
                                       vp, vp]
+        L.nf4o_forward_rows.argtypes = [vp, vp, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp]
+        L.nf4o_forward.argtypes = [vp, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, vp, vp]
         L.nf4o_set_threads.argtypes = [C.c_int]
         L.nf4o_set_threads.restype = None
         L.nf4o_max_threads.restype = C.c_int
@@ -158,4 +160,37 @@ def backward_a(go: np.ndarray, dtype: int, scales: np.ndarray, data: np.ndarray,
     rc = lib().nf4o_backward_a(_p(go), dtype, _p(scales), _p(data), M, N, K, _p(ref),
                                _p(bound) if want_bound else None)
     _check(rc, "backward_a")
+    return ref, bound
+
+
+def forward_rows(a16: np.ndarray, bt: np.ndarray, rows, want_bound: bool = True):
+    """fp64 rows of the forward product C = f16(A) @ deq(B) from f16 operands:
+    a16 [M, K], bt = deq(B) transposed [N, K]."""
+    a16 = np.ascontiguousarray(a16, dtype=np.uint16)
+    bt = np.ascontiguousarray(bt, dtype=np.uint16)
+    M, K = a16.shape
+    N, K2 = bt.shape
+    assert K == K2
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    ref = np.empty((rows.size, N), dtype=np.float64)
+    bound = np.empty((rows.size, N), dtype=np.float64) if want_bound else None
+    rc = lib().nf4o_forward_rows(_p(a16), _p(bt), M, N, K, _p(rows), rows.size, _p(ref),
+                                 _p(bound) if want_bound else None)
+    _check(rc, "forward_rows")
+    return ref, bound
+
+
+def forward(a: np.ndarray, dtype: int, scales: np.ndarray, data: np.ndarray, N: int,
+            want_bound: bool = True):
+    """Whole forward product C [M, N] = f16(A)[M, K] @ deq(B)[K, N] in fp64
+    (and the |.|-sum bound) from raw inputs (A fp32, or bf16 as uint16 bits)."""
+    a = np.ascontiguousarray(a, dtype=np.float32 if dtype == F32 else np.uint16)
+    M, K = a.shape
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    data = np.ascontiguousarray(data, dtype=np.uint8)
+    ref = np.empty((M, N), dtype=np.float64)
+    bound = np.empty((M, N), dtype=np.float64) if want_bound else None
+    rc = lib().nf4o_forward(_p(a), dtype, _p(scales), _p(data), M, N, K, _p(ref),
+                            _p(bound) if want_bound else None)
+    _check(rc, "forward")
     return ref, bound

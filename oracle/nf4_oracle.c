@@ -280,6 +280,60 @@ int nf4o_backward_a(const void* go, int dtype, const float* scales,
     return rc;
 }
 
+/* Forward product C[M x N] = A[M x K] @ deq(B)[K x N] (the module header of
+ * [P1] names this forward kernel as the one the backward is the transposed
+ * counterpart of; shared dimension K).  The operands are rounded as in the
+ * backward ([P1] PHASE 1 and 2), and each C[m][n] is summed over k in order in
+ * fp64.  bt = deq(B) transposed, f16 bits [N x K] (nf4o_dequantize_f16), so
+ * C[m][n] is the dot product of row m of A16 with row n of bt. */
+int nf4o_forward_rows(const uint16_t* a16, const uint16_t* bt, int M, int N, int K,
+                      const int* rows, int nrows, double* ref, double* bound) {
+    if (!a16 || !bt || !rows || !ref || M < 0 || N <= 0 || K <= 0 || nrows < 0)
+        return -1;
+    for (int i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= M) return -2;
+    double* f16v = (double*)malloc(sizeof(double) * 65536);
+    if (!f16v) return -3;
+    for (int h = 0; h < 65536; ++h) f16v[h] = nf4o_f16_to_f64((uint16_t)h);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < nrows; ++i) {
+        const uint16_t* arow = a16 + (long long)rows[i] * K;
+        for (int n = 0; n < N; ++n) {
+            const uint16_t* brow = bt + (long long)n * K;
+            double acc = 0.0, mag = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const double p = f16v[arow[k]] * f16v[brow[k]];
+                acc += p;
+                mag += fabs(p);
+            }
+            ref[(long long)i * N + n] = acc;
+            if (bound) bound[(long long)i * N + n] = mag;
+        }
+    }
+    free(f16v);
+    return 0;
+}
+
+int nf4o_forward(const void* a, int dtype, const float* scales, const uint8_t* data,
+                 int M, int N, int K, double* ref, double* bound) {
+    if (!a || !scales || !data || !ref || M < 0 || N <= 0 || K <= 0 || K % 64 != 0)
+        return -1;
+    uint16_t* a16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)M * (size_t)K + 2);
+    uint16_t* bt = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)N * (size_t)K);
+    int* rows = (int*)malloc(sizeof(int) * (size_t)M + sizeof(int));
+    int rc = -3;
+    if (a16 && bt && rows) {
+        rc = nf4o_round_operand(a, dtype, (long long)M * K, a16);
+        if (rc == 0) rc = nf4o_dequantize_f16(scales, data, K, N, bt);
+        for (int i = 0; i < M; ++i) rows[i] = i;
+        if (rc == 0) rc = nf4o_forward_rows(a16, bt, M, N, K, rows, M, ref, bound);
+    }
+    free(a16);
+    free(bt);
+    free(rows);
+    return rc;
+}
+
 void nf4o_set_threads(int n) {
 #ifdef _OPENMP
     if (n > 0) omp_set_num_threads(n);

@@ -76,6 +76,17 @@ int nf4o_backward_a(const void* go, int dtype, const float* scales,
                     const uint8_t* data, int M, int N, int K,
                     double* ref, double* bound);
 
+/* Forward product: ref[i][n] = sum_k f16(A)[rows[i], k] * deq(B)[k, n], in
+ * fp64, k ascending; bound[i][n] the same over |products| (may be NULL).  a16
+ * is [M][K] f16 bits, bt is deq(B) transposed, [N][K] f16 bits. */
+int nf4o_forward_rows(const uint16_t* a16, const uint16_t* bt, int M, int N, int K,
+                      const int* rows, int nrows, double* ref, double* bound);
+
+/* Whole forward problem from raw inputs (A fp32 or bf16 bits, [M][K]); ref and
+ * bound are [M][N]; bound may be NULL. */
+int nf4o_forward(const void* a, int dtype, const float* scales, const uint8_t* data,
+                 int M, int N, int K, double* ref, double* bound);
+
 /* OpenMP thread control for the row loops (1 when built without OpenMP). */
 void nf4o_set_threads(int n);
 int nf4o_max_threads(void);

@@ -313,3 +313,63 @@ def test_oracle_rejects_bad_arguments():
     bt = np.zeros((8, 64), dtype=np.uint16)
     with pytest.raises(ValueError):
         oracle.backward_a_rows(go16, bt, [4])  # row out of range
+
+
+# ---------------------------------------------------------------- forward product
+def _fwd_case(M, N, K, dtype=F32, seed=23):
+    """A [M, K] and an NF4 weight B [K, N]: the forward product's inputs (the
+    backward's generators with the roles of N and K swapped for A)."""
+    p = Problem(M, K, N, dtype, 1.0, 0.02, False, seed)
+    a = make_grad_out(p)  # [M, K]
+    w = make_weight(Problem(M, N, K, dtype, 1.0, 0.02, False, seed + 1))  # [K, N]
+    data, scales = oracle.quantize(w)
+    return a, data, scales
+
+
+def test_forward_bruteforce_exact_8x16x64():
+    """Exact rational sum over k of the f16 operand products vs the fp64 oracle."""
+    M, N, K = 8, 16, 64
+    a, data, scales = _fwd_case(M, N, K)
+    ref, bound = oracle.forward(a, F32, scales, data, N)
+    a16 = oracle.round_operand(a, F32).view(np.float16).astype(np.float64)
+    bt = oracle.dequantize_f16(scales, data, K, N).view(np.float16).astype(np.float64)
+    for m in range(M):
+        for n in range(N):
+            prods = [Fraction(a16[m, k]) * Fraction(bt[n, k]) for k in range(K)]
+            assert abs(ref[m, n] - float(sum(prods))) <= 1e-15 * bound[m, n] + 1e-300
+            assert bound[m, n] == pytest.approx(float(sum(abs(x) for x in prods)), rel=1e-15)
+
+
+def test_forward_matches_torch_fp64_matmul():
+    for dtype in (F32, BF16):
+        M, N, K = 24, 80, 256
+        a, data, scales = _fwd_case(M, N, K, dtype, seed=29)
+        ref, _ = oracle.forward(a, dtype, scales, data, N, want_bound=False)
+        a16 = oracle.round_operand(a, dtype).view(np.float16).astype(np.float64)
+        deq = oracle.dequantize_f16(scales, data, K, N).view(np.float16).astype(np.float64).T
+        want = torch.from_numpy(a16) @ torch.from_numpy(np.ascontiguousarray(deq))  # [M,K]@[K,N]
+        np.testing.assert_allclose(ref, want.numpy(), rtol=1e-12, atol=1e-300)
+
+
+def test_forward_one_hot_rows_recover_dequantised_rows():
+    """A row e_k picks row k of deq(B) [K x N]: C[m, n] = deq(B)[k, n] exactly,
+    across block (64) and tile boundaries and odd and even k."""
+    M, N, K = 1, 96, 320
+    _, data, scales = _fwd_case(M, N, K, seed=31)
+    bt = oracle.dequantize_f16(scales, data, K, N).view(np.float16).astype(np.float64)
+    ks = [0, 1, 62, 63, 64, 65, 127, 128, 255, 256, 319]
+    a = np.zeros((len(ks), K), dtype=np.float32)
+    for i, k in enumerate(ks):
+        a[i, k] = 1.0
+    ref, _ = oracle.forward(a, F32, scales, data, N)
+    for i, k in enumerate(ks):
+        np.testing.assert_array_equal(ref[i], bt[:, k])
+
+
+def test_forward_rows_entry_matches_full():
+    a, data, scales = _fwd_case(17, 32, 128, seed=37)
+    ref, bound = oracle.forward(a, F32, scales, data, 32)
+    r, b = oracle.forward_rows(oracle.round_operand(a, F32),
+                               oracle.dequantize_f16(scales, data, 128, 32), [0, 9, 16])
+    np.testing.assert_array_equal(r, ref[[0, 9, 16]])
+    np.testing.assert_array_equal(b, bound[[0, 9, 16]])
