@@ -52,6 +52,17 @@ def workloads() -> dict[str, list[Problem]]:
     return w
 
 
+# Forward product C[M x N] = A[M x K] @ dequant(B_nf4[K x N]) (nf4_forward_ws):
+# the same projections in the forward direction.  (M, N out, K in, A dtype,
+# A std, B std, outliers, seed)
+FWD_WORKLOADS = {
+    "fwd_q_proj": (2048, 1536, 1536, F32, 1e-2, 0.02, False, 0),
+    "fwd_up_proj": (4096, 8960, 1536, BF16, 1e-2, 0.02, True, 0),
+    "fwd_down_proj": (4096, 1536, 8960, BF16, 1e-2, 0.02, True, 2),
+    "fwd_large": (8191, 14336, 4096, F32, 1.0, 0.015, False, 0),
+}
+
+
 def describe(name: str, probs: list[Problem]) -> str:
     if len(probs) == 1:
         p = probs[0]
@@ -293,6 +304,92 @@ def bench_ours(args, rank, world, dev):
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(probs, budget_s=args.cpu_seconds)
     return line
+
+
+def bench_forward(args, dev):
+    """The forward product through nf4_forward_ws on rotating input sets beyond
+    L2 (a CUDA graph of one step per set), its GEMM kernel alone (f16 A left in
+    each set's workspace by the steps), the tensor roofline and the clocks."""
+    import backward_gemm_gb300 as nb
+    from backward_gemm_gb300.build import build
+
+    build()
+    nb.lib()
+    M, N, K, dt, a_std, b_std, outl, seed = FWD_WORKLOADS[args.workload]
+    a_np = make_grad_out(Problem(M, K, N, dt, a_std, b_std, outl, seed))      # A [M, K]
+    B_np = make_weight(Problem(M, N, K, dt, a_std, b_std, outl, seed + 1))    # B [K, N]
+    a_bytes = M * K * (4 if dt == F32 else 2)
+    per_set = a_bytes + 4 * M * N + K * N // 2 + 2 * M * K
+    copies = max(2, min(16, -(-2 * L2_BYTES // per_set)))
+    sets = []
+    for _ in range(copies):
+        a_t = (torch.from_numpy(a_np).to(dev) if dt == F32
+               else torch.from_numpy(a_np.view(np.int16)).to(dev).view(torch.bfloat16))
+        w = nb.quantize(torch.from_numpy(B_np).to(dev))
+        sets.append((a_t, w, torch.empty((M, N), device=dev), nb.fwd_workspace(M, K, dev)))
+    stream = torch.cuda.Stream(device=dev)
+    steps = args.steps
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            a_t, w, c, ws = sets[i % copies]
+            nb.forward_ws(a_t, w, ws, out=c)
+        nb.check_error()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for a_t, w, c, ws in sets:
+                nb.forward_ws(a_t, w, ws, out=c)
+        graph.replay()
+        stream.synchronize()
+        full, rem = divmod(steps, copies)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index) as clocks:
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                a_t, w, c, ws = sets[i]
+                nb.forward_ws(a_t, w, ws, out=c)
+            ev1.record(stream)
+            ev1.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        # The GEMM alone: its f16 A is in each set's workspace after the steps.
+        runs = [(ws[: 2 * M * K].view(torch.float16).view(M, K), w, c, ws) for _, w, c, ws in sets]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(steps):
+            a16, w, c, ws = runs[i % copies]
+            nb.forward_ws(a16, w, ws, out=c)
+        e1.record(stream)
+        e1.synchronize()
+        kern_ms = e0.elapsed_time(e1) / steps
+        nb.check_error()
+    flops = 2 * M * N * K
+    alg_bytes = a_bytes + K * N // 2 + 4 * N * (K // 64) + 4 * M * N
+    peaks, peak_kind = load_peaks()
+    peak_tf = peaks["bf16_tflops_sustained" if ms > 1000.0 else "bf16_tflops"]
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    return {
+        "metric": "NF4 forward GEMM (C = A @ dequant(B)) TFLOP/s and % of GB300 dense FP16 tensor roofline",
+        "value": flops * steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 operands, f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: M={M} N={N} K={K} A {DTYPE_NAMES[dt]}",
+                   "gflop_per_step": flops / 1e9, "algorithmic_mb_per_step": alg_bytes / 1e6,
+                   "l2": f"rotating {copies} input sets, {copies * per_set / 2**20:.0f} MiB > L2",
+                   "timing": f"CUDA graph of {copies} steps, CUDA events",
+                   "entry": "nf4_forward_ws", "parallelism": "dp1 (M-sharded replicas, no collective)"},
+        "e2e": None,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None,
+                     "peak_source": f"{peak_kind} bf16 (f16 nominal rate = bf16)",
+                     "kernel": "bwd_a_kernel (forward orientation)", "kernel_ms": kern_ms,
+                     "timed": "GEMM alone (f16 A entry, CUDA events, same rotating sets)"},
+        "gpu_launches": steps * 2,
+        "clocks": clocks.summary(),
+    }
 
 
 SMALL_M_MAX = 64      # the library's default few-token limit (nf4_set_small_m_max)
@@ -539,7 +636,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="q_proj", choices=sorted(workloads()))
+    ap.add_argument("--workload", default="q_proj", choices=sorted(workloads()) + sorted(FWD_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--entry", default="ws", choices=["plain", "ws"],
                     help="single-problem entry point: nf4_backward_a_ex, or nf4_backward_a_ws "
@@ -557,7 +654,14 @@ def main():
 
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
-    if args.impl == "reference":
+    if args.workload in FWD_WORKLOADS:
+        if args.impl == "reference" or world > 1:
+            line = {"impl": args.impl, "unavailable": "forward workloads run on one GPU, ours arm only"}
+        else:
+            dev = torch.device("cuda", local)
+            torch.cuda.set_device(dev)
+            line = bench_forward(args, dev)
+    elif args.impl == "reference":
         line = bench_reference(args, rank, world)
     else:
         dev = torch.device("cuda", local)
