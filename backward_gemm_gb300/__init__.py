@@ -49,6 +49,8 @@ SIGNATURES = {
     "nf4_backward_a_ws_bytes": (_sz, [_i, _i]),
     "nf4_backward_a_ws": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
     "nf4_forward_ws_bytes": (_sz, [_i, _i]),
+    "rms_norm_backward_ws_bytes": (_sz, [_i, _i]),
+    "rms_norm_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _sz, _vp]),
     "nf4_forward_ws": (_i, [_vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp]),
     "nf4_tile_rows": (_i, [_i, _i, _i, _i, _i]),
     "nf4_set_tile_rows": (_i, [_i]),
@@ -283,6 +285,36 @@ def forward_ws(A: torch.Tensor, w: NF4Weight, workspace: torch.Tensor | None = N
                                 M, w.N, K, _ptr(workspace), nbytes, _stream()),
            "nf4_forward_ws")
     return out
+
+
+def rms_norm_backward(x: torch.Tensor, gamma: torch.Tensor, rms: torch.Tensor,
+                      grad_y: torch.Tensor, want_gamma: bool = True,
+                      workspace: torch.Tensor | None = None, out: torch.Tensor | None = None):
+    """Backward of RMS layer normalisation through ``rms_norm_backward``:
+    x, grad_y float32 [rows, H], gamma float32 [H], rms float32 [rows] (the
+    forward's sqrt(mean(x^2) + eps)).  Returns (grad_x [rows, H], grad_gamma
+    [H] or None)."""
+    for name, t in (("x", x), ("gamma", gamma), ("rms", rms), ("grad_y", grad_y)):
+        _require_cuda_contig(name, t)
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    rows, H = x.shape
+    if tuple(grad_y.shape) != (rows, H) or tuple(gamma.shape) != (H,) or tuple(rms.shape) != (rows,):
+        raise ValueError("shapes: x, grad_y [rows, H], gamma [H], rms [rows]")
+    if out is None:
+        out = torch.empty_like(x)
+    dgamma = torch.empty(H, dtype=torch.float32, device=x.device) if want_gamma else None
+    nbytes = 0
+    if want_gamma:
+        if workspace is None:
+            n = int(lib().rms_norm_backward_ws_bytes(rows, H))
+            workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=x.device)
+        nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().rms_norm_backward(_ptr(x), _ptr(gamma), _ptr(rms), _ptr(grad_y), _ptr(out),
+                                   _ptr(dgamma) if want_gamma else None, rows, H,
+                                   _ptr(workspace) if want_gamma else None, nbytes, _stream()),
+           "rms_norm_backward")
+    return out, dgamma
 
 
 def fwd_workspace(M: int, K: int, device=None) -> torch.Tensor:

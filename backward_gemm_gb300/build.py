@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnf4bwd.so")
 
-SOURCES = ["nf4_quant.cu", "nf4_gemm.cu"]
+SOURCES = ["nf4_quant.cu", "nf4_gemm.cu", "rms_norm_bwd.cu"]
 HEADERS = ["ptx.cuh", "nf4_dequant.cuh", "nf4_common.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,

@@ -392,6 +392,92 @@ def bench_forward(args, dev):
     }
 
 
+# Backward of RMS layer normalisation (rms_norm_backward), the step upstream of
+# the projections' backward: rows = tokens, hidden = the model width.
+RMSNORM_WORKLOADS = {"rmsnorm_bwd": (4096, 1536)}
+
+
+def bench_rmsnorm(args, dev):
+    """rms_norm_backward (dL/dx and dL/dgamma) on rotating input sets beyond L2;
+    HBM roofline of its algorithmic bytes (x and g read, dL/dx written, r,
+    gamma and dL/dgamma)."""
+    import backward_gemm_gb300 as nb
+    from backward_gemm_gb300.build import build
+
+    build()
+    nb.lib()
+    rows, H = RMSNORM_WORKLOADS[args.workload]
+    gen = torch.Generator().manual_seed(0)
+    x = torch.randn(rows, H, generator=gen)
+    gy = torch.randn(rows, H, generator=gen) * 1e-2
+    gamma = 1.0 + 0.1 * torch.randn(H, generator=gen)
+    rms = torch.sqrt((x.double() ** 2).mean(dim=1) + 1e-6).float()
+    per_set = 12 * rows * H
+    copies = max(2, min(16, -(-2 * L2_BYTES // per_set)))
+    ws = torch.empty(max(int(nb.lib().rms_norm_backward_ws_bytes(rows, H)), 16),
+                     dtype=torch.uint8, device=dev)
+    sets = [(x.to(dev), gamma.to(dev), rms.to(dev), gy.to(dev), torch.empty(rows, H, device=dev),
+             torch.empty(H, device=dev)) for _ in range(copies)]
+    L = nb.lib()
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    nbytes = ws.numel()
+
+    def step(st):
+        xs, gs, rs, ys, ox, og = st
+        rc = L.rms_norm_backward(P(xs), P(gs), P(rs), P(ys), P(ox), P(og), rows, H, P(ws), nbytes,
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        if rc != 0:
+            raise RuntimeError(f"rms_norm_backward failed: {rc}")
+
+    stream = torch.cuda.Stream(device=dev)
+    steps = args.steps
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(sets[i % copies])
+        nb.check_error()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for st in sets:
+                step(st)
+        graph.replay()
+        stream.synchronize()
+        full, rem = divmod(steps, copies)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index) as clocks:
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                step(sets[i])
+            ev1.record(stream)
+            ev1.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        nb.check_error()
+    alg_bytes = 12 * rows * H + 4 * rows + 8 * H
+    gbs = alg_bytes * steps / (ms * 1e-3) / 1e9
+    peaks, peak_kind = load_peaks()
+    return {
+        "metric": "RMSNorm backward (dL/dx, dL/dgamma) GB/s and % of GB300 HBM roofline",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: rows={rows} hidden={H}",
+                   "algorithmic_mb_per_step": alg_bytes / 1e6,
+                   "l2": f"rotating {copies} input sets, {copies * per_set / 2**20:.0f} MiB > L2",
+                   "timing": f"CUDA graph of {copies} steps, CUDA events",
+                   "entry": "rms_norm_backward", "parallelism": "dp1"},
+        "e2e": None,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_kind} HBM copy",
+                     "kernel": "rows_kernel + gamma_kernel", "kernel_ms": ms / steps,
+                     "timed": "whole step (two launches)"},
+        "gpu_launches": steps * 2,
+        "clocks": clocks.summary(),
+    }
+
+
 SMALL_M_MAX = 64      # the library's default few-token limit (nf4_set_small_m_max)
 DESCS_PER_UPLOAD = 48  # descriptors per upload kernel of a grouped launch
 F16_JOBS_PER_LAUNCH = 64  # problems per grouped f16 pass (nf4_backward_a_batched_ws)
@@ -636,7 +722,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="q_proj", choices=sorted(workloads()) + sorted(FWD_WORKLOADS))
+    ap.add_argument("--workload", default="q_proj", choices=sorted(workloads()) + sorted(FWD_WORKLOADS) + sorted(RMSNORM_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--entry", default="ws", choices=["plain", "ws"],
                     help="single-problem entry point: nf4_backward_a_ex, or nf4_backward_a_ws "
@@ -654,7 +740,14 @@ def main():
 
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
-    if args.workload in FWD_WORKLOADS:
+    if args.workload in RMSNORM_WORKLOADS:
+        if args.impl == "reference" or world > 1:
+            line = {"impl": args.impl, "unavailable": "the RMSNorm workload runs on one GPU, ours arm only"}
+        else:
+            dev = torch.device("cuda", local)
+            torch.cuda.set_device(dev)
+            line = bench_rmsnorm(args, dev)
+    elif args.workload in FWD_WORKLOADS:
         if args.impl == "reference" or world > 1:
             line = {"impl": args.impl, "unavailable": "forward workloads run on one GPU, ours arm only"}
         else:

@@ -335,6 +335,33 @@ int nf4_check_error(void* stream);
  */
 int nf4_check_error_site(void* stream, unsigned int* site);
 
+/*
+ * Backward of RMS layer normalisation (page "trueno-gpu 0.4.17 --
+ * src/kernels/backward/rms_norm.rs", module doc: forward y_i = x_i * gamma_i /
+ * r per row, r = sqrt(mean(x^2) + eps) kept by the forward pass; the kernel's
+ * parameters input, gamma, rms, grad_output, grad_input, num_rows,
+ * hidden_dim).  Computes the gradient of that forward:
+ *   grad_input[row][i] = gamma_i * g_i / r - x_i * mean_j(x_j g_j gamma_j) / r^3
+ *   grad_gamma[i]      = sum over rows of g_i * x_i / r        (if grad_gamma != NULL)
+ * with g = grad_output.  The page's kernel multiplies the second term of
+ * grad_input by gamma_i too and adds eps to r^2 again; neither is done here
+ * (the page's own test criterion, agreement with finite differences, rules
+ * them out), and eps is not needed since r holds it.  Rows need not fit a warp.
+ *   input, grad_output, grad_input  [num_rows][hidden_dim] fp32, 16-byte aligned
+ *   gamma [hidden_dim] fp32, 16-byte aligned; rms [num_rows] fp32, 4-byte aligned
+ *   hidden_dim  multiple of 4, at most 8192; num_rows >= 0 (0: grad_gamma zeroed)
+ *   workspace   with grad_gamma: caller-owned device memory, 16-byte aligned, at
+ *               least rms_norm_backward_ws_bytes(num_rows, hidden_dim) bytes
+ *               (per-CTA partial sums, summed in CTA order: deterministic)
+ * Returns NF4_ERR_INVALID, NF4_ERR_ALIGN or NF4_ERR_WORKSPACE (nothing
+ * enqueued) for arguments outside these rules.
+ */
+size_t rms_norm_backward_ws_bytes(int num_rows, int hidden_dim);
+int rms_norm_backward(const float* input, const float* gamma, const float* rms,
+                      const float* grad_output, float* grad_input, float* grad_gamma,
+                      int num_rows, int hidden_dim, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,6 +16,7 @@ import ctypes as C
 
 import numpy as np
 
+from . import rms_norm  # noqa: F401  (RMS layer-norm forward/backward, fp64)
 from .build import build_oracle
 
 F32 = 0
