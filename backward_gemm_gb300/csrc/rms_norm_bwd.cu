@@ -16,7 +16,8 @@
 // row to one warp (hidden <= 32) and leaves out dL/dgamma.
 //
 // Design (HBM-bound: 12 bytes per element of a row, read x and g, write dL/dx):
-// a CTA of T threads takes rows blockIdx.x, + gridDim.x, ...; thread t owns the
+// a CTA of T threads takes rows blockIdx.x, + gridDim.x, ..., two at a time
+// (both rows' loads in flight together); thread t owns the
 // float4 columns t, t + T, ... (V of them at most), keeps gamma for them in
 // registers and the rows' dL/dgamma contributions too.  The row's dot product
 // is reduced by warp shuffles and a fixed-order sum over the warps, so results
@@ -59,7 +60,8 @@ __global__ void __launch_bounds__(T) rows_kernel(const float4* __restrict__ x,
                                                  int hidden) {
   constexpr int kWarps = T / 32;
   static_assert(kWarps <= kMaxWarps, "block size");
-  __shared__ float red[2][kWarps];
+  // [parity][row of the pair][warp]
+  __shared__ float red[2][2][kWarps];
   const int h4 = hidden >> 2;
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
@@ -71,56 +73,73 @@ __global__ void __launch_bounds__(T) rows_kernel(const float4* __restrict__ x,
     acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const float inv_h = 1.0f / static_cast<float>(hidden);
+  const int G = gridDim.x;
   int parity = 0;
-  for (int row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
-    const int64_t base = static_cast<int64_t>(row) * h4;
-    float4 xv[V], gv[V];
-    float dot = 0.0f;
+  // Two of the CTA's rows per turn (blockIdx.x + 2*i*G and + G): both rows'
+  // loads are in flight together, and one barrier serves both reductions.
+  for (int row0 = blockIdx.x; row0 < rows; row0 += 2 * G, parity ^= 1) {
+    const bool two = row0 + G < rows;
+    float4 xv[2][V], gv[2][V];
+    float dot[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-      const int c = t + j * T;
-      if (c < h4) {
-        xv[j] = ld_stream(x + base + c);
-        gv[j] = ld_stream(gy + base + c);
-      } else {
-        xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        gv[j] = xv[j];
+    for (int q = 0; q < 2; ++q) {
+      const int64_t base = static_cast<int64_t>(row0 + q * G) * h4;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int c = t + j * T;
+        if (c < h4 && (q == 0 || two)) {
+          xv[q][j] = ld_stream(x + base + c);
+          gv[q][j] = ld_stream(gy + base + c);
+        } else {
+          xv[q][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          gv[q][j] = xv[q][j];
+        }
       }
     }
-    const float r = __ldg(rms + row);
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-      dot += xv[j].x * gv[j].x * gam[j].x;
-      dot += xv[j].y * gv[j].y * gam[j].y;
-      dot += xv[j].z * gv[j].z * gam[j].z;
-      dot += xv[j].w * gv[j].w * gam[j].w;
+    for (int q = 0; q < 2; ++q) {
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        dot[q] += xv[q][j].x * gv[q][j].x * gam[j].x;
+        dot[q] += xv[q][j].y * gv[q][j].y * gam[j].y;
+        dot[q] += xv[q][j].z * gv[q][j].z * gam[j].z;
+        dot[q] += xv[q][j].w * gv[q][j].w * gam[j].w;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dot[q] += __shfl_xor_sync(0xFFFFFFFFu, dot[q], o);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-    // Two reduction slots alternate by row, so one barrier per row suffices:
-    // a slot is rewritten two rows later, after the next row's barrier.
-    if (lane == 0) red[parity][warp] = dot;
+    // Two reduction slots alternate by turn, so one barrier per turn suffices:
+    // a slot is rewritten two turns later, after the next turn's barrier.
+    if (lane == 0) {
+      red[parity][0][warp] = dot[0];
+      red[parity][1][warp] = dot[1];
+    }
     __syncthreads();
-    float total = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) total += red[parity][w];
-    const float inv_r = 1.0f / r;
-    // mean(x g gamma) / r^2: the factor of x_i in the correction term.
-    const float corr = total * inv_h * inv_r * inv_r;
+    for (int q = 0; q < 2; ++q) {
+      if (q == 1 && !two) break;
+      const int64_t base = static_cast<int64_t>(row0 + q * G) * h4;
+      float total = 0.0f;
 #pragma unroll
-    for (int j = 0; j < V; ++j) {
-      const int c = t + j * T;
-      if (c < h4) {
-        float4 o;
-        o.x = inv_r * (gam[j].x * gv[j].x - xv[j].x * corr);
-        o.y = inv_r * (gam[j].y * gv[j].y - xv[j].y * corr);
-        o.z = inv_r * (gam[j].z * gv[j].z - xv[j].z * corr);
-        o.w = inv_r * (gam[j].w * gv[j].w - xv[j].w * corr);
-        st_stream(gx + base + c, o);
-        acc[j].x += gv[j].x * xv[j].x * inv_r;
-        acc[j].y += gv[j].y * xv[j].y * inv_r;
-        acc[j].z += gv[j].z * xv[j].z * inv_r;
-        acc[j].w += gv[j].w * xv[j].w * inv_r;
+      for (int w = 0; w < kWarps; ++w) total += red[parity][q][w];
+      const float inv_r = 1.0f / __ldg(rms + row0 + q * G);
+      // mean(x g gamma) / r^2: the factor of x_i in the correction term.
+      const float corr = total * inv_h * inv_r * inv_r;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int c = t + j * T;
+        if (c < h4) {
+          float4 o;
+          o.x = inv_r * (gam[j].x * gv[q][j].x - xv[q][j].x * corr);
+          o.y = inv_r * (gam[j].y * gv[q][j].y - xv[q][j].y * corr);
+          o.z = inv_r * (gam[j].z * gv[q][j].z - xv[q][j].z * corr);
+          o.w = inv_r * (gam[j].w * gv[q][j].w - xv[q][j].w * corr);
+          st_stream(gx + base + c, o);
+          acc[j].x += gv[q][j].x * xv[q][j].x * inv_r;
+          acc[j].y += gv[q][j].y * xv[q][j].y * inv_r;
+          acc[j].z += gv[q][j].z * xv[q][j].z * inv_r;
+          acc[j].w += gv[q][j].w * xv[q][j].w * inv_r;
+        }
       }
     }
   }
@@ -134,14 +153,28 @@ __global__ void __launch_bounds__(T) rows_kernel(const float4* __restrict__ x,
   }
 }
 
-// dL/dgamma_i = the sum of the CTAs' partial rows, in CTA order.
+// dL/dgamma_i = the sum of the CTAs' partial rows.  A CTA takes 32 columns;
+// warp w sums the partial rows w, w + 8, ... in order (lane = column, so each
+// load is one coalesced 128-byte row piece), then the 8 warp sums are added in
+// warp order: a fixed order, so the result does not depend on timing.
 __global__ void __launch_bounds__(256) gamma_kernel(const float* __restrict__ partial, int parts,
                                                     int hidden, float* __restrict__ dgamma) {
-  const int i = blockIdx.x * 256 + threadIdx.x;
-  if (i >= hidden) return;
+  __shared__ float sums[8][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int i = blockIdx.x * 32 + lane;
   float s = 0.0f;
-  for (int b = 0; b < parts; ++b) s += partial[static_cast<int64_t>(b) * hidden + i];
-  dgamma[i] = s;
+  if (i < hidden) {
+#pragma unroll 4
+    for (int b = warp; b < parts; b += 8) s += partial[static_cast<int64_t>(b) * hidden + i];
+  }
+  sums[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && i < hidden) {
+    float total = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) total += sums[w][lane];
+    dgamma[i] = total;
+  }
 }
 
 struct Plan {
@@ -160,9 +193,9 @@ inline Plan plan_for(int hidden) {
   return {512, 4};
 }
 
-// CTAs of a launch: 4 per SM (one row in flight each) when dL/dgamma is wanted
-// -- each CTA then writes a partial row, so more CTAs cost partial-sum traffic
-// -- and 8 per SM otherwise.
+// CTAs of a launch: 4 per SM (two rows in flight each) when dL/dgamma is
+// wanted -- each CTA then writes a partial row, so more CTAs cost partial-sum
+// traffic -- and 8 per SM otherwise.
 inline int grid_for(int rows, bool with_gamma) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -224,8 +257,8 @@ extern "C" int rms_norm_backward(const float* input, const float* gamma, const f
 #undef NF4_RMSB_LAUNCH
   if (cudaGetLastError() != cudaSuccess) return NF4_ERR_CUDA;
   if (grad_gamma != nullptr) {
-    rmsb::gamma_kernel<<<(hidden_dim + 255) / 256, 256, 0, st>>>(partial, grid, hidden_dim,
-                                                                  grad_gamma);
+    rmsb::gamma_kernel<<<(hidden_dim + 31) / 32, 256, 0, st>>>(partial, grid, hidden_dim,
+                                                                grad_gamma);
     if (cudaGetLastError() != cudaSuccess) return NF4_ERR_CUDA;
   }
   return NF4_OK;
