@@ -27,21 +27,22 @@ def lib():
 def declared_functions() -> list[str]:
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(nf4_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:nf4|rms_norm)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_documented_calls():
     names = declared_functions()
     for n in ("nf4_quantize", "nf4_dequantize_f16", "nf4_backward_a", "nf4_backward_a_ex",
               "nf4_backward_a_batched", "nf4_backward_a_batched_workspace", "nf4_check_error",
-              "nf4_status_string", "nf4_abi_version"):
+              "nf4_status_string", "nf4_abi_version", "nf4_forward_ws", "nf4_forward_ws_bytes",
+              "rms_norm_backward", "rms_norm_backward_ws_bytes"):
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (nf4_\w+)", out))
+    exported = set(re.findall(r"\bT ((?:nf4|rms_norm)_\w+)", out))
     missing = [n for n in declared_functions() if n not in exported]
     assert not missing, missing
     for n in declared_functions():
@@ -98,3 +99,37 @@ def test_empty_problems_enqueue_nothing(lib):
     # M == 0 is a no-op that needs no valid pointers (nothing is read or written).
     assert lib.nf4_backward_a(None, None, None, None, 0, 64, 128, None) == nb.NF4_OK
     assert lib.nf4_backward_a_batched(None, 0, None, 0, None) == nb.NF4_OK
+
+
+def test_forward_and_rms_norm_validation_before_any_device_work(lib):
+    import backward_gemm_gb300 as nb
+
+    fake = C.c_void_p(0x100000)  # never dereferenced: every call below fails validation
+    odd = C.c_void_p(0x100004)
+    # Forward: K % 64, N % 4, unknown dtype, null and misaligned pointers, workspace.
+    assert lib.nf4_forward_ws(fake, 0, fake, fake, fake, 16, 64, 100, fake, 1 << 20,
+                              None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_forward_ws(fake, 0, fake, fake, fake, 16, 66, 128, fake, 1 << 20,
+                              None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_forward_ws(fake, 9, fake, fake, fake, 16, 64, 128, fake, 1 << 20,
+                              None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_forward_ws(None, 0, fake, fake, fake, 16, 64, 128, fake, 1 << 20,
+                              None) == nb.NF4_ERR_INVALID
+    assert lib.nf4_forward_ws(odd, 0, fake, fake, fake, 16, 64, 128, fake, 1 << 20,
+                              None) == nb.NF4_ERR_ALIGN
+    assert lib.nf4_forward_ws(fake, 0, fake, fake, fake, 16, 64, 128, None, 0,
+                              None) == nb.NF4_ERR_WORKSPACE
+    assert lib.nf4_forward_ws(None, 0, None, None, None, 0, 64, 128, None, 0, None) == nb.NF4_OK
+    # RMSNorm backward: hidden % 4, hidden > 8192, negative rows, pointers, workspace.
+    assert lib.rms_norm_backward(fake, fake, fake, fake, fake, None, 4, 62, None, 0,
+                                 None) == nb.NF4_ERR_INVALID
+    assert lib.rms_norm_backward(fake, fake, fake, fake, fake, None, 4, 8196, None, 0,
+                                 None) == nb.NF4_ERR_INVALID
+    assert lib.rms_norm_backward(fake, fake, fake, fake, fake, None, -1, 64, None, 0,
+                                 None) == nb.NF4_ERR_INVALID
+    assert lib.rms_norm_backward(None, fake, fake, fake, fake, None, 4, 64, None, 0,
+                                 None) == nb.NF4_ERR_INVALID
+    assert lib.rms_norm_backward(odd, fake, fake, fake, fake, None, 4, 64, None, 0,
+                                 None) == nb.NF4_ERR_ALIGN
+    assert lib.rms_norm_backward(fake, fake, fake, fake, fake, fake, 4, 64, None, 0,
+                                 None) == nb.NF4_ERR_WORKSPACE
