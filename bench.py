@@ -603,16 +603,24 @@ def bench_e2e(args, probs, host_go, sets, stream, dev, flops, world):
 
 
 def kernel_source_digest() -> str:
-    """SHA-256 over the CUDA sources of the library (file names and contents)."""
+    """SHA-256 over the CUDA sources of the library (file names and code, with
+    comments and blank lines removed: a change to a comment leaves the kernels,
+    and so their counters, as they were).  The sources hold no string literal
+    with a comment marker."""
     import hashlib
+    import re
 
     csrc = os.path.join(ROOT, "backward_gemm_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", "", text)
+            code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
             h.update(name.encode())
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            h.update(code.encode())
     return h.hexdigest()
 
 
