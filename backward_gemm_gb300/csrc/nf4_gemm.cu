@@ -7,31 +7,37 @@
 // warp a 16x16 output tile and runs WMMA 16x16x16 over N; here the same
 // arithmetic runs as a persistent, warp-specialised kernel on pairs of SMs:
 //
-//   pair tile   256 tokens x 256 output columns k, computed by a cluster of two
-//               CTAs with tcgen05.mma.cta_group::2 (M=256, N=256, K=16).  CTA r
-//               of the pair holds grad_out rows 128r..128r+127 of the tile (the A
-//               operand) and dequantises B^T for output columns 128r..128r+127
-//               (its half of the B operand); the MMA reads both halves, so each
-//               SM dequantises only half of what a single-CTA tile would need.
-//               The shared dimension N is consumed 64 at a time (4 MMAs).
-//   warp 4      TMA producer (each CTA): grad_out (fp32 as two 32-column boxes,
-//               or one bf16 box, 128-byte swizzle) and the CTA's NF4 bytes (64
-//               rows n x 64 bytes = 128 k, 64-byte swizzle) into a 3-stage ring
+//   pair tile   256 (or 512: two M-blocks) tokens x 256 output columns k,
+//               computed by a cluster of two CTAs with tcgen05.mma.cta_group::2
+//               (M=256, N=256, K=16).  CTA r of the pair holds grad_out rows
+//               128r..128r+127 of each M-block (the A operand) and dequantises
+//               B^T for output columns 128r..128r+127 (its half of the B
+//               operand); the MMA reads both halves, so each SM dequantises
+//               only half of what a single-CTA tile would need.  The shared
+//               dimension N is consumed 64 at a time (4 MMAs per M-block).
+//   warp 4      raw producer (each CTA): the NF4 bytes (64 rows n x 64 bytes =
+//               128 k, 64-byte swizzle) and the stage's block scales, plus
+//               grad_out (fp32 or bf16 boxes, 128-byte swizzle) in the variants
+//               that convert it in shared memory, into a ring of raw stages
+//   warp 23     pre-converted variant: copies each stage's f16 A operand (made
+//               by the f16 pre-pass) with TMA into a ring of A slots
 //   warps 6-21  converters, two groups of 8 warps that take alternate stages:
-//               grad_out -> f16 into the K-major A operand; NF4 codes x block
-//               scale -> f16 into the MN-major B^T operand (one 64-k NF4 block
-//               is one 128-byte swizzle row); stage i goes to operand slot
-//               i % 3, so a group can start as soon as MMA i-3 is done
-//   warp 5      allocates 512 TMEM columns in both CTAs; in CTA 0 one thread
-//               issues the pair MMAs into a double-buffered fp32 accumulator
-//               (2 x 256 columns) and commits to barriers of both CTAs.  CTA 1's
-//               converter warps signal a finished stage to CTA 0 with 16-byte
-//               bulk copies that complete on CTA 0's operand barrier
+//               NF4 codes x block scale -> f16 into the MN-major B^T operand
+//               (one 64-k NF4 block is one 128-byte swizzle row), and grad_out
+//               -> f16 into the K-major A operand where it is not pre-converted
+//   warp 5      allocates 512 TMEM columns in both CTAs; in CTA 0 one elected
+//               lane of the converged warp issues the pair MMAs into a
+//               double-buffered fp32 accumulator (2 x 256 columns; 512-token
+//               tiles use both as one) and commits to barriers of both CTAs.
+//               CTA 1's converter warps signal a finished stage to CTA 0 with
+//               16-byte bulk copies that complete on CTA 0's operand barrier
 //   warp 22     CTA 0: waits on the operand barriers and publishes each ready
-//               stage in a shared-memory word the MMA thread polls
+//               stage in a shared-memory word the MMA warp polls
 //   warps 0-3   epilogue (each CTA): tcgen05.ld of a 32-lane quarter, staged
-//               through shared memory and written with TMA stores, which clip
-//               rows >= M and columns >= K; overlaps the next tile's main loop
+//               through shared memory (double-buffered, or a whole M-block in
+//               the idle rings) and written with TMA stores, which clip rows >=
+//               M and columns >= K; overlaps the next tile's main loop when the
+//               accumulator is double-buffered
 //
 // Out-of-range operands contribute 0 (page above, "PHASE 1"/"PHASE 2": zero the
 // out-of-bounds elements): TMA fills rows >= M and columns >= N of grad_out
@@ -39,7 +45,11 @@
 //
 // The same kernel serves one problem (descriptor passed as a kernel parameter)
 // and a grouped launch over many projections (descriptors in a caller-owned
-// device workspace, tiles of all problems flattened into one list).
+// device workspace, tiles of all problems flattened into one list); a single
+// problem's last partial wave of tiles may be split by stages over all pairs
+// (stream-K, partial sums added in a fixed order).  A per-problem flag turns
+// the pre-converted variant around for the forward product C = A @ dequant(B)
+// (contracted over K; the dequantised weight becomes a K-major B operand).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
