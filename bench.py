@@ -725,6 +725,75 @@ def bench_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def bench_reference_extra(args, rank, world):
+    """The oracle arm of the forward and RMSNorm workloads: the CPU oracle as it
+    stands on the host cores, each step a bounded sample of the workload's rows
+    (about a minute for warm-up plus timed steps), on the ours arm's metric."""
+    if rank != 0:
+        return None
+    import oracle
+    from oracle.build import build_oracle
+
+    build_oracle()
+    per_step_s = 60.0 / max(args.steps + args.warmup, 1)
+    if args.workload in FWD_WORKLOADS:
+        M, N, K, dt, a_std, b_std, outl, seed = FWD_WORKLOADS[args.workload]
+        a = make_grad_out(Problem(M, K, N, dt, a_std, b_std, outl, seed))
+        data, scales = oracle.quantize(make_weight(Problem(M, N, K, dt, a_std, b_std, outl, seed + 1)))
+        probe = min(M, 8)
+        t0 = time.perf_counter()
+        bt = oracle.dequantize_f16(scales, data, K, N)
+        oracle.forward_rows(oracle.round_operand(a[:probe], dt), bt,
+                            np.arange(probe, dtype=np.int32), want_bound=False)
+        rate = 2 * probe * N * K / max(time.perf_counter() - t0, 1e-6)
+        rows = max(1, min(M, int(rate * per_step_s / (2 * N * K))))
+
+        def step():
+            b = oracle.dequantize_f16(scales, data, K, N)
+            oracle.forward_rows(oracle.round_operand(a[:rows], dt), b,
+                                np.arange(rows, dtype=np.int32), want_bound=False)
+
+        metric = "NF4 forward GEMM (C = A @ dequant(B)) TFLOP/s and % of GB300 dense FP16 tensor roofline"
+        unit, per_row = "TFLOP/s", 2 * N * K
+        workload = f"{args.workload}: M={M} N={N} K={K} A {DTYPE_NAMES[dt]}"
+        what = f"of {M} rows of {M}x{N}x{K} per step (dequantise + rounding + fp64 rows)"
+    else:
+        rows_all, H = RMSNORM_WORKLOADS[args.workload]
+        gen = torch.Generator().manual_seed(0)
+        x = torch.randn(rows_all, H, generator=gen).numpy()
+        gy = (torch.randn(rows_all, H, generator=gen) * 1e-2).numpy()
+        gamma = (1.0 + 0.1 * torch.randn(H, generator=gen)).numpy()
+        rms = np.sqrt((x.astype(np.float64) ** 2).mean(axis=1) + 1e-6).astype(np.float32)
+        probe = min(rows_all, 64)
+        t0 = time.perf_counter()
+        oracle.rms_norm.backward(x[:probe], gamma, rms[:probe], gy[:probe])
+        rate = 12 * probe * H / max(time.perf_counter() - t0, 1e-6)
+        rows = max(1, min(rows_all, int(rate * per_step_s / (12 * H))))
+
+        def step():
+            oracle.rms_norm.backward(x[:rows], gamma, rms[:rows], gy[:rows])
+
+        metric = "RMSNorm backward (dL/dx, dL/dgamma) GB/s and % of GB300 HBM roofline"
+        unit, per_row = "GB/s", 12 * H
+        workload = f"{args.workload}: rows={rows_all} hidden={H}"
+        what = f"of {rows_all} rows of {rows_all}x{H} per step (fp64 numpy)"
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt_s = time.perf_counter() - t0
+    value = per_row * rows * args.steps / dt_s / (1e12 if unit == "TFLOP/s" else 1e9)
+    return {"metric": metric, "impl": "reference", "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt_s * 1e3 / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload, "parallelism": "host cores, rank 0 only"},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": f"{rows} {what}"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -748,20 +817,15 @@ def main():
 
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
-    if args.workload in RMSNORM_WORKLOADS:
-        if args.impl == "reference" or world > 1:
-            line = {"impl": args.impl, "unavailable": "the RMSNorm workload runs on one GPU, ours arm only"}
+    if args.workload in RMSNORM_WORKLOADS or args.workload in FWD_WORKLOADS:
+        if args.impl == "reference":
+            line = bench_reference_extra(args, rank, world)
+        elif world > 1:
+            line = {"impl": args.impl, "unavailable": "this workload is measured on one GPU"}
         else:
             dev = torch.device("cuda", local)
             torch.cuda.set_device(dev)
-            line = bench_rmsnorm(args, dev)
-    elif args.workload in FWD_WORKLOADS:
-        if args.impl == "reference" or world > 1:
-            line = {"impl": args.impl, "unavailable": "forward workloads run on one GPU, ours arm only"}
-        else:
-            dev = torch.device("cuda", local)
-            torch.cuda.set_device(dev)
-            line = bench_forward(args, dev)
+            line = (bench_rmsnorm if args.workload in RMSNORM_WORKLOADS else bench_forward)(args, dev)
     elif args.impl == "reference":
         line = bench_reference(args, rank, world)
     else:
