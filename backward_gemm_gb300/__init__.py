@@ -65,6 +65,7 @@ SIGNATURES = {
     "nf4_backward_a_batched_noalloc": (_i, [C.POINTER(Nf4Problem), _i, _vp]),
     "nf4_set_small_m_max": (_i, [_i]),
     "nf4_small_m_split": (_i, [_i, _i, _i, _i, C.POINTER(_i)]),
+    "nf4_watchdog_selftest": (_i, [C.c_longlong, _vp, _vp]),
 }
 
 _lib = None
@@ -126,6 +127,49 @@ def _require_cuda_contig(name: str, t: torch.Tensor) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_shapes(go: torch.Tensor, w: "NF4Weight", out: torch.Tensor | None,
+                  what: str = "problem") -> tuple[int, int]:
+    """Shape and type rules of one backward-A problem: grad_out [M, N] with N =
+    the weight's N, the weight's codes [N, K/2] uint8 and scales [N, K/64]
+    float32, out (when given) float32 [M, K].  Returns (M, N)."""
+    if go.dim() != 2:
+        raise ValueError(f"{what}: grad_out must be 2-D [M, N], got shape {tuple(go.shape)}")
+    M, N = go.shape
+    if N != w.N:
+        raise ValueError(f"{what}: grad_out has N={N}, weight has N={w.N}")
+    if w.data.dtype != torch.uint8 or w.data.numel() != w.N * (w.K // 2):
+        raise ValueError(f"{what}: weight codes must be uint8 [N, K/2] = [{w.N}, {w.K // 2}]")
+    if w.scales.dtype != torch.float32 or w.scales.numel() != w.N * (w.K // 64):
+        raise ValueError(f"{what}: weight scales must be float32 [N, K/64] = [{w.N}, {w.K // 64}]")
+    if out is not None and (out.dtype != torch.float32 or tuple(out.shape) != (M, w.K)):
+        raise ValueError(f"{what}: out must be float32 [M, K] = [{M}, {w.K}], got "
+                         f"{out.dtype} {tuple(out.shape)}")
+    _dtype_code(go)
+    return M, N
+
+
+def _check_devices(go: torch.Tensor, w: "NF4Weight", out: torch.Tensor | None,
+                   what: str = "problem") -> None:
+    """grad_out, the weight's codes and scales and out (when given): contiguous,
+    on one CUDA device."""
+    tensors = [("grad_out", go), ("weight codes", w.data), ("weight scales", w.scales)]
+    if out is not None:
+        tensors.append(("out", out))
+    for name, t in tensors:
+        _require_cuda_contig(f"{what}: {name}", t)
+    if any(t.device != go.device for _, t in tensors):
+        raise ValueError(f"{what}: grad_out, the weight and out must be on one device")
+
+
+def _check_problem(go: torch.Tensor, w: "NF4Weight", out: torch.Tensor | None,
+                   what: str = "problem") -> tuple[int, int]:
+    """Every rule of one backward-A problem, checked before anything is launched
+    (shapes and types first, then devices).  Returns (M, N)."""
+    M, N = _check_shapes(go, w, out, what)
+    _check_devices(go, w, out, what)
+    return M, N
+
+
 class NF4Weight:
     """A frozen weight B [K x N] in NF4: ``data`` u8 [N, K/2], ``scales`` f32 [N, K/64]."""
 
@@ -159,15 +203,9 @@ def dequantize_f16(w: NF4Weight) -> torch.Tensor:
 
 def backward_a(grad_out: torch.Tensor, w: NF4Weight, out: torch.Tensor | None = None):
     """grad_A [M, K] fp32 = grad_out [M, N] (fp32 or bf16) @ deq(B)^T."""
-    _require_cuda_contig("grad_out", grad_out)
-    M, N = grad_out.shape
-    if N != w.N:
-        raise ValueError(f"grad_out has N={N}, weight has N={w.N}")
+    M, N = _check_problem(grad_out, w, out)
     if out is None:
         out = torch.empty((M, w.K), dtype=torch.float32, device=grad_out.device)
-    _require_cuda_contig("out", out)
-    if out.dtype != torch.float32 or tuple(out.shape) != (M, w.K):
-        raise ValueError("out must be float32 [M, K]")
     _check(lib().nf4_backward_a_ex(_ptr(grad_out), _dtype_code(grad_out), _ptr(w.scales),
                                    _ptr(w.data), _ptr(out), M, N, w.K, _stream()),
            "nf4_backward_a_ex")
@@ -241,15 +279,9 @@ def backward_a_ws(grad_out: torch.Tensor, w: NF4Weight, workspace: torch.Tensor 
     """As :func:`backward_a`, through ``nf4_backward_a_ws``: grad_out is first
     rounded to f16 into ``workspace`` by its own pass, and the GEMM loads the A
     operand with TMA.  Same result as :func:`backward_a`, bit for bit."""
-    _require_cuda_contig("grad_out", grad_out)
-    M, N = grad_out.shape
-    if N != w.N:
-        raise ValueError(f"grad_out has N={N}, weight has N={w.N}")
+    M, N = _check_problem(grad_out, w, out)
     if out is None:
         out = torch.empty((M, w.K), dtype=torch.float32, device=grad_out.device)
-    _require_cuda_contig("out", out)
-    if out.dtype != torch.float32 or tuple(out.shape) != (M, w.K):
-        raise ValueError("out must be float32 [M, K]")
     if workspace is None:
         workspace = ws_workspace(M, N, grad_out.device)
     _require_cuda_contig("workspace", workspace)
@@ -328,43 +360,40 @@ def batched_workspace(count: int, device=None) -> torch.Tensor:
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
 
 
-def backward_a_batched(items, workspace: torch.Tensor | None = None):
-    """Grouped launch.  ``items``: sequence of (grad_out, NF4Weight, out-or-None).
-    Returns the list of outputs."""
-    items = list(items)
-    arr = (Nf4Problem * max(len(items), 1))()
-    outs = []
-    for i, (go, w, out) in enumerate(items):
-        _require_cuda_contig("grad_out", go)
-        M, N = go.shape
-        if out is None:
-            out = torch.empty((M, w.K), dtype=torch.float32, device=go.device)
-        _require_cuda_contig("out", out)
-        outs.append(out)
-        arr[i] = Nf4Problem(go.data_ptr(), _dtype_code(go), w.scales.data_ptr(), w.data.data_ptr(),
-                            out.data_ptr(), M, N, w.K)
-    if workspace is None:
-        workspace = batched_workspace(len(items), items[0][0].device if items else None)
-    _check(lib().nf4_backward_a_batched(arr, len(items), _ptr(workspace), workspace.numel(),
-                                        _stream()), "nf4_backward_a_batched")
-    return outs
-
-
 def _problem_array(items, make_out: bool):
+    """The host array of nf4_problem for a grouped call, every item checked by
+    the single-call rules first (nothing is allocated or launched when one
+    fails); missing outputs are created when ``make_out``."""
+    items = list(items)
+    for i, (go, w, out) in enumerate(items):
+        _check_shapes(go, w, out, f"item {i}")
+        if out is None and not make_out:
+            raise ValueError(f"item {i}: every output must be given")
+    for i, (go, w, out) in enumerate(items):
+        _check_devices(go, w, out, f"item {i}")
     arr = (Nf4Problem * max(len(items), 1))()
     outs = []
     for i, (go, w, out) in enumerate(items):
-        _require_cuda_contig("grad_out", go)
         M, N = go.shape
         if out is None:
-            if not make_out:
-                raise ValueError("every output must be given")
             out = torch.empty((M, w.K), dtype=torch.float32, device=go.device)
-        _require_cuda_contig("out", out)
         outs.append(out)
         arr[i] = Nf4Problem(go.data_ptr(), _dtype_code(go), w.scales.data_ptr(), w.data.data_ptr(),
                             out.data_ptr(), M, N, w.K)
     return arr, outs
+
+
+def backward_a_batched(items, workspace: torch.Tensor | None = None):
+    """Grouped launch.  ``items``: sequence of (grad_out, NF4Weight, out-or-None).
+    Returns the list of outputs."""
+    items = list(items)
+    arr, outs = _problem_array(items, make_out=True)
+    if workspace is None:
+        workspace = batched_workspace(len(items), items[0][0].device if items else None)
+    _require_cuda_contig("workspace", workspace)
+    _check(lib().nf4_backward_a_batched(arr, len(items), _ptr(workspace), workspace.numel(),
+                                        _stream()), "nf4_backward_a_batched")
+    return outs
 
 
 def batched_ws_bytes(items) -> int:
@@ -404,16 +433,10 @@ def backward_a_batched_noalloc(items):
     fixed array inside the library, at most 256 problems).  ``items`` as for
     backward_a_batched, but every output must be given (no tensor is created)."""
     items = list(items)
-    arr = (Nf4Problem * max(len(items), 1))()
-    for i, (go, w, out) in enumerate(items):
-        _require_cuda_contig("grad_out", go)
-        _require_cuda_contig("out", out)
-        M, N = go.shape
-        arr[i] = Nf4Problem(go.data_ptr(), _dtype_code(go), w.scales.data_ptr(), w.data.data_ptr(),
-                            out.data_ptr(), M, N, w.K)
+    arr, outs = _problem_array(items, make_out=False)
     _check(lib().nf4_backward_a_batched_noalloc(arr, len(items), _stream()),
            "nf4_backward_a_batched_noalloc")
-    return [out for _, _, out in items]
+    return outs
 
 
 def set_small_m_max(m_max: int) -> int:
@@ -442,6 +465,16 @@ def small_m_split(N: int, K: int, sms: int, cta_slots: int) -> tuple[int, int]:
     per = C.c_int(0)
     S = lib().nf4_small_m_split(N, K, sms, cta_slots, C.byref(per))
     return int(S), int(per.value)
+
+
+def watchdog_selftest(limit_cycles: int = 200_000) -> torch.Tensor:
+    """Enqueue the bounded-wait self-test (a CTA whose waits give up after
+    ``limit_cycles``); returns the 3 device words it writes.  The next
+    :func:`check_error` raises for the recorded timeout."""
+    where = torch.zeros(3, dtype=torch.int32, device="cuda")
+    _check(lib().nf4_watchdog_selftest(int(limit_cycles), _ptr(where), _stream()),
+           "nf4_watchdog_selftest")
+    return where
 
 
 def check_error() -> None:

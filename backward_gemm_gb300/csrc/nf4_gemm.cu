@@ -2313,6 +2313,44 @@ extern "C" int nf4_debug_set_trace(void* buf) {
 }
 #endif
 
+// ------------------------------------------------------------------ watchdog self-test
+// One CTA whose waits cannot be satisfied: thread 0 waits on an mbarrier that
+// nothing arrives on, with a short limit, so it gives up, records the timeout
+// (status word and site) and raises the CTA's abort flag; thread 32 waits on a
+// second such barrier with the normal limit and must return as soon as it sees
+// the flag (without recording a second site).  Both then exit: the context
+// stays usable.  `where` receives the first barrier's shared-memory address
+// and whether the second wait returned without a completed phase.
+__global__ void wait_selftest_kernel(long long limit, unsigned int* where) {
+  __shared__ __align__(8) unsigned long long bars[2];
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+  const uint32_t b0 = smem_addr(&bars[0]), b1 = smem_addr(&bars[1]);
+  if (threadIdx.x == 0) {
+    mbar_init(b0, 1);
+    mbar_init(b1, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait(b0, 0, abort_flag, limit);
+    where[0] = b0;
+    where[1] = ok ? 1u : 0u;
+  } else if (threadIdx.x == 32) {
+    where[2] = mbar_wait(b1, 0, abort_flag) ? 1u : 0u;
+  }
+  __syncthreads();
+}
+
+extern "C" int nf4_watchdog_selftest(long long limit_cycles, unsigned int* where, void* stream) {
+  if (limit_cycles < 1000 || limit_cycles > kWaitLimitCycles || where == nullptr ||
+      !aligned(where, 4))
+    return NF4_ERR_INVALID;
+  wait_selftest_kernel<<<1, 64, 0, as_stream(stream)>>>(limit_cycles, where);
+  return launch_status();
+}
+
 extern "C" int nf4_check_error(void* stream) {
   return nf4_check_error_site(stream, nullptr);
 }

@@ -89,10 +89,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false (and
-// records kStatusTimeout) if that takes longer than kWaitLimitCycles, or soon after
-// another role of the CTA has given up (*abort_flag != 0).
+// records kStatusTimeout) if that takes longer than `limit` SM cycles
+// (kWaitLimitCycles unless a self-test asks for less), or soon after another
+// role of the CTA has given up (*abort_flag != 0).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
@@ -100,7 +102,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag != nullptr && *abort_flag != 0) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       record_timeout(bar, parity);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;

@@ -4,8 +4,11 @@
 
 A step is one pass of the hot path over one batch of synthetic input: one
 backward-A call on the workload's projection(s) (a grouped launch when the
-workload has several).  The default workload is the single Qwen2.5-1.5B q_proj
-backward (M=2048 tokens, N=K=1536, fp32 grad_out).
+workload has several).  The default workload is the full training step of a
+Qwen2.5-1.5B-shaped model: 28 layers x 7 projections (q, k, v, o, gate, up,
+down) at M=4096 tokens with fp32 grad_out, as one grouped call (196 problems,
+10.7 TFLOP).  ``--layers L`` runs the first L layers only (for a profiler
+capture of a small case).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
 and a device synchronise, timed with CUDA events on the launching stream.
@@ -37,16 +40,18 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import BF16, CONFIGS, DTYPE_NAMES, F32, Problem, make_grad_out, make_weight  # noqa
+from workloads import (BF16, CONFIGS, DTYPE_NAMES, F32, Problem, full_step, make_grad_out,  # noqa
+                       make_weight)
 
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def workloads() -> dict[str, list[Problem]]:
+def workloads(layers: int | None = None) -> dict[str, list[Problem]]:
     w = {"q_proj": CONFIGS["q_proj"], "tiny": CONFIGS["tiny"],
          "up_proj": [CONFIGS["mlp"][0]], "down_proj": [CONFIGS["mlp"][1]],
-         "mlp": CONFIGS["mlp"], "full_step": CONFIGS["full_step"]}
+         "mlp": CONFIGS["mlp"],
+         "full_step": CONFIGS["full_step"] if layers is None else full_step(layers=layers)}
     for p in CONFIGS["large"]:
         w[p.name] = [p]
     return w
@@ -67,6 +72,10 @@ def describe(name: str, probs: list[Problem]) -> str:
     if len(probs) == 1:
         p = probs[0]
         return f"{name}: M={p.M} N={p.N} K={p.K} grad_out {DTYPE_NAMES[p.go_dtype]}"
+    if name == "full_step":
+        return (f"full_step: {len(probs) // 7} layers x 7 projections (q, k, v, o, gate, up, down; "
+                f"hidden 1536, kv 256, intermediate 8960), M={probs[0].M} tokens, grad_out "
+                f"{DTYPE_NAMES[probs[0].go_dtype]}, one grouped call")
     return f"{name}: {len(probs)} projections grouped, M={probs[0].M}"
 
 
@@ -197,7 +206,7 @@ def bench_ours(args, rank, world, dev):
     build()
     nb.lib()
 
-    probs = workloads()[args.workload]
+    probs = workloads(args.layers)[args.workload]
     flops = sum(p.flops for p in probs)
     alg_bytes = sum(p.algorithmic_bytes for p in probs)
     entry = args.entry if len(probs) > 1 or probs[0].M > SMALL_M_MAX else "plain"
@@ -258,7 +267,9 @@ def bench_ours(args, rank, world, dev):
     # pre-pass), over the same rotating sets.
     kernel_ms = None
     if entry == "ws" and len(probs) == 1 and probs[0].N % 8 == 0:
-        kernel_ms = time_gemm_only(sets, probs[0], stream, dev, K)
+        kernel_ms = time_gemm_only(sets, probs[0], stream, dev, min(K, 200))
+    elif entry == "ws" and len(probs) > 1 and all(p.M > SMALL_M_MAX for p in probs):
+        kernel_ms = time_group_gemm_only(sets, probs, stream, dev, min(K, 200))
 
     peaks, peak_kind = load_peaks()
     long_run = ms > 1000.0
@@ -280,8 +291,11 @@ def bench_ours(args, rank, world, dev):
                            else f"{peak_kind} HBM copy")
     roof["kernel"] = kernel_names(probs, entry)
     roof["kernel_ms"] = kern_ms
-    roof["timed"] = ("bwd_a_kernel alone (f16 grad_out entry, CUDA events, same rotating sets)"
-                     if kernel_ms is not None else "whole step")
+    roof["timed"] = ("whole step" if kernel_ms is None else
+                     "bwd_a_kernel alone (f16 grad_out entry, CUDA events, same rotating sets)"
+                     if len(probs) == 1 else
+                     "grouped bwd_a_kernel launch alone (f16 grad_out read in place, CUDA events, "
+                     "same rotating sets; its descriptor-upload kernels, ~2 us each, included)")
 
     line = {
         "metric": "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline",
@@ -510,6 +524,41 @@ def time_gemm_only(sets, p, stream, dev, steps):
     return ev0.elapsed_time(ev1) / steps
 
 
+def time_group_gemm_only(sets, probs, stream, dev, steps):
+    """Average device time (ms) of a grouped step's GEMM launch alone:
+    nf4_backward_a_batched_ws given, as f16 grad_out, the copies the steps left
+    in each set's workspace (f16 input is read in place, so no pre-pass runs;
+    only the descriptor uploads precede the GEMM)."""
+    import backward_gemm_gb300 as nb
+
+    count = len(probs)
+    desc = (640 * count + 255) // 256 * 256  # descriptor area (nf4_backward_a_batched_ws_bytes)
+    runs = []
+    for items, ws in sets:
+        at = desc
+        f16_items = []
+        for p, (go, w, out) in zip(probs, items):
+            pitch = (p.N + 7) // 8 * 8
+            n = 2 * p.M * pitch
+            assert pitch == p.N, "f16 copies are read as [M, N] (N % 8 == 0)"
+            f16_items.append((ws[at: at + n].view(torch.float16).view(p.M, p.N), w, out))
+            at += (n + 255) // 256 * 256
+        runs.append((f16_items, ws))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            nb.backward_a_batched_ws(*runs[i % len(runs)])
+        nb.check_error()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for i in range(steps):
+            nb.backward_a_batched_ws(*runs[i % len(runs)])
+        ev1.record(stream)
+        ev1.synchronize()
+        nb.check_error()
+    return ev0.elapsed_time(ev1) / steps
+
+
 def kernel_names(probs, entry="plain") -> str:
     """The library kernels one step launches: the few-token kernel for M <= 64,
     the pair kernel otherwise (after the f16 pre-pass with the ws entry)."""
@@ -642,36 +691,47 @@ def traffic_for(workload: str):
 
 # ---------------------------------------------------------------- oracle (CPU) arm
 def cpu_baseline(probs, budget_s: float = 15.0, rows_per_problem: int | None = None):
-    """The CPU oracle as it stands, on a bounded sample: for each problem a slice
-    of its rows (quantise, dequantise and operand rounding included)."""
+    """The CPU oracle as it stands, on a bounded sample: for each distinct
+    problem shape a slice of its rows, about 50 GFLOP of fp64 work each
+    (dequantise, operand rounding and the product timed)."""
     import oracle
 
     threads = oracle.max_threads()
-    t0 = time.perf_counter()
+    t_total = 0.0
     done_flops = 0
     rows_total = 0
     sample_desc = []
+    # The GPU step starts from quantised weights, so the oracle's quantisation
+    # (a one-off per weight) is not timed; its dequantisation, the rounding of
+    # grad_out and the fp64 product are.  One problem of each distinct shape
+    # (for the full step: the seven projections of the first layer).
+    shapes, seen = [], set()
     for p in probs:
+        if (p.M, p.N, p.K, p.go_dtype) not in seen:
+            seen.add((p.M, p.N, p.K, p.go_dtype))
+            shapes.append(p)
+    for p in shapes:
         go = make_grad_out(p)
-        B = make_weight(p)
-        data, scales = oracle.quantize(B)
+        data, scales = oracle.quantize(make_weight(p))
+        t0 = time.perf_counter()
         bt = oracle.dequantize_f16(scales, data, p.K, p.N)
-        rows = rows_per_problem or max(1, min(p.M, int(2e9 / (2 * p.N * p.K)) or 1))
+        rows = rows_per_problem or max(1, min(p.M, int(5e10 / (2 * p.N * p.K)) or 1))
         go16 = oracle.round_operand(go[:rows], p.go_dtype)
         oracle.backward_a_rows(go16, bt, np.arange(rows, dtype=np.int32), want_bound=False)
+        t_total += time.perf_counter() - t0
         done_flops += 2 * rows * p.N * p.K
         rows_total += rows
-        if len(sample_desc) < 3:
-            sample_desc.append(f"{rows} of {p.M} rows of {p.M}x{p.N}x{p.K}")
-        if time.perf_counter() - t0 > budget_s:
+        sample_desc.append(f"{rows} of {p.M} rows of {p.M}x{p.N}x{p.K}")
+        if t_total > budget_s:
             break
-    dt = time.perf_counter() - t0
-    return {"value": done_flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "seconds": dt,
-            "sample": "; ".join(sample_desc) + (f" (+{len(probs) - 3} more problems, "
-                                                if len(probs) > 3 else "")
-                      + ("" if len(probs) <= 3 else f"{rows_total} rows total)")
-                      + "; fp64 sums, includes quantise/dequantise/rounding"}
+    more = ""
+    if len(shapes) > 3:
+        more = (f" (... {rows_total} rows of {len(sample_desc)} distinct shapes of the "
+                f"{len(probs)} problems, to a {budget_s:.0f} s budget)")
+    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": t_total,
+            "sample": "; ".join(sample_desc) + more
+                      + "; fp64 sums; dequantise + rounding + product timed, quantise not"}
 
 
 def bench_reference(args, rank, world):
@@ -681,26 +741,40 @@ def bench_reference(args, rank, world):
     from oracle.build import build_oracle
 
     build_oracle()
-    probs = workloads()[args.workload]
-    p = probs[0]
-    go = make_grad_out(p)
-    data, scales = oracle.quantize(make_weight(p))
+    probs = workloads(args.layers)[args.workload]
+    # The workload's distinct projection shapes (for the full step: the seven
+    # projections of the first layer; the other layers repeat them), each
+    # with its own seeded inputs; quantisation is a one-off per weight and is
+    # not timed.
+    shapes, seen = [], set()
+    for p in probs:
+        if (p.M, p.N, p.K, p.go_dtype) not in seen:
+            seen.add((p.M, p.N, p.K, p.go_dtype))
+            shapes.append(p)
+    inputs = []
+    for p in shapes:
+        data, scales = oracle.quantize(make_weight(p))
+        inputs.append((p, make_grad_out(p), data, scales))
     steps_done = 0
-    # A bounded per-step sample: probe the oracle's rate on a few rows, then size
-    # each step so that warm-up plus timed steps take about a minute in total.
-    probe = min(p.M, 8)
+    # A bounded per-step sample: probe the oracle's rate on a few rows of each
+    # shape, then size each step (the same number of rows of every shape) so
+    # that warm-up plus timed steps take about a minute in total.
+    probe = min(min(p.M for p in shapes), 8)
     t0 = time.perf_counter()
-    bt = oracle.dequantize_f16(scales, data, p.K, p.N)
-    oracle.backward_a_rows(oracle.round_operand(go[:probe], p.go_dtype), bt,
-                           np.arange(probe, dtype=np.int32), want_bound=False)
-    rate = 2 * probe * p.N * p.K / max(time.perf_counter() - t0, 1e-6)
+    for p, go, data, scales in inputs:
+        bt = oracle.dequantize_f16(scales, data, p.K, p.N)
+        oracle.backward_a_rows(oracle.round_operand(go[:probe], p.go_dtype), bt,
+                               np.arange(probe, dtype=np.int32), want_bound=False)
+    per_row = sum(2 * p.N * p.K for p in shapes)
+    rate = probe * per_row / max(time.perf_counter() - t0, 1e-6)
     per_step_s = 60.0 / max(args.steps + args.warmup, 1)
-    rows = max(1, min(p.M, int(rate * per_step_s / (2 * p.N * p.K))))
+    rows = max(1, min(min(p.M for p in shapes), int(rate * per_step_s / per_row)))
 
     def step():
-        bt = oracle.dequantize_f16(scales, data, p.K, p.N)
-        go16 = oracle.round_operand(go[:rows], p.go_dtype)
-        oracle.backward_a_rows(go16, bt, np.arange(rows, dtype=np.int32), want_bound=False)
+        for p, go, data, scales in inputs:
+            bt = oracle.dequantize_f16(scales, data, p.K, p.N)
+            go16 = oracle.round_operand(go[:rows], p.go_dtype)
+            oracle.backward_a_rows(go16, bt, np.arange(rows, dtype=np.int32), want_bound=False)
 
     for _ in range(args.warmup):
         step()
@@ -709,9 +783,11 @@ def bench_reference(args, rank, world):
         step()
         steps_done += 1
     dt = time.perf_counter() - t0
-    flops = 2 * rows * p.N * p.K * steps_done
+    flops = rows * per_row * steps_done
     value = flops / dt / 1e12
-    sample = f"{rows} of {p.M} rows of {p.M}x{p.N}x{p.K} per step (dequantise + rounding + fp64 rows)"
+    sample = (f"{rows} rows of each of {len(shapes)} distinct projection shapes ("
+              + ", ".join(f"{p.M}x{p.N}x{p.K}" for p in shapes)
+              + ") per step (dequantise + rounding + fp64 rows)")
     return {"metric": "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline",
             "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(steps_done, 1),
@@ -799,7 +875,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="q_proj", choices=sorted(workloads()) + sorted(FWD_WORKLOADS) + sorted(RMSNORM_WORKLOADS))
+    ap.add_argument("--workload", default="full_step",
+                    choices=sorted(workloads()) + sorted(FWD_WORKLOADS) + sorted(RMSNORM_WORKLOADS))
+    ap.add_argument("--layers", type=int, default=None,
+                    help="full_step only: run the first L of the 28 layers (a small case for a "
+                         "profiler capture)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--entry", default="ws", choices=["plain", "ws"],
                     help="single-problem entry point: nf4_backward_a_ex, or nf4_backward_a_ws "

@@ -310,7 +310,10 @@ int nf4_backward_a_batched_ws(const nf4_problem* problems, int count, void* work
  *              enqueues nothing
  *   set-up     the first call on a device looks up the array's device address
  *              (cudaGetSymbolAddress) with that device current; make that first
- *              call before any stream capture
+ *              call before any stream capture.  The address is kept for the
+ *              life of the process: after a cudaDeviceReset it is stale, so a
+ *              process that resets a device must not call this entry point on
+ *              that device again
  *   sharing    every call on a device uses the same array, which keeps the last
  *              call's descriptors; each call rewrites every descriptor its
  *              kernel reads before the kernel runs, so nothing needs clearing,
@@ -334,6 +337,25 @@ int nf4_check_error(void* stream);
  * (4 words, host memory) is zeroed when there was no timeout; may be NULL.
  */
 int nf4_check_error_site(void* stream, unsigned int* site);
+
+/*
+ * Self-test of the bounded waits that every kernel of this library uses (no
+ * counterpart on the pages).  Enqueues on `stream` one CTA whose waits can never
+ * be satisfied: one thread waits on an mbarrier that nothing arrives on, with a
+ * limit of limit_cycles SM clock cycles, gives up, records NF4_ERR_TIMEOUT and
+ * where it waited in the library's status word (the same path a stalled
+ * pipeline takes), and raises the CTA's abort flag; a second thread, waiting
+ * with the normal limit on another such barrier, must return as soon as it
+ * sees that flag.  Both exit; the GPU context stays usable.  The next
+ * nf4_check_error_site then reports NF4_ERR_TIMEOUT with site = {1 (block 0),
+ * 0 (thread 0), the barrier's shared-memory address, 0 (parity)} and clears it.
+ *   limit_cycles  1000 .. 2e9
+ *   where         device memory for 3 words: [0] the barrier's shared-memory
+ *                 address, [1] 1 if the first wait returned success (it must
+ *                 not), [2] 1 if the second wait did (it must not)
+ * Returns NF4_ERR_INVALID for arguments outside these rules (nothing enqueued).
+ */
+int nf4_watchdog_selftest(long long limit_cycles, unsigned int* where, void* stream);
 
 /*
  * Backward of RMS layer normalisation (page "trueno-gpu 0.4.17 --

@@ -133,3 +133,42 @@ def test_forward_and_rms_norm_validation_before_any_device_work(lib):
                                  None) == nb.NF4_ERR_ALIGN
     assert lib.rms_norm_backward(fake, fake, fake, fake, fake, fake, 4, 64, None, 0,
                                  None) == nb.NF4_ERR_WORKSPACE
+
+
+def test_grouped_bindings_check_every_item_before_any_launch(monkeypatch):
+    """The grouped bindings apply the single-call rules to every item (N equal to
+    the weight's, out float32 [M, K], the weight's codes and scales of the right
+    size) and raise before the library is called or anything is allocated."""
+    import torch
+
+    import backward_gemm_gb300 as nb
+
+    def no_library():
+        raise AssertionError("the library was reached")
+
+    monkeypatch.setattr(nb, "lib", no_library)
+    M, N, K = 100, 64, 128
+    w = nb.NF4Weight(torch.zeros((N, K // 2), dtype=torch.uint8), torch.zeros((N, K // 64)), K, N)
+    go = torch.zeros((M, N))
+    good_out = torch.zeros((M, K))
+    cases = {
+        "out too small": (go, w, torch.zeros((M, K - 64))),
+        "out not float32": (go, w, torch.zeros((M, K), dtype=torch.float16)),
+        "N differs from the weight's": (torch.zeros((M, N + 8)), w, good_out),
+        "codes of the wrong size": (go, nb.NF4Weight(torch.zeros((N, K // 4), dtype=torch.uint8),
+                                                     w.scales, K, N), good_out),
+        "scales of the wrong size": (go, nb.NF4Weight(w.data, torch.zeros((N, 1)), K, N), good_out),
+        "grad_out not 2-D": (torch.zeros((M, N, 1)), w, good_out),
+    }
+    for what, bad in cases.items():
+        for call in (nb.backward_a_batched, nb.backward_a_batched_ws, nb.backward_a_batched_noalloc):
+            with pytest.raises(ValueError):
+                call([(go, w, good_out), bad])
+        with pytest.raises(ValueError):
+            nb.backward_a(bad[0], bad[1], bad[2])
+    # A well-formed item still needs CUDA tensors: refused on the host as well.
+    with pytest.raises(ValueError, match="CUDA"):
+        nb.backward_a_batched([(go, w, good_out)])
+    # The no-allocation call never creates outputs.
+    with pytest.raises(ValueError):
+        nb.backward_a_batched_noalloc([(go, w, None)])
