@@ -50,6 +50,8 @@ def lib():
                                            C.c_int, vp, vp]
         L.nf4o_backward_a.argtypes = [vp, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int,
                                       vp, vp]
+        L.nf4o_backward_a_fused_rows.argtypes = [C.c_int, vp, vp, vp, C.c_int, C.c_int, vp,
+                                                 C.c_int, vp, vp]
         L.nf4o_forward_rows.argtypes = [vp, vp, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp]
         L.nf4o_forward.argtypes = [vp, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, vp, vp]
         L.nf4o_set_threads.argtypes = [C.c_int]
@@ -161,6 +163,29 @@ def backward_a(go: np.ndarray, dtype: int, scales: np.ndarray, data: np.ndarray,
     rc = lib().nf4o_backward_a(_p(go), dtype, _p(scales), _p(data), M, N, K, _p(ref),
                                _p(bound) if want_bound else None)
     _check(rc, "backward_a")
+    return ref, bound
+
+
+def backward_a_fused_rows(go16s, bts, rows, want_bound: bool = True):
+    """fp64 rows of the fused input gradient sum_p f16(go_p) @ deq(B_p)^T from
+    f16 operands: go16s[p] [M, N_p], bts[p] = deq(B_p) transposed [N_p, K]."""
+    go16s = [np.ascontiguousarray(g, dtype=np.uint16) for g in go16s]
+    bts = [np.ascontiguousarray(b, dtype=np.uint16) for b in bts]
+    P = len(go16s)
+    assert P == len(bts) and P > 0
+    M = go16s[0].shape[0]
+    K = bts[0].shape[1]
+    Ns = np.array([g.shape[1] for g in go16s], dtype=np.int32)
+    for g, b in zip(go16s, bts):
+        assert g.shape[0] == M and b.shape == (g.shape[1], K)
+    gp = (C.c_void_p * P)(*[g.ctypes.data for g in go16s])
+    bp = (C.c_void_p * P)(*[b.ctypes.data for b in bts])
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    ref = np.empty((rows.size, K), dtype=np.float64)
+    bound = np.empty((rows.size, K), dtype=np.float64) if want_bound else None
+    rc = lib().nf4o_backward_a_fused_rows(P, gp, bp, _p(Ns), M, K, _p(rows), rows.size, _p(ref),
+                                          _p(bound) if want_bound else None)
+    _check(rc, "backward_a_fused_rows")
     return ref, bound
 
 

@@ -280,6 +280,52 @@ int nf4o_backward_a(const void* go, int dtype, const float* scales,
     return rc;
 }
 
+/* Sibling-projection fusion: the input gradient of a layer input x that feeds
+ * several projections p (q, k and v; or gate and up), each with its own NF4
+ * weight B_p [K x N_p] and output gradient go_p [M x N_p], is the sum of their
+ * backward-A products ([P1] struct doc comment: 7 backward projections per
+ * layer, q/k/v and gate/up sharing the layer's input width K):
+ *     grad_x[m][k] = sum_p sum_n f16(go_p)[m][n] * deq(B_p)[k][n].
+ * One fp64 accumulator per element, parts in order, n ascending within a part;
+ * bound = the same sum over absolute values (may be NULL).  go16[p] is [M][N[p]]
+ * f16 bits, bt[p] is deq(B_p) transposed, [N[p]][K] f16 bits. */
+int nf4o_backward_a_fused_rows(int parts, const uint16_t* const* go16,
+                               const uint16_t* const* bt, const int* N, int M, int K,
+                               const int* rows, int nrows, double* ref, double* bound) {
+    if (parts <= 0 || !go16 || !bt || !N || !rows || !ref || M < 0 || K <= 0 || nrows < 0)
+        return -1;
+    for (int p = 0; p < parts; ++p)
+        if (!go16[p] || !bt[p] || N[p] <= 0) return -1;
+    for (int i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= M) return -2;
+    double* f16v = (double*)malloc(sizeof(double) * 65536);
+    if (!f16v) return -3;
+    for (int h = 0; h < 65536; ++h) f16v[h] = nf4o_f16_to_f64((uint16_t)h);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < nrows; ++i) {
+        const long long m = rows[i];
+        double* r = ref + (long long)i * K;
+        double* a = bound ? bound + (long long)i * K : NULL;
+        for (int k = 0; k < K; ++k) {
+            r[k] = 0.0;
+            if (a) a[k] = 0.0;
+        }
+        for (int p = 0; p < parts; ++p) {
+            for (int n = 0; n < N[p]; ++n) {
+                const double g = f16v[go16[p][m * N[p] + n]];
+                const uint16_t* col = bt[p] + (long long)n * K;
+                for (int k = 0; k < K; ++k) {
+                    const double q = g * f16v[col[k]];
+                    r[k] += q;
+                    if (a) a[k] += fabs(q);
+                }
+            }
+        }
+    }
+    free(f16v);
+    return 0;
+}
+
 /* Forward product C[M x N] = A[M x K] @ deq(B)[K x N] (the module header of
  * [P1] names this forward kernel as the one the backward is the transposed
  * counterpart of; shared dimension K).  The operands are rounded as in the

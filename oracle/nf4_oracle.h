@@ -76,6 +76,15 @@ int nf4o_backward_a(const void* go, int dtype, const float* scales,
                     const uint8_t* data, int M, int N, int K,
                     double* ref, double* bound);
 
+/* Sibling-projection fusion: the input gradient of a layer input shared by
+ * `parts` projections, ref[i][k] = sum over parts p, then n < N[p], of
+ * f16(go_p)[rows[i], n] * deq(B_p)[k, n], one fp64 sum per element (parts in
+ * order, n ascending); bound the same over |products| (may be NULL).  go16[p]
+ * is [M][N[p]] f16 bits, bt[p] is [N[p]][K] f16 bits. */
+int nf4o_backward_a_fused_rows(int parts, const uint16_t* const* go16,
+                               const uint16_t* const* bt, const int* N, int M, int K,
+                               const int* rows, int nrows, double* ref, double* bound);
+
 /* Forward product: ref[i][n] = sum_k f16(A)[rows[i], k] * deq(B)[k, n], in
  * fp64, k ascending; bound[i][n] the same over |products| (may be NULL).  a16
  * is [M][K] f16 bits, bt is deq(B) transposed, [N][K] f16 bits. */

@@ -373,3 +373,72 @@ def test_forward_rows_entry_matches_full():
                                oracle.dequantize_f16(scales, data, 128, 32), [0, 9, 16])
     np.testing.assert_array_equal(r, ref[[0, 9, 16]])
     np.testing.assert_array_equal(b, bound[[0, 9, 16]])
+
+
+# ---------------------------------------------------------------- fused sibling projections
+# grad_x = sum_p f16(go_p) @ deq(B_p)^T over projections that share the layer
+# input (q/k/v, gate/up): page "aprender-gpu 0.32.0 -- src/kernels/backward/
+# nf4_tensor_core.rs", struct doc comment (7 backward projections per layer)
+# and the Qwen-dimension test (q/k/v and gate/up share the input width).
+def _fused_case(M, Ns, K, seed):
+    go16s, bts = [], []
+    for j, N in enumerate(Ns):
+        p, go, data, scales = _small_case(M, N, K, seed=seed + j)
+        go16s.append(oracle.round_operand(go, F32))
+        bts.append(oracle.dequantize_f16(scales, data, K, N))
+    return go16s, bts
+
+
+def test_fused_exact_rational_sum():
+    M, Ns, K = 5, (16, 8, 24), 64
+    go16s, bts = _fused_case(M, Ns, K, 31)
+    ref, bound = oracle.backward_a_fused_rows(go16s, bts, np.arange(M))
+    g = [x.view(np.float16).astype(np.float64) for x in go16s]
+    b = [x.view(np.float16).astype(np.float64) for x in bts]
+    for m in range(M):
+        for k in range(0, K, 7):
+            exact = sum(Fraction(g[p][m, n]) * Fraction(b[p][n, k])
+                        for p in range(3) for n in range(Ns[p]))
+            assert abs(ref[m, k] - float(exact)) <= 1e-15 * bound[m, k] + 1e-300
+            ab = sum(abs(Fraction(g[p][m, n]) * Fraction(b[p][n, k]))
+                     for p in range(3) for n in range(Ns[p]))
+            assert bound[m, k] == pytest.approx(float(ab), rel=1e-15)
+
+
+def test_fused_equals_sum_of_separate_products_on_exact_inputs():
+    """grad_out values on a coarse grid (multiples of 1/8 up to 4): every product
+    and every partial sum is exact in fp64, so the fused sum must equal the sum
+    of the separate backward-A products bit for bit."""
+    M, Ns, K = 9, (64, 16, 40), 128
+    go16s, bts = [], []
+    for j, N in enumerate(Ns):
+        p, go, data, scales = _small_case(M, N, K, seed=41 + j)
+        go = np.clip(np.round(go * 8) / 8, -4, 4).astype(np.float32)
+        go16s.append(oracle.round_operand(go, F32))
+        bts.append(oracle.dequantize_f16(scales, data, K, N))
+    fused, _ = oracle.backward_a_fused_rows(go16s, bts, np.arange(M))
+    parts = [oracle.backward_a_rows(g, b, np.arange(M))[0] for g, b in zip(go16s, bts)]
+    np.testing.assert_array_equal(fused, parts[0] + parts[1] + parts[2])
+
+
+def test_fused_one_hot_rows_recover_one_projections_dequantised_columns():
+    M, Ns, K = 4, (32, 16, 48), 192
+    _, bts = _fused_case(1, Ns, K, 51)
+    one = np.float16(1.0).view(np.uint16)
+    picks = [(0, 0), (1, 15), (2, 47), (2, 16)]  # (part, n) per row
+    go16s = [np.zeros((M, N), dtype=np.uint16) for N in Ns]
+    for m, (p, n) in enumerate(picks):
+        go16s[p][m, n] = one
+    ref, _ = oracle.backward_a_fused_rows(go16s, bts, np.arange(M))
+    for m, (p, n) in enumerate(picks):
+        np.testing.assert_array_equal(ref[m], bts[p][n].view(np.float16).astype(np.float64))
+
+
+def test_fused_matches_torch_fp64_matmul_of_the_concatenation():
+    M, Ns, K = 20, (96, 32, 32), 256
+    go16s, bts = _fused_case(M, Ns, K, 61)
+    ref, _ = oracle.backward_a_fused_rows(go16s, bts, np.arange(M), want_bound=False)
+    g = np.concatenate([x.view(np.float16).astype(np.float64) for x in go16s], axis=1)
+    b = np.concatenate([x.view(np.float16).astype(np.float64) for x in bts], axis=0)
+    want = torch.from_numpy(g) @ torch.from_numpy(b)
+    np.testing.assert_allclose(ref, want.numpy(), rtol=1e-12, atol=1e-300)
