@@ -52,6 +52,8 @@ def lib():
                                       vp, vp]
         L.nf4o_backward_a_fused_rows.argtypes = [C.c_int, vp, vp, vp, C.c_int, C.c_int, vp,
                                                  C.c_int, vp, vp]
+        L.nf4o_gemm_backward_b_rows.argtypes = [vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp,
+                                                C.c_int, vp, vp]
         L.nf4o_forward_rows.argtypes = [vp, vp, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp, vp]
         L.nf4o_forward.argtypes = [vp, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, vp, vp]
         L.nf4o_set_threads.argtypes = [C.c_int]
@@ -186,6 +188,30 @@ def backward_a_fused_rows(go16s, bts, rows, want_bound: bool = True):
     rc = lib().nf4o_backward_a_fused_rows(P, gp, bp, _p(Ns), M, K, _p(rows), rows.size, _p(ref),
                                           _p(bound) if want_bound else None)
     _check(rc, "backward_a_fused_rows")
+    return ref, bound
+
+
+HALF_F16 = 0
+HALF_BF16 = 1
+
+
+def gemm_backward_b_rows(a: np.ndarray, gc: np.ndarray, dtype16: int, rows=None,
+                         want_bound: bool = True):
+    """fp64 rows of the dense weight gradient grad_B = A^T @ grad_C from 16-bit
+    operands given as raw bits (uint16): a [M, K], gc [M, N]; dtype16 HALF_F16
+    or HALF_BF16.  rows: the output rows k (default all).  Returns (ref, bound),
+    each [len(rows), N]."""
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    gc = np.ascontiguousarray(gc, dtype=np.uint16)
+    M, K = a.shape
+    M2, N = gc.shape
+    assert M == M2
+    rows = np.arange(K, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    ref = np.empty((rows.size, N), dtype=np.float64)
+    bound = np.empty((rows.size, N), dtype=np.float64) if want_bound else None
+    rc = lib().nf4o_gemm_backward_b_rows(_p(a), _p(gc), int(dtype16), M, K, N, _p(rows), rows.size,
+                                         _p(ref), _p(bound) if want_bound else None)
+    _check(rc, "gemm_backward_b_rows")
     return ref, bound
 
 

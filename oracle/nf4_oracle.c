@@ -6,6 +6,9 @@
  * so that no a*b+c is fused and every float operation rounds as written.
  *
  * Sources followed, by page and section:
+ *   [P3]  "trueno-gpu 0.4.17 -- src/kernels/backward/mod.rs", module list
+ *         (GemmBackwardAKernel / GemmBackwardBKernel: gradients of both
+ *         operands of a matrix product) and its parameter test.
  *   [P1]  "aprender-gpu 0.32.0 -- src/kernels/backward/nf4_tensor_core.rs"
  *         struct doc comment: grad_A = grad_out @ dequant(B_nf4)^T, shared
  *         dimension N, output dimension K.
@@ -378,6 +381,53 @@ int nf4o_forward(const void* a, int dtype, const float* scales, const uint8_t* d
     free(bt);
     free(rows);
     return rc;
+}
+
+/* Dense weight gradient of C = A @ B ([P3] "trueno-gpu 0.4.17 --
+ * src/kernels/backward/mod.rs": GemmBackwardBKernel, "matrix multiplication
+ * gradients for A and B", kernel parameters a_ptr and grad_b_ptr):
+ *     grad_B[k][n] = sum_m A[m][k] * grad_C[m][n]      (grad_B = A^T @ grad_C)
+ * for the trainable (dense, 16-bit) weights next to the frozen NF4 base.  The
+ * page does not print the kernel; this is the plain definition.  A [M][K] and
+ * grad_C [M][N] are 16-bit floats given as raw bits (dtype16 0: f16, 1: bf16),
+ * widened exactly; the sum runs over m ascending in fp64.  ref and bound are
+ * [nrows][N] for the output rows k = rows[i]; bound (may be NULL) the same sum
+ * over absolute values. */
+static double half_to_f64(uint16_t h, int dtype16) {
+    return dtype16 == 1 ? (double)nf4o_bf16_to_f32(h) : nf4o_f16_to_f64(h);
+}
+
+int nf4o_gemm_backward_b_rows(const uint16_t* a, const uint16_t* gc, int dtype16, int M, int K,
+                              int N, const int* rows, int nrows, double* ref, double* bound) {
+    if (!a || !gc || !rows || !ref || (dtype16 != 0 && dtype16 != 1) || M < 0 || K <= 0 ||
+        N <= 0 || nrows < 0)
+        return -1;
+    for (int i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= K) return -2;
+    double* v = (double*)malloc(sizeof(double) * 65536);
+    if (!v) return -3;
+    for (int h = 0; h < 65536; ++h) v[h] = half_to_f64((uint16_t)h, dtype16);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < nrows; ++i) {
+        const int k = rows[i];
+        double* r = ref + (long long)i * N;
+        double* b = bound ? bound + (long long)i * N : NULL;
+        for (int n = 0; n < N; ++n) {
+            r[n] = 0.0;
+            if (b) b[n] = 0.0;
+        }
+        for (int m = 0; m < M; ++m) {
+            const double x = v[a[(long long)m * K + k]];
+            const uint16_t* g = gc + (long long)m * N;
+            for (int n = 0; n < N; ++n) {
+                const double q = x * v[g[n]];
+                r[n] += q;
+                if (b) b[n] += fabs(q);
+            }
+        }
+    }
+    free(v);
+    return 0;
 }
 
 void nf4o_set_threads(int n) {

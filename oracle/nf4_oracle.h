@@ -96,6 +96,13 @@ int nf4o_forward_rows(const uint16_t* a16, const uint16_t* bt, int M, int N, int
 int nf4o_forward(const void* a, int dtype, const float* scales, const uint8_t* data,
                  int M, int N, int K, double* ref, double* bound);
 
+/* Dense weight gradient grad_B = A^T @ grad_C of C = A @ B (A [M][K], grad_C
+ * [M][N], 16-bit floats as raw bits: dtype16 0 = f16, 1 = bf16): ref[i][n] =
+ * sum_m A[m][rows[i]] * grad_C[m][n] in fp64, m ascending; bound the same over
+ * |products| (may be NULL).  ref and bound are [nrows][N]. */
+int nf4o_gemm_backward_b_rows(const uint16_t* a, const uint16_t* gc, int dtype16, int M, int K,
+                              int N, const int* rows, int nrows, double* ref, double* bound);
+
 /* OpenMP thread control for the row loops (1 when built without OpenMP). */
 void nf4o_set_threads(int n);
 int nf4o_max_threads(void);

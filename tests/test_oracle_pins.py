@@ -442,3 +442,59 @@ def test_fused_matches_torch_fp64_matmul_of_the_concatenation():
     b = np.concatenate([x.view(np.float16).astype(np.float64) for x in bts], axis=0)
     want = torch.from_numpy(g) @ torch.from_numpy(b)
     np.testing.assert_allclose(ref, want.numpy(), rtol=1e-12, atol=1e-300)
+
+
+# ---------------------------------------------------------------- dense GemmBackwardB
+# grad_B = A^T @ grad_C (page "trueno-gpu 0.4.17 -- src/kernels/backward/mod.rs",
+# module list: GEMM gradients for A and B; GemmBackwardBKernel's a_ptr and
+# grad_b_ptr parameters), 16-bit operands, fp64 sum over the tokens m.
+def _half_case(M, K, N, dtype16, seed):
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randn(M, K, generator=g) * 0.5
+    c = torch.randn(M, N, generator=g) * 0.01
+    dt = torch.bfloat16 if dtype16 == oracle.HALF_BF16 else torch.float16
+    a, c = a.to(dt), c.to(dt)
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    return bits(a), bits(c), a.double().numpy(), c.double().numpy()
+
+
+@pytest.mark.parametrize("dtype16", [oracle.HALF_F16, oracle.HALF_BF16])
+def test_gemm_backward_b_exact_rational_sum(dtype16):
+    M, K, N = 24, 6, 10
+    a, c, af, cf = _half_case(M, K, N, dtype16, 5)
+    ref, bound = oracle.gemm_backward_b_rows(a, c, dtype16)
+    for k in range(K):
+        for n in range(N):
+            exact = sum(Fraction(af[m, k]) * Fraction(cf[m, n]) for m in range(M))
+            assert abs(ref[k, n] - float(exact)) <= 1e-15 * bound[k, n] + 1e-300
+            ab = sum(abs(Fraction(af[m, k]) * Fraction(cf[m, n])) for m in range(M))
+            assert bound[k, n] == pytest.approx(float(ab), rel=1e-15)
+
+
+@pytest.mark.parametrize("dtype16", [oracle.HALF_F16, oracle.HALF_BF16])
+def test_gemm_backward_b_matches_torch_fp64(dtype16):
+    M, K, N = 300, 40, 72
+    a, c, af, cf = _half_case(M, K, N, dtype16, 9)
+    ref, _ = oracle.gemm_backward_b_rows(a, c, dtype16, want_bound=False)
+    want = torch.from_numpy(af).T @ torch.from_numpy(cf)
+    np.testing.assert_allclose(ref, want.numpy(), rtol=1e-12, atol=1e-300)
+    # Sampled output rows equal the same rows of the whole result.
+    rows = np.array([0, 7, 39], dtype=np.int32)
+    sub, _ = oracle.gemm_backward_b_rows(a, c, dtype16, rows=rows)
+    np.testing.assert_array_equal(sub, ref[rows])
+
+
+def test_gemm_backward_b_one_hot_tokens_pick_rows_of_grad_c():
+    """A one-hot in column k of token m makes row k of grad_B equal to row m
+    of grad_C exactly; a token with A = 0 contributes nothing."""
+    M, K, N = 8, 5, 24
+    _, c, _, cf = _half_case(M, K, N, oracle.HALF_BF16, 13)
+    one = np.uint16(0x3F80)  # bf16 1.0
+    a = np.zeros((M, K), dtype=np.uint16)
+    picks = {0: 3, 2: 6, 4: 1}  # k -> m
+    for k, m in picks.items():
+        a[m, k] = one
+    ref, _ = oracle.gemm_backward_b_rows(a, c, oracle.HALF_BF16)
+    for k in range(K):
+        want = cf[picks[k]] if k in picks else np.zeros(N)
+        np.testing.assert_array_equal(ref[k], want)
