@@ -39,6 +39,11 @@ class Nf4Problem(C.Structure):
                 ("grad_A", _vp), ("M", _i), ("N", _i), ("K", _i)]
 
 
+class Nf4Part(C.Structure):
+    """Mirror of ``nf4_part``."""
+    _fields_ = [("grad_out", _vp), ("go_dtype", _i), ("N", _i)]
+
+
 SIGNATURES = {
     "nf4_abi_version": (_i, []),
     "nf4_status_string": (C.c_char_p, [_i]),
@@ -66,6 +71,10 @@ SIGNATURES = {
     "nf4_set_small_m_max": (_i, [_i]),
     "nf4_small_m_split": (_i, [_i, _i, _i, _i, C.POINTER(_i)]),
     "nf4_watchdog_selftest": (_i, [C.c_longlong, _vp, _vp]),
+    "nf4_backward_a_fused": (_i, [C.POINTER(Nf4Part), _i, _vp, _vp, _vp, _i, _i, _vp, _sz, _vp]),
+    "nf4_gemm_backward_b_splits": (_i, [_i, _i, _i, _i]),
+    "nf4_gemm_backward_b_ws_bytes": (_sz, [_i, _i, _i]),
+    "nf4_gemm_backward_b": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -347,6 +356,89 @@ def rms_norm_backward(x: torch.Tensor, gamma: torch.Tensor, rms: torch.Tensor,
                                    _ptr(workspace) if want_gamma else None, nbytes, _stream()),
            "rms_norm_backward")
     return out, dgamma
+
+
+def stack_weights(weights) -> NF4Weight:
+    """The NF4 weights of sibling projections (same K) stacked along N, in order:
+    their codes and scales concatenated row-wise (the layout
+    :func:`backward_a_fused` reads; equal to quantising the concatenated dense
+    weights, since every 64-element block lies within one column)."""
+    weights = list(weights)
+    K = weights[0].K
+    if any(w.K != K for w in weights):
+        raise ValueError("stacked weights must share K")
+    return NF4Weight(torch.cat([w.data for w in weights], 0),
+                     torch.cat([w.scales for w in weights], 0), K, sum(w.N for w in weights))
+
+
+def backward_a_fused(grad_outs, w: NF4Weight, workspace: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None):
+    """grad_x [M, K] = sum_p grad_outs[p] [M, N_p] @ dequant(B_p)^T in one GEMM
+    (``nf4_backward_a_fused``): ``w`` is the projections' weights stacked along
+    N (:func:`stack_weights`), ``grad_outs`` their output gradients in the same
+    order (float32, bfloat16 or float16; every N_p a multiple of 8)."""
+    grad_outs = list(grad_outs)
+    if not grad_outs:
+        raise ValueError("at least one part")
+    M = grad_outs[0].shape[0] if grad_outs[0].dim() == 2 else -1
+    for i, g in enumerate(grad_outs):
+        if g.dim() != 2 or g.shape[0] != M:
+            raise ValueError(f"part {i}: grad_out must be [M, N_p] with M={M}")
+        _dtype_code(g)
+    if sum(g.shape[1] for g in grad_outs) != w.N:
+        raise ValueError(f"the parts' N sum to {sum(g.shape[1] for g in grad_outs)}, "
+                         f"the stacked weight has N={w.N}")
+    if out is not None and (out.dtype != torch.float32 or tuple(out.shape) != (M, w.K)):
+        raise ValueError(f"out must be float32 [M, K] = [{M}, {w.K}]")
+    for i, g in enumerate(grad_outs):
+        _require_cuda_contig(f"part {i}: grad_out", g)
+    for name, t in (("weight codes", w.data), ("weight scales", w.scales)):
+        _require_cuda_contig(name, t)
+    dev = grad_outs[0].device
+    if out is None:
+        out = torch.empty((M, w.K), dtype=torch.float32, device=dev)
+    _require_cuda_contig("out", out)
+    if workspace is None:
+        workspace = ws_workspace(M, w.N, dev)
+    _require_cuda_contig("workspace", workspace)
+    arr = (Nf4Part * len(grad_outs))()
+    for i, g in enumerate(grad_outs):
+        arr[i] = Nf4Part(g.data_ptr(), _dtype_code(g), g.shape[1])
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().nf4_backward_a_fused(arr, len(grad_outs), _ptr(w.scales), _ptr(w.data), _ptr(out),
+                                      M, w.K, _ptr(workspace), nbytes, _stream()),
+           "nf4_backward_a_fused")
+    return out
+
+
+def gemm_backward_b(A: torch.Tensor, grad_C: torch.Tensor, workspace: torch.Tensor | None = None,
+                    out: torch.Tensor | None = None):
+    """grad_B [K, N] fp32 = A[M, K]^T @ grad_C[M, N] through ``nf4_gemm_backward_b``
+    (the weight gradient of C = A @ B): A and grad_C both bfloat16 or both
+    float16, K and N multiples of 8.  A workspace (default: allocated here when
+    the call splits the tokens) holds per-split partial sums."""
+    if A.dim() != 2 or grad_C.dim() != 2 or A.shape[0] != grad_C.shape[0]:
+        raise ValueError("A must be [M, K] and grad_C [M, N] with the same M")
+    if A.dtype != grad_C.dtype or A.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("A and grad_C must both be bfloat16 or both float16")
+    M, K = A.shape
+    N = grad_C.shape[1]
+    if out is not None and (out.dtype != torch.float32 or tuple(out.shape) != (K, N)):
+        raise ValueError(f"out must be float32 [K, N] = [{K}, {N}]")
+    _require_cuda_contig("A", A)
+    _require_cuda_contig("grad_C", grad_C)
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.float32, device=A.device)
+    _require_cuda_contig("out", out)
+    if workspace is None:
+        n = int(lib().nf4_gemm_backward_b_ws_bytes(M, K, N))
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=A.device)
+    _require_cuda_contig("workspace", workspace)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().nf4_gemm_backward_b(_ptr(A), _ptr(grad_C), _dtype_code(A), _ptr(out), M, K, N,
+                                     _ptr(workspace), nbytes, _stream()),
+           "nf4_gemm_backward_b")
+    return out
 
 
 def fwd_workspace(M: int, K: int, device=None) -> torch.Tensor:

@@ -21,7 +21,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libnf4bwd.so")
 
 SOURCES = ["nf4_quant.cu", "nf4_gemm.cu", "rms_norm_bwd.cu"]
-HEADERS = ["ptx.cuh", "nf4_dequant.cuh", "nf4_common.h"]
+HEADERS = ["ptx.cuh", "nf4_dequant.cuh", "nf4_common.h", "pair_kernel.cuh", "prepass.cuh",
+           "host_plan.cuh", "small_m_host.cuh", "nf4_small_m.cuh", "nf4_trace.cuh",
+           "dense_gemm.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
               "--expt-relaxed-constexpr", "-diag-suppress", "1160"]
@@ -46,9 +48,22 @@ def is_stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
+def _defines() -> list[str]:
+    """Diagnostic builds: NF4BWD_DEFINES="NF4_TRACE" (clock probes, read back
+    through nf4_debug_set_trace) or "NF4_PROGRESS" (per-role progress counters,
+    nf4_debug_set_progress), comma-separated.  Product builds define neither."""
+    names = [d.strip() for d in os.environ.get("NF4BWD_DEFINES", "").split(",") if d.strip()]
+    allowed = {"NF4_TRACE", "NF4_PROGRESS"}
+    bad = [d for d in names if d not in allowed]
+    if bad:
+        raise RuntimeError(f"NF4BWD_DEFINES: unknown {bad}; allowed {sorted(allowed)}")
+    return [f"-D{d}" for d in names]
+
+
 def _compile(src: str, extra: list[str]) -> str:
     obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *_defines(), *extra, "-c", os.path.join(CSRC, src), "-o",
+           obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")

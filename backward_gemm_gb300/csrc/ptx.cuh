@@ -362,6 +362,20 @@ __device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t
                : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16) of global memory at p (16-byte
+// aligned) into L2 ahead of its use; no completion to wait for.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
 // Order this thread's async-proxy global accesses (bulk copies) with its
 // generic-proxy ones.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -569,10 +583,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor for kind::f16 with f16 A and B, f32 accumulator.
 // a_mn_major / b_mn_major: 0 = K-major operand, 1 = MN-major operand.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uint32_t a_mn_major,
-                                                     uint32_t b_mn_major) {
+                                                     uint32_t b_mn_major, uint32_t bf16 = 0) {
   return (1u << 4)             // D format: f32
-         | (0u << 7)           // A format: f16
-         | (0u << 10)          // B format: f16
+         | (bf16 << 7)         // A format: f16 (0) or bf16 (1)
+         | (bf16 << 10)        // B format: the same as A
          | (a_mn_major << 15)  // A major
          | (b_mn_major << 16)  // B major
          | ((N >> 3) << 17)    // N / 8

@@ -40,8 +40,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import (BF16, CONFIGS, DTYPE_NAMES, F32, Problem, full_step, make_grad_out,  # noqa
-                       make_weight)
+from workloads import (BF16, CONFIGS, DTYPE_NAMES, F32, FUSED, Problem, full_step,  # noqa
+                       make_grad_out, make_weight)
 
 L2_BYTES = 129 * 2**20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -404,6 +404,225 @@ def bench_forward(args, dev):
         "gpu_launches": steps * 2,
         "clocks": clocks.summary(),
     }
+
+
+# Fused input gradient of sibling projections (nf4_backward_a_fused): q/k/v and
+# gate/up of one layer at M = 4096, each part with its own seeded grad_out
+# (fp32) and weight; the weights stacked along N.
+def bench_fused(args, dev):
+    """nf4_backward_a_fused on rotating input sets beyond L2 (a CUDA graph of one
+    step per set), its GEMM alone (the pre-converted single call on the f16 A
+    operand the steps left in each set's workspace), the tensor roofline, the
+    clocks and the oracle's fused sum on a bounded sample."""
+    import backward_gemm_gb300 as nb
+    from backward_gemm_gb300.build import build
+
+    build()
+    nb.lib()
+    parts = FUSED[args.workload]
+    M, K = parts[0].M, parts[0].K
+    N = sum(p.N for p in parts)
+    host_go = [make_grad_out(p) for p in parts]
+    host_B = [make_weight(p) for p in parts]
+    per_set = sum(p.go_bytes for p in parts) + 4 * M * K + K * N // 2 + 2 * M * N
+    copies = max(2, min(16, -(-2 * L2_BYTES // per_set)))
+    sets = []
+    for _ in range(copies):
+        gos = [torch.from_numpy(g).to(dev) for g in host_go]
+        w = nb.stack_weights([nb.quantize(torch.from_numpy(B).to(dev)) for B in host_B])
+        sets.append((gos, w, torch.empty((M, K), device=dev), nb.ws_workspace(M, N, dev)))
+    stream = torch.cuda.Stream(device=dev)
+    steps = args.steps
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            gos, w, out, ws = sets[i % copies]
+            nb.backward_a_fused(gos, w, ws, out=out)
+        nb.check_error()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for gos, w, out, ws in sets:
+                nb.backward_a_fused(gos, w, ws, out=out)
+        graph.replay()
+        stream.synchronize()
+        full, rem = divmod(steps, copies)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index) as clocks:
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                gos, w, out, ws = sets[i]
+                nb.backward_a_fused(gos, w, ws, out=out)
+            ev1.record(stream)
+            ev1.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        # The GEMM alone: the f16 A operand [M, N] is in each set's workspace.
+        runs = [(ws[: 2 * M * N].view(torch.float16).view(M, N), w, out, ws)
+                for _, w, out, ws in sets]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        kern_steps = min(steps, 200)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(kern_steps):
+            a16, w, out, ws = runs[i % copies]
+            nb.backward_a_ws(a16, w, ws, out=out)
+        e1.record(stream)
+        e1.synchronize()
+        kern_ms = e0.elapsed_time(e1) / kern_steps
+        nb.check_error()
+    flops = 2 * M * N * K
+    alg_bytes = sum(p.go_bytes for p in parts) + K * N // 2 + 4 * N * (K // 64) + 4 * M * K
+    peaks, peak_kind = load_peaks()
+    peak_tf = peaks["bf16_tflops_sustained" if ms > 1000.0 else "bf16_tflops"]
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    line = {
+        "metric": "NF4 fused sibling-projection backward-A (grad_x = sum_p g_p @ dequant(B_p)^T) "
+                  "TFLOP/s and % of GB300 dense FP16 tensor roofline",
+        "value": flops * steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 operands, f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: M={M} K={K} parts N=" +
+                               "+".join(str(p.N) for p in parts) + " grad_out f32",
+                   "gflop_per_step": flops / 1e9, "algorithmic_mb_per_step": alg_bytes / 1e6,
+                   "l2": f"rotating {copies} input sets, {copies * per_set / 2**20:.0f} MiB > L2",
+                   "timing": f"CUDA graph of {copies} steps, CUDA events",
+                   "entry": "nf4_backward_a_fused", "parallelism": "dp1"},
+        "e2e": None,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": traffic_for(args.workload),
+                     "peak_source": f"{peak_kind} bf16 (f16 nominal rate = bf16)",
+                     "kernel": "to_f16_group_kernel + bwd_a_kernel", "kernel_ms": kern_ms,
+                     "timed": "bwd_a_kernel alone (f16 A operand entry, CUDA events, same rotating sets)"},
+        "gpu_launches": steps * 2,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline_fused(parts, host_go, host_B, args.cpu_seconds)
+    return line
+
+
+def cpu_baseline_fused(parts, host_go, host_B, budget_s: float = 15.0):
+    """The oracle's fused sum as it stands on a bounded sample of rows (about
+    50 GFLOP; dequantise, rounding and the product timed, quantise not)."""
+    import oracle
+
+    M, K = parts[0].M, parts[0].K
+    N = sum(p.N for p in parts)
+    qs = [oracle.quantize(B) for B in host_B]
+    rows = max(1, min(M, int(5e10 / (2 * N * K))))
+    t0 = time.perf_counter()
+    bts = [oracle.dequantize_f16(s, d, K, p.N) for p, (d, s) in zip(parts, qs)]
+    go16s = [oracle.round_operand(g[:rows], p.go_dtype) for p, g in zip(parts, host_go)]
+    oracle.backward_a_fused_rows(go16s, bts, np.arange(rows, dtype=np.int32), want_bound=False)
+    dt = time.perf_counter() - t0
+    return {"value": 2 * rows * N * K / dt / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.max_threads(), "kind": "oracle", "seconds": dt,
+            "sample": f"{rows} of {M} rows of the fused {M}x{N}x{K} product; fp64 sums; "
+                      "dequantise + rounding + product timed, quantise not"}
+
+
+# Dense weight gradient grad_B = A^T @ grad_C (nf4_gemm_backward_b), bf16 operands:
+# a full q_proj-shaped weight gradient (compute bound) and a rank-16 adapter's
+# gradient against the up projection's output width (HBM bound).  (M tokens,
+# K rows of grad_B, N columns)
+BWD_B_WORKLOADS = {"bwd_b_dense": (4096, 1536, 1536), "bwd_b_lora": (4096, 16, 8960)}
+
+
+def bench_backward_b(args, dev):
+    """nf4_gemm_backward_b on rotating input sets beyond L2 (a CUDA graph of one
+    step per set), the roofline of the bound that applies (tensor or HBM), the
+    clocks and the oracle on a bounded sample of output rows."""
+    import backward_gemm_gb300 as nb
+    from backward_gemm_gb300.build import build
+
+    build()
+    nb.lib()
+    M, K, N = BWD_B_WORKLOADS[args.workload]
+    g = torch.Generator().manual_seed(0)
+    a_h = (torch.randn(M, K, generator=g) * 0.5).to(torch.bfloat16)
+    c_h = (torch.randn(M, N, generator=g) * 0.01).to(torch.bfloat16)
+    per_set = 2 * M * (K + N) + 4 * K * N
+    copies = max(2, min(16, -(-2 * L2_BYTES // per_set)))
+    wsb = int(nb.lib().nf4_gemm_backward_b_ws_bytes(M, K, N))
+    sets = [(a_h.to(dev), c_h.to(dev), torch.empty((K, N), device=dev),
+             torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)) for _ in range(copies)]
+    stream = torch.cuda.Stream(device=dev)
+    steps = args.steps
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            a, c, out, ws = sets[i % copies]
+            nb.gemm_backward_b(a, c, ws, out=out)
+        nb.check_error()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for a, c, out, ws in sets:
+                nb.gemm_backward_b(a, c, ws, out=out)
+        graph.replay()
+        stream.synchronize()
+        full, rem = divmod(steps, copies)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index) as clocks:
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                a, c, out, ws = sets[i]
+                nb.gemm_backward_b(a, c, ws, out=out)
+            ev1.record(stream)
+            ev1.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        nb.check_error()
+    flops = 2 * M * K * N
+    alg_bytes = 2 * M * (K + N) + 4 * K * N
+    peaks, peak_kind = load_peaks()
+    peak_tf = peaks["bf16_tflops_sustained" if ms > 1000.0 else "bf16_tflops"]
+    step_s = ms * 1e-3 / steps
+    splits = int(nb.lib().nf4_gemm_backward_b_splits(M, K, N, 76))
+    if flops / (peak_tf * 1e12) >= alg_bytes / (peaks["hbm_gbs"] * 1e9):
+        achieved = flops / step_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf,
+                "peak_source": f"{peak_kind} bf16 {'sustained' if ms > 1000.0 else 'burst'}"}
+    else:
+        achieved = alg_bytes / step_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_kind} HBM copy"}
+    roof.update({"traffic": traffic_for(args.workload),
+                 "kernel": "backward_b_kernel" + (" + reduce_splits_kernel" if splits > 1 else ""),
+                 "kernel_ms": ms / steps, "timed": "whole step"})
+    line = {
+        "metric": "Dense GemmBackwardB (grad_B = A^T @ grad_C) TFLOP/s and % of GB300 roofline",
+        "value": flops * steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 operands, f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: M={M} tokens, K={K}, N={N}, bf16",
+                   "gflop_per_step": flops / 1e9, "algorithmic_mb_per_step": alg_bytes / 1e6,
+                   "token_splits": splits,
+                   "l2": f"rotating {copies} input sets, {copies * per_set / 2**20:.0f} MiB > L2",
+                   "timing": f"CUDA graph of {copies} steps, CUDA events",
+                   "entry": "nf4_gemm_backward_b", "parallelism": "dp1"},
+        "e2e": None,
+        "roofline": roof,
+        "gpu_launches": steps * (2 if splits > 1 else 1),
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu:
+        import oracle
+
+        bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+        rows = max(1, min(K, int(5e10 / (2 * M * N))))
+        t0 = time.perf_counter()
+        oracle.gemm_backward_b_rows(bits(a_h), bits(c_h), oracle.HALF_BF16,
+                                    rows=np.arange(rows, dtype=np.int32), want_bound=False)
+        dt_s = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 2 * M * N * rows / dt_s / 1e12, "unit": "TFLOP/s",
+                                "cores": oracle.max_threads(), "kind": "oracle", "seconds": dt_s,
+                                "sample": f"{rows} of {K} output rows; fp64 sums over {M} tokens"}
+    return line
 
 
 # Backward of RMS layer normalisation (rms_norm_backward), the step upstream of
@@ -812,7 +1031,55 @@ def bench_reference_extra(args, rank, world):
 
     build_oracle()
     per_step_s = 60.0 / max(args.steps + args.warmup, 1)
-    if args.workload in FWD_WORKLOADS:
+    if args.workload in BWD_B_WORKLOADS:
+        M, K, N = BWD_B_WORKLOADS[args.workload]
+        g = torch.Generator().manual_seed(0)
+        bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+        a_b = bits((torch.randn(M, K, generator=g) * 0.5).to(torch.bfloat16))
+        c_b = bits((torch.randn(M, N, generator=g) * 0.01).to(torch.bfloat16))
+        probe = min(K, 2)
+        t0 = time.perf_counter()
+        oracle.gemm_backward_b_rows(a_b, c_b, oracle.HALF_BF16, rows=np.arange(probe, dtype=np.int32),
+                                    want_bound=False)
+        rate = 2 * probe * M * N / max(time.perf_counter() - t0, 1e-6)
+        rows = max(1, min(K, int(rate * per_step_s / (2 * M * N))))
+
+        def step():
+            oracle.gemm_backward_b_rows(a_b, c_b, oracle.HALF_BF16,
+                                        rows=np.arange(rows, dtype=np.int32), want_bound=False)
+
+        metric = "Dense GemmBackwardB (grad_B = A^T @ grad_C) TFLOP/s and % of GB300 roofline"
+        unit, per_row = "TFLOP/s", 2 * M * N
+        workload = f"{args.workload}: M={M} tokens, K={K}, N={N}, bf16"
+        what = f"of {K} output rows of the {M}-token weight gradient per step (fp64 sums)"
+    elif args.workload in FUSED:
+        parts = FUSED[args.workload]
+        M, K = parts[0].M, parts[0].K
+        N = sum(p.N for p in parts)
+        gos = [make_grad_out(p) for p in parts]
+        qs = [oracle.quantize(make_weight(p)) for p in parts]
+        probe = 8
+        t0 = time.perf_counter()
+        bts = [oracle.dequantize_f16(s, d, K, p.N) for p, (d, s) in zip(parts, qs)]
+        oracle.backward_a_fused_rows([oracle.round_operand(g[:probe], p.go_dtype)
+                                      for p, g in zip(parts, gos)], bts,
+                                     np.arange(probe, dtype=np.int32), want_bound=False)
+        rate = 2 * probe * N * K / max(time.perf_counter() - t0, 1e-6)
+        rows = max(1, min(M, int(rate * per_step_s / (2 * N * K))))
+
+        def step():
+            b = [oracle.dequantize_f16(s, d, K, p.N) for p, (d, s) in zip(parts, qs)]
+            oracle.backward_a_fused_rows([oracle.round_operand(g[:rows], p.go_dtype)
+                                          for p, g in zip(parts, gos)], b,
+                                         np.arange(rows, dtype=np.int32), want_bound=False)
+
+        metric = ("NF4 fused sibling-projection backward-A (grad_x = sum_p g_p @ dequant(B_p)^T) "
+                  "TFLOP/s and % of GB300 dense FP16 tensor roofline")
+        unit, per_row = "TFLOP/s", 2 * N * K
+        workload = (f"{args.workload}: M={M} K={K} parts N=" + "+".join(str(p.N) for p in parts)
+                    + " grad_out f32")
+        what = f"of {M} rows of the fused {M}x{N}x{K} product per step (dequantise + rounding + fp64 rows)"
+    elif args.workload in FWD_WORKLOADS:
         M, N, K, dt, a_std, b_std, outl, seed = FWD_WORKLOADS[args.workload]
         a = make_grad_out(Problem(M, K, N, dt, a_std, b_std, outl, seed))
         data, scales = oracle.quantize(make_weight(Problem(M, N, K, dt, a_std, b_std, outl, seed + 1)))
@@ -876,7 +1143,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="full_step",
-                    choices=sorted(workloads()) + sorted(FWD_WORKLOADS) + sorted(RMSNORM_WORKLOADS))
+                    choices=sorted(workloads()) + sorted(FWD_WORKLOADS) + sorted(RMSNORM_WORKLOADS)
+                    + sorted(FUSED) + sorted(BWD_B_WORKLOADS))
     ap.add_argument("--layers", type=int, default=None,
                     help="full_step only: run the first L of the 28 layers (a small case for a "
                          "profiler capture)")
@@ -897,7 +1165,8 @@ def main():
 
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
-    if args.workload in RMSNORM_WORKLOADS or args.workload in FWD_WORKLOADS:
+    if args.workload in RMSNORM_WORKLOADS or args.workload in FWD_WORKLOADS or \
+            args.workload in FUSED or args.workload in BWD_B_WORKLOADS:
         if args.impl == "reference":
             line = bench_reference_extra(args, rank, world)
         elif world > 1:
@@ -905,7 +1174,10 @@ def main():
         else:
             dev = torch.device("cuda", local)
             torch.cuda.set_device(dev)
-            line = (bench_rmsnorm if args.workload in RMSNORM_WORKLOADS else bench_forward)(args, dev)
+            line = (bench_rmsnorm if args.workload in RMSNORM_WORKLOADS else
+                    bench_fused if args.workload in FUSED else
+                    bench_backward_b if args.workload in BWD_B_WORKLOADS else
+                    bench_forward)(args, dev)
     elif args.impl == "reference":
         line = bench_reference(args, rank, world)
     else:

@@ -169,6 +169,50 @@ size_t nf4_forward_ws_bytes(int M, int K);
 int nf4_forward_ws(const void* A, int a_dtype, const float* scales, const uint8_t* data, float* C,
                    int M, int N, int K, void* workspace, size_t workspace_bytes, void* stream);
 
+/* One projection of a fused call (nf4_backward_a_fused). */
+typedef struct nf4_part {
+  const void* grad_out; /* [M][N] of type go_dtype, 16-byte aligned */
+  int go_dtype;         /* NF4_F32, NF4_BF16 or NF4_F16 */
+  int N;                /* the projection's output width, a positive multiple of 8 */
+} nf4_part;
+
+/*
+ * Input gradient of a layer input shared by several projections, summed in
+ * one GEMM:
+ *
+ *     grad_x[M x K] = sum_p grad_out_p[M x N_p] @ dequant(B_p[K x N_p])^T
+ *
+ * The page's doc comment counts 7 backward projections per layer (page above,
+ * struct doc comment); q, k and v read the same layer input, as do gate and up
+ * (the same page's Qwen-dimension test: q/k/v and gate/up share the input width
+ * K), so their input gradients add.  Summing them over the concatenated shared
+ * dimension N = sum N_p in one accumulator replaces count separate grad_A
+ * results and their addition.  The pages do not spell the fusion out; this is
+ * the sum of the backward-A products, each with the arithmetic of
+ * nf4_backward_a_ws (operands rounded to f16, f32 accumulation).  Two launches
+ * on `stream`: a pass writes each part's grad_out, rounded to f16, into its
+ * columns of one A operand in `workspace`, then the pair kernel runs the
+ * single problem M x N x K (every M: no few-token path).  The result equals,
+ * bit for bit, nf4_backward_a_ws on the column-wise concatenation of the
+ * grad_out parts with the stacked weight.
+ *   parts    HOST array of `count` parts (1..64), read before the call returns
+ *   scales, data  the parts' NF4 weights stacked along N in part order:
+ *            data [sum N_p][K/2], scales [sum N_p][K/64] (rows of each
+ *            weight's data and scales concatenated; this is what nf4_quantize
+ *            gives for the dense weights concatenated along N, since every
+ *            64-element block lies within one column)
+ *   grad_x   [M][K] fp32, 16-byte aligned, overwritten
+ *   K        positive multiple of 64; M == 0 enqueues nothing
+ *   workspace, workspace_bytes  as nf4_backward_a_ws with N = sum N_p: at least
+ *            the f16 copy (2 * M * sum N_p bytes); nf4_backward_a_ws_bytes(M,
+ *            sum N_p) bytes allow the split of a last partial wave
+ * Returns NF4_ERR_INVALID, NF4_ERR_ALIGN or NF4_ERR_WORKSPACE (nothing
+ * enqueued) for arguments outside these rules.
+ */
+int nf4_backward_a_fused(const nf4_part* parts, int count, const float* scales,
+                         const uint8_t* data, float* grad_x, int M, int K, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /*
  * Tokens per pair tile, 256 or 512, that the pre-converted kernel uses for an
  * M x N x K problem run by `pairs` pairs of CTAs (pure host computation).  A
@@ -268,27 +312,36 @@ int nf4_backward_a_batched(const nf4_problem* problems, int count, void* workspa
 
 /*
  * Bytes of workspace nf4_backward_a_batched_ws needs for these problems: the
- * descriptors (the same as nf4_backward_a_batched's, rounded up to 256) plus
- * an f16 copy of every fp32 or bf16 grad_out (2 * M * ((N + 7) & ~7) bytes
- * each, rounded up to 256).  `problems` is a host array; 0 for count <= 0.
+ * descriptors (the same as nf4_backward_a_batched's, rounded up to 256), an
+ * f16 copy of every fp32 or bf16 grad_out (2 * M * ((N + 7) & ~7) bytes each,
+ * rounded up to 256), and, when at most 256 problems have such a copy, the
+ * bookkeeping of the pass that writes the copies beside the GEMM (4 bytes per
+ * 256-row block of each such problem plus 1028, rounded up to 256).  `problems`
+ * is a host array; 0 for count <= 0.
  */
 size_t nf4_backward_a_batched_ws_bytes(const nf4_problem* problems, int count);
 
 /*
  * The grouped launch of the pre-converted path (see nf4_backward_a_ws): every
- * fp32 or bf16 grad_out is rounded to f16 into the workspace by grouped
- * streaming passes, then one persistent launch of the pair kernel with
- * TMA-loaded A operands runs all problems' tiles (longest first), as a
- * programmatic dependent of the last pass.  NF4_F16 grad_out is accepted and
+ * fp32 or bf16 grad_out is rounded to f16 into the workspace, and one
+ * persistent launch of the pair kernel with TMA-loaded A operands runs all
+ * problems' tiles (longest first).  With the full workspace the rounding pass
+ * runs BESIDE the GEMM: one block of it per SM converts 64-row slabs in the
+ * GEMM's order and counts each finished slab into its 256-row block's ready
+ * word; the GEMM (a programmatic dependent of the pass, so it starts as soon
+ * as the pass has) waits for a block's count before its first copy from it.
+ * With room for the descriptors and copies only, the passes run first and the
+ * GEMM follows the last of them.  The results are the same.  NF4_F16 grad_out is accepted and
  * read in place.  Few-token problems (M at most nf4_set_small_m_max, fp32 or
  * bf16) run as their own launches of the few-token kernel, as in
  * nf4_backward_a_batched.  Each problem's grad_A equals, bit for bit, what
  * nf4_backward_a_ws gives for it without a split (tiles are never split
  * here).  No counterpart on the pages.
- *   workspace  caller-owned device memory, 256-byte aligned, at least
- *              nf4_backward_a_batched_ws_bytes(problems, count) bytes; too
- *              small, NULL or misaligned returns NF4_ERR_WORKSPACE and enqueues
- *              nothing; must not be reused until the stream has run the call
+ *   workspace  caller-owned device memory, 256-byte aligned,
+ *              nf4_backward_a_batched_ws_bytes(problems, count) bytes; smaller
+ *              than the descriptors and copies, NULL or misaligned returns
+ *              NF4_ERR_WORKSPACE and enqueues nothing; must not be reused until
+ *              the stream has run the call
  */
 int nf4_backward_a_batched_ws(const nf4_problem* problems, int count, void* workspace,
                               size_t workspace_bytes, void* stream);
@@ -322,6 +375,37 @@ int nf4_backward_a_batched_ws(const nf4_problem* problems, int count, void* work
  * It calls no cudaMalloc or cudaFree and uses no heap memory on the host.
  */
 int nf4_backward_a_batched_noalloc(const nf4_problem* problems, int count, void* stream);
+
+/*
+ * Dense weight gradient of a matrix product C = A @ B:
+ *
+ *     grad_B[K x N] = A[M x K]^T @ grad_C[M x N]
+ *
+ * (page "trueno-gpu 0.4.17 -- src/kernels/backward/mod.rs": the backward
+ * module's GEMM kernels give the gradients of both operands of a matrix
+ * product; GemmBackwardBKernel takes a_ptr and writes grad_b_ptr.  The page
+ * does not print that kernel; this is the plain definition.)  Beside a frozen
+ * NF4 base weight it is the gradient of the trainable 16-bit weights (LoRA
+ * adapters or fully trained layers): the sum runs over the M tokens, both
+ * operands are 16-bit floats of one type, products are summed in fp32 by the
+ * tensor cores (tcgen05 pair MMAs, both operands loaded by TMA as they are).
+ *   A, grad_C  [M][K] and [M][N], row-major, NF4_BF16 or NF4_F16 (`dtype`,
+ *              both), 16-byte aligned; K and N positive multiples of 8
+ *   grad_B     [K][N] fp32, 16-byte aligned, overwritten; M == 0 writes zeros
+ *   workspace  when the output tiles are too few to occupy the GPU, the tokens
+ *              are cut into nf4_gemm_backward_b_splits(M, K, N, pairs) runs
+ *              whose fp32 partial sums go to the workspace and are added in
+ *              run order by a second kernel (deterministic);
+ *              nf4_gemm_backward_b_ws_bytes(M, K, N) bytes (0: none needed),
+ *              256-byte aligned; with less (or NULL) the call splits less (or
+ *              not at all) and gives the same values up to fp32 summation order
+ * Returns NF4_ERR_INVALID or NF4_ERR_ALIGN (nothing enqueued) for arguments
+ * outside these rules.
+ */
+int nf4_gemm_backward_b_splits(int M, int K, int N, int pairs);
+size_t nf4_gemm_backward_b_ws_bytes(int M, int K, int N);
+int nf4_gemm_backward_b(const void* A, const void* grad_C, int dtype, float* grad_B, int M, int K,
+                        int N, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Synchronise `stream`, then report and clear the library's device status word

@@ -598,12 +598,18 @@ def test_batched_ws_rejects_small_workspace_without_launching():
                              out.data_ptr(), p.M, p.N, p.K)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     L = nb().lib()
-    assert L.nf4_backward_a_batched_ws(arr, 1, C.c_void_p(ws.data_ptr()), need - 1, None) == \
+    # Below the descriptors and the f16 copies: rejected.  (Between that and
+    # `need`, the f16 pass runs before the GEMM instead of beside it.)
+    least = _sequential_ws_bytes(items)
+    assert least < need
+    assert L.nf4_backward_a_batched_ws(arr, 1, C.c_void_p(ws.data_ptr()), least - 1, None) == \
         nb().NF4_ERR_WORKSPACE
     assert L.nf4_backward_a_batched_ws(arr, 1, None, 0, None) == nb().NF4_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert bool((out == 3.0).all())
     assert L.nf4_backward_a_batched_ws(arr, 1, C.c_void_p(ws.data_ptr()), need, None) == nb().NF4_OK
+    nb().check_error()
+    assert L.nf4_backward_a_batched_ws(arr, 1, C.c_void_p(ws.data_ptr()), least, None) == nb().NF4_OK
     nb().check_error()
 
 
@@ -687,3 +693,53 @@ def test_whole_waves_plus_split_wave_with_512_token_tiles():
     nb().check_error()
     assert torch.equal(a, b)
     assert torch.allclose(a, whole, rtol=1e-4, atol=1e-5)
+
+
+def _sequential_ws_bytes(items) -> int:
+    """Workspace of nf4_backward_a_batched_ws with no room for the streamed
+    pass's bookkeeping: the descriptors and the f16 copies only."""
+    r = lambda x: (x + 255) // 256 * 256
+    n = r(640 * len(items))
+    for go, w, _ in items:
+        M, N = go.shape
+        if M > 0 and N > 0 and go.dtype != torch.float16:
+            n += r(2 * M * ((N + 7) // 8 * 8))
+    return n
+
+
+def test_batched_ws_streamed_and_sequential_passes_agree():
+    """With room for its bookkeeping, the grouped pre-converted launch runs its
+    f16 pass beside the GEMM (the GEMM waits per 256-row block); without, the
+    pass runs first.  Both give the same bits, and the oracle's values."""
+    probs = [Problem(1300, 2048, 1536, F32, 1e-2, 0.02, False, 91),   # ragged 512-row tail
+             Problem(300, 136, 640, BF16, 1e-2, 0.02, True, 92),
+             Problem(16, 512, 256, F32, 1.0, 0.02, False, 93),        # few tokens
+             Problem(4096, 256, 1536, F32, 1e-2, 0.02, False, 94),
+             Problem(513, 1032, 768, F32, 1.0, 0.02, False, 95)]
+    items, refs = [], []
+    for p in probs:
+        go = make_grad_out(p)
+        B = make_weight(p)
+        items.append((to_device_go(go, p.go_dtype), nb().quantize(torch.from_numpy(B).cuda()), None))
+        data_o, scales_o = oracle.quantize(B)
+        go16 = oracle.round_operand(go, p.go_dtype)
+        bt = oracle.dequantize_f16(scales_o, data_o, p.K, p.N)
+        rows = sample_rows(p.M, 8, p.seed)
+        refs.append((rows,) + oracle.backward_a_rows(go16, bt, rows))
+    # One problem given in f16 (read in place: no pass, no counters).
+    pf = Problem(700, 320, 512, F32, 1.0, 0.02, False, 96)
+    items.append((torch.from_numpy(oracle.f32_to_f16(make_grad_out(pf)).view(np.int16)).cuda()
+                  .view(torch.float16), nb().quantize(torch.from_numpy(make_weight(pf)).cuda()),
+                  None))
+    full = nb().batched_ws_workspace(items)
+    seq_bytes = _sequential_ws_bytes(items)
+    assert full.numel() > seq_bytes
+    streamed = nb().backward_a_batched_ws(items, full)
+    sequential = nb().backward_a_batched_ws(items, full[:seq_bytes])
+    again = nb().backward_a_batched_ws(items, full)
+    nb().check_error()
+    for i, (a, b, c) in enumerate(zip(streamed, sequential, again)):
+        assert torch.equal(a, b), f"problem {i}: streamed != sequential pass"
+        assert torch.equal(a, c), f"problem {i}: not repeatable"
+    for p, out, (rows, ref, bound) in zip(probs, streamed, refs):
+        assert_close(out.cpu().numpy()[rows], ref, bound, str(p))

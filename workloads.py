@@ -110,6 +110,19 @@ def full_step(M: int = 4096, layers: int = LAYERS) -> list[Problem]:
     return out
 
 
+# Sibling projections whose input gradients add (they read the same layer
+# input): q/k/v and gate/up of one layer, as parts of one fused call; each part
+# keeps its own seeded grad_out and weight (layer 0 of the full step).
+def fused_parts(names: tuple[str, ...], M: int = 4096, layer: int = 0) -> list[Problem]:
+    probs = full_step(M, layers=layer + 1)[7 * layer: 7 * layer + 7]
+    return [p for p in probs if p.name.split(".")[1] in names]
+
+
+FUSED: dict[str, list[Problem]] = {
+    "fused_qkv": fused_parts(("q", "k", "v")),
+    "fused_gate_up": fused_parts(("gate", "up")),
+}
+
 CONFIGS: dict[str, list[Problem]] = {
     "tiny": [Problem(32, 64, 128, F32, 1.0, 0.02, False, 0, "tiny")],
     "q_proj": [Problem(2048, HIDDEN, HIDDEN, F32, 1e-2, 0.02, False, 0, "q_proj")],
