@@ -52,6 +52,13 @@ static bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* ba
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tile raster (ProblemDesc::row_group): problems with many row blocks and many
+// column tiles run in groups of 4 row blocks, column tiles slowest within a
+// group; small problems keep the plain order (columns fastest).
+static inline int raster_rows(int tiles_m, int tiles_k) {
+  return tiles_m >= 8 && tiles_k >= 16 ? 4 : 1;
+}
+
 // Argument rules shared by the single and grouped entry points.
 static int check_problem(const void* go, int dtype, const float* scales, const uint8_t* data,
                          const float* grad_A, int M, int N, int K) {
@@ -97,6 +104,7 @@ static int fill_desc_rest(ProblemDesc* d, int dtype, const float* scales, const 
   d->dtype = dtype;
   d->tiles_m = (M + rows_per_tile - 1) / rows_per_tile;
   d->tiles_k = (K + BK - 1) / BK;
+  d->row_group = raster_rows(d->tiles_m, d->tiles_k);
   d->n_stages = (N + BN - 1) / BN;
   d->tile_begin = 0;
   return NF4_OK;
@@ -165,6 +173,7 @@ static int fill_desc_fwd(ProblemDesc* d, const uint16_t* a_f16, const float* sca
   d->dtype = NF4_BF16;  // not read by this variant
   d->tiles_m = (M + rows_per_tile - 1) / rows_per_tile;
   d->tiles_k = (N + BK - 1) / BK;
+  d->row_group = raster_rows(d->tiles_m, d->tiles_k);
   d->n_stages = K / BN;
   d->tile_begin = 0;
   d->scale_tma = 0;

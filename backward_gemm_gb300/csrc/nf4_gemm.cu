@@ -551,7 +551,12 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
   // Longest tiles first (stable), as the grouped entry point orders them.
   std::vector<int> order(descs.size());
   for (size_t i = 0; i < order.size(); ++i) order[i] = static_cast<int>(i);
+  // With the pass beside the GEMM, problems with more GEMM work per byte of the
+  // pass come first (largest K: the pass writes M x N elements for 2 M N K
+  // flops), so that the pass gets ahead while the GEMM works on them; then
+  // longest tiles first.
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    if (streamed && descs[a].K != descs[b].K) return descs[a].K > descs[b].K;
     return descs[a].n_stages > descs[b].n_stages;
   });
   {

@@ -207,6 +207,11 @@ struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
   // writing; the A producer waits for a block's full count before its first
   // copy from it.  nullptr otherwise.
   const unsigned int* ready;
+  // Tile order: 1 = output-column tiles fastest over all row blocks; G > 1 =
+  // groups of G row blocks, column tiles slowest within a group, so that the
+  // pairs running at the same time share both a few row blocks of A and a few
+  // column blocks of the weight in L2.
+  int row_group;
 };
 
 static_assert(sizeof(ProblemDesc) % 16 == 0, "descriptor copy granularity");
@@ -235,8 +240,18 @@ __device__ __forceinline__ Tile tile_fields(const ProblemDesc& d, const ProblemD
   // from DRAM once per column tile when it does not fit in L2).
   const int local = t - d.tile_begin;
   const int tk = d.tiles_k;
-  r.mt = local / tk;
-  r.kt = local % tk;
+  const int G = d.row_group;
+  if (G > 1) {
+    const int per_group = G * tk;
+    const int g = local / per_group;
+    const int idx = local - g * per_group;
+    const int rows = min(G, d.tiles_m - g * G);  // the last group may be shorter
+    r.kt = idx / rows;
+    r.mt = g * G + (idx - r.kt * rows);
+  } else {
+    r.mt = local / tk;
+    r.kt = local % tk;
+  }
   r.ns = d.n_stages;
   r.stma = d.scale_tma;
   r.fwd = d.fwd;

@@ -826,48 +826,60 @@ def bench_e2e(args, probs, host_go, sets, stream, dev, flops, world):
     h2d = sum(t.numel() * t.element_size() for t in pinned_in)
     d2h = sum(t.numel() * 4 for t in pinned_out)
     steps = max(4, min(args.steps, 50))
-    s_in = torch.cuda.Stream(device=dev)
-    s_out = torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
+    # Copies of a step are spread over E streams per direction (problem j on
+    # stream j % E), so that several copy engines serve each direction.
+    E = 2 if len(probs) > 1 else 1
+    s_in = [torch.cuda.Stream(device=dev) for _ in range(E)]
+    s_out = [torch.cuda.Stream(device=dev) for _ in range(E)]
+    ev_in = [[torch.cuda.Event() for _ in range(E)] for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [[torch.cuda.Event() for _ in range(E)] for _ in range(2)]
 
     def issue(i):
         b = i % 2
         items, ws = bufs[b]
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(ev_comp[b])       # step i-2 no longer reads these inputs
-            for (go_d, _, _), hin in zip(items, pinned_in):
-                dst = go_d.view(torch.int16) if go_d.dtype == torch.bfloat16 else go_d
-                dst.copy_(hin, non_blocking=True)
-            ev_in[b].record(s_in)
+        for e in range(E):
+            with torch.cuda.stream(s_in[e]):
+                if i >= 2:
+                    s_in[e].wait_event(ev_comp[b])   # step i-2 no longer reads these inputs
+                for j in range(e, len(items), E):
+                    go_d, hin = items[j][0], pinned_in[j]
+                    dst = go_d.view(torch.int16) if go_d.dtype == torch.bfloat16 else go_d
+                    dst.copy_(hin, non_blocking=True)
+                ev_in[b][e].record(s_in[e])
         with torch.cuda.stream(stream):
-            stream.wait_event(ev_in[b])
-            if i >= 2:
-                stream.wait_event(ev_out[b])      # step i-2's outputs are copied out
+            for e in range(E):
+                stream.wait_event(ev_in[b][e])
+                if i >= 2:
+                    stream.wait_event(ev_out[b][e])  # step i-2's outputs are copied out
             run_step(items, ws)
             ev_comp[b].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_comp[b])
-            for (_, _, out), hout in zip(items, pinned_out):
-                hout.copy_(out, non_blocking=True)
-            ev_out[b].record(s_out)
+        for e in range(E):
+            with torch.cuda.stream(s_out[e]):
+                s_out[e].wait_event(ev_comp[b])
+                for j in range(e, len(items), E):
+                    pinned_out[j].copy_(items[j][2], non_blocking=True)
+                ev_out[b][e].record(s_out[e])
 
     for i in range(2):
         issue(i)
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(s_in)
+    ev0.record(s_in[0])
+    for e in range(1, E):
+        s_in[e].wait_event(ev0)
     for i in range(steps):
         issue(i)
-    ev1.record(s_out)
+    for e in range(1, E):
+        s_out[0].wait_stream(s_out[e])
+    ev1.record(s_out[0])
     ev1.synchronize()
     torch.cuda.synchronize(dev)
     ms = ev0.elapsed_time(ev1) / steps
     return {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "steps": steps, "pipelined": "copy-in, compute, copy-out on three streams, two buffer sets"}
+            "steps": steps,
+            "pipelined": f"copy-in ({E} streams), compute, copy-out ({E} streams), two buffer sets"}
 
 
 def kernel_source_digest() -> str:
