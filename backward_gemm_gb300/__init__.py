@@ -44,6 +44,12 @@ class Nf4Part(C.Structure):
     _fields_ = [("grad_out", _vp), ("go_dtype", _i), ("N", _i)]
 
 
+class Nf4FusedProblem(C.Structure):
+    """Mirror of ``nf4_fused_problem``."""
+    _fields_ = [("parts", C.POINTER(Nf4Part)), ("count", _i), ("scales", _vp), ("data", _vp),
+                ("grad_x", _vp), ("M", _i), ("K", _i)]
+
+
 SIGNATURES = {
     "nf4_abi_version": (_i, []),
     "nf4_status_string": (C.c_char_p, [_i]),
@@ -72,6 +78,8 @@ SIGNATURES = {
     "nf4_small_m_split": (_i, [_i, _i, _i, _i, C.POINTER(_i)]),
     "nf4_watchdog_selftest": (_i, [C.c_longlong, _vp, _vp]),
     "nf4_backward_a_fused": (_i, [C.POINTER(Nf4Part), _i, _vp, _vp, _vp, _i, _i, _vp, _sz, _vp]),
+    "nf4_backward_a_fused_batched_ws_bytes": (_sz, [C.POINTER(Nf4FusedProblem), _i]),
+    "nf4_backward_a_fused_batched": (_i, [C.POINTER(Nf4FusedProblem), _i, _vp, _sz, _vp]),
     "nf4_gemm_backward_b_splits": (_i, [_i, _i, _i, _i]),
     "nf4_gemm_backward_b_ws_bytes": (_sz, [_i, _i, _i]),
     "nf4_gemm_backward_b": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _vp, _sz, _vp]),
@@ -409,6 +417,63 @@ def backward_a_fused(grad_outs, w: NF4Weight, workspace: torch.Tensor | None = N
                                       M, w.K, _ptr(workspace), nbytes, _stream()),
            "nf4_backward_a_fused")
     return out
+
+
+def _fused_array(problems):
+    """Host arrays of nf4_fused_problem (and their parts) for (grad_outs, w, out)
+    items, every item checked before anything is created."""
+    problems = list(problems)
+    for i, (gos, w, out) in enumerate(problems):
+        gos = list(gos)
+        if not gos or len(gos) > 8:
+            raise ValueError(f"problem {i}: 1 to 8 parts")
+        M = gos[0].shape[0] if gos[0].dim() == 2 else -1
+        for j, g in enumerate(gos):
+            if g.dim() != 2 or g.shape[0] != M:
+                raise ValueError(f"problem {i} part {j}: grad_out must be [M, N_p] with M={M}")
+            _dtype_code(g)
+            _require_cuda_contig(f"problem {i} part {j}: grad_out", g)
+        if sum(g.shape[1] for g in gos) != w.N:
+            raise ValueError(f"problem {i}: the parts' N sum to {sum(g.shape[1] for g in gos)}, "
+                             f"the stacked weight has N={w.N}")
+        if out is not None:
+            if out.dtype != torch.float32 or tuple(out.shape) != (M, w.K):
+                raise ValueError(f"problem {i}: out must be float32 [M, K] = [{M}, {w.K}]")
+            _require_cuda_contig(f"problem {i}: out", out)
+        _require_cuda_contig(f"problem {i}: weight codes", w.data)
+        _require_cuda_contig(f"problem {i}: weight scales", w.scales)
+    arr = (Nf4FusedProblem * max(len(problems), 1))()
+    keep, outs = [], []
+    for i, (gos, w, out) in enumerate(problems):
+        gos = list(gos)
+        M = gos[0].shape[0]
+        if out is None:
+            out = torch.empty((M, w.K), dtype=torch.float32, device=gos[0].device)
+        parts = (Nf4Part * len(gos))(*[Nf4Part(g.data_ptr(), _dtype_code(g), g.shape[1])
+                                      for g in gos])
+        keep.append(parts)
+        outs.append(out)
+        arr[i] = Nf4FusedProblem(parts, len(gos), w.scales.data_ptr(), w.data.data_ptr(),
+                                 out.data_ptr(), M, w.K)
+    return arr, keep, outs
+
+
+def backward_a_fused_batched(problems, workspace: torch.Tensor | None = None):
+    """Many fused problems in one grouped launch (``nf4_backward_a_fused_batched``).
+    ``problems``: sequence of (grad_outs, stacked NF4Weight, out-or-None); a
+    one-part problem is a plain backward-A.  Returns the outputs."""
+    problems = list(problems)
+    arr, keep, outs = _fused_array(problems)
+    if workspace is None:
+        n = int(lib().nf4_backward_a_fused_batched_ws_bytes(arr, len(problems)))
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8,
+                                device=outs[0].device if outs else "cuda")
+    _require_cuda_contig("workspace", workspace)
+    _check(lib().nf4_backward_a_fused_batched(arr, len(problems), _ptr(workspace),
+                                              workspace.numel(), _stream()),
+           "nf4_backward_a_fused_batched")
+    del keep
+    return outs
 
 
 def gemm_backward_b(A: torch.Tensor, grad_C: torch.Tensor, workspace: torch.Tensor | None = None,

@@ -410,62 +410,76 @@ extern "C" int nf4_backward_a_batched(const nf4_problem* problems, int count, vo
 
 // ------------------------------------------------------------------ grouped, pre-converted
 namespace nf4 {
-// Problems of a grouped pre-converted launch whose grad_out needs the f16 copy
-// (fp32 or bf16, M above the few-token limit or not), in problem order.
-static size_t group_copy_bytes(const nf4_problem* problems, int count) {
+// One problem of a grouped pre-converted launch: a plain backward-A problem
+// (one part) or a fused one (the parts' grad_out side by side along N, the
+// weights stacked along N).
+constexpr int kMaxParts = 8;
+struct GPart {
+  const void* src;
+  int dtype, N;
+};
+struct GProblem {
+  GPart part[kMaxParts];
+  int nparts;
+  const float* scales;
+  const uint8_t* data;
+  float* out;
+  int M, N, K;  // N: the sum of the parts'
+};
+
+// A problem that gets an f16 copy: every fused problem, a plain one unless its
+// grad_out is f16 already (then it is read in place).
+static inline bool needs_copy(const GProblem& p) {
+  return p.M > 0 && p.N > 0 && (p.nparts > 1 || p.part[0].dtype != NF4_F16);
+}
+
+// A plain problem that the few-token kernel runs on its own.
+static inline bool few_token(const GProblem& p, int small_max) {
+  return p.nparts == 1 && p.part[0].dtype != NF4_F16 && p.M > 0 && p.N > 0 && p.M <= small_max;
+}
+
+static size_t group_copy_bytes(const GProblem* problems, int count) {
   size_t total = 0;
-  for (int i = 0; i < count; ++i) {
-    const nf4_problem& p = problems[i];
-    if (p.M > 0 && p.N > 0 && p.go_dtype != NF4_F16) total += round256(f16_bytes(p.M, p.N));
-  }
+  for (int i = 0; i < count; ++i)
+    if (needs_copy(problems[i])) total += round256(f16_bytes(problems[i].M, problems[i].N));
   return total;
 }
 
-}  // namespace nf4
-
-// Words of the streamed pre-pass's bookkeeping for these problems (0 when the
-// group cannot be streamed): the work counter, the per-SM claim flags and one
-// ready counter per 256-row block of every problem that gets an f16 copy.
-static size_t stream_words(const nf4_problem* problems, int count) {
+// Words of the streamed pass's bookkeeping for these problems (0 when the group
+// cannot be streamed): the work counter, the per-SM claim flags and one ready
+// counter per 256-row block of every problem with a copy.
+static size_t stream_words(const GProblem* problems, int count) {
   size_t blocks = 0;
   int jobs = 0;
   for (int i = 0; i < count; ++i) {
-    const nf4_problem& p = problems[i];
-    if (p.M > 0 && p.N > 0 && p.go_dtype != NF4_F16) {
-      ++jobs;
-      blocks += static_cast<size_t>((p.M + 255) / 256);
-    }
+    if (!needs_copy(problems[i])) continue;
+    jobs += problems[i].nparts;
+    blocks += static_cast<size_t>((problems[i].M + 255) / 256);
   }
   if (jobs == 0 || jobs > kStreamMaxJobs) return 0;
   return 1 + kStreamClaimWords + blocks;
 }
 
-extern "C" size_t nf4_backward_a_batched_ws_bytes(const nf4_problem* problems, int count) {
-  if (count <= 0 || problems == nullptr) return 0;
+static size_t grouped_ws_bytes(const GProblem* problems, int count) {
   return round256(sizeof(ProblemDesc) * static_cast<size_t>(count)) +
          group_copy_bytes(problems, count) +
          round256(sizeof(unsigned int) * stream_words(problems, count));
 }
 
-extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count, void* workspace,
-                                         size_t workspace_bytes, void* stream) {
-  if (count < 0 || (count > 0 && problems == nullptr)) return NF4_ERR_INVALID;
-  for (int i = 0; i < count; ++i) {
-    const nf4_problem& p = problems[i];
-    const int rc = check_problem(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
-    if (rc != NF4_OK) return rc;
-  }
-  cudaStream_t st = as_stream(stream);
+// The grouped launch of the pre-converted path over checked problems.
+static int grouped_ws(const GProblem* problems, int count, void* workspace, size_t workspace_bytes,
+                      cudaStream_t st) {
   const size_t desc_bytes = round256(sizeof(ProblemDesc) * static_cast<size_t>(count));
   // Nothing is enqueued before the workspace is known to be big enough.
   bool any_gemm = false;
   const int small_max = small_m::g_max_m.load();
   for (int i = 0; i < count; ++i) {
-    const nf4_problem& p = problems[i];
-    if (p.M > 0 && p.N > 0 && (p.M > small_max || p.go_dtype == NF4_F16)) any_gemm = true;
+    const GProblem& p = problems[i];
+    if (p.M > 0 && p.N > 0 && !few_token(p, small_max)) any_gemm = true;
   }
+  const size_t copy_bytes = group_copy_bytes(problems, count);
   if (any_gemm && (workspace == nullptr || !aligned(workspace, 256) ||
-                   workspace_bytes < desc_bytes + group_copy_bytes(problems, count)))
+                   workspace_bytes < desc_bytes + copy_bytes))
     return NF4_ERR_WORKSPACE;
   // Tile size for the whole group: 512 tokens when every GEMM problem has more
   // than 256 tokens, there are at least half a wave of 512-token tiles and the
@@ -478,8 +492,8 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
   int64_t t2 = 0, t2_stages = 0;
   bool all_tall = true;
   for (int i = 0; i < count; ++i) {
-    const nf4_problem& p = problems[i];
-    if (p.M == 0 || p.N == 0 || (p.go_dtype != NF4_F16 && p.M <= small_max)) continue;
+    const GProblem& p = problems[i];
+    if (p.M == 0 || p.N == 0 || few_token(p, small_max)) continue;
     const int64_t tiles = static_cast<int64_t>((p.M + 511) / 512) * ((p.K + BK - 1) / BK);
     t2 += tiles;
     t2_stages += tiles * ((p.N + BN - 1) / BN);
@@ -492,7 +506,6 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
   const int rows_per_tile = tiles512 ? LayoutPreA2::kRowsPerTile : LayoutPreA::kRowsPerTile;
   // With room for its bookkeeping after the copies, the f16 pass runs beside
   // the GEMM (to_f16_stream_kernel), otherwise before it.
-  const size_t copy_bytes = group_copy_bytes(problems, count);
   const size_t swords = stream_words(problems, count);
   const bool streamed = any_gemm && swords > 0 &&
                         workspace_bytes >= desc_bytes + copy_bytes +
@@ -504,71 +517,80 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
   std::vector<ProblemDesc> descs;
   descs.reserve(count);
   std::vector<F16Job> jobs;
-  std::vector<int> job_of;  // per descriptor: its f16 job, or -1 (f16 input)
+  std::vector<int> jobs_of;  // per descriptor: its first f16 job (jobs_n of them), or -1
+  std::vector<int> jobs_n;
   uint8_t* copy = static_cast<uint8_t*>(workspace) + desc_bytes;
   for (int i = 0; i < count; ++i) {
-    const nf4_problem& p = problems[i];
+    const GProblem& p = problems[i];
     if (p.M == 0) continue;
     if (p.N == 0) {
-      if (cudaMemsetAsync(p.grad_A, 0, sizeof(float) * static_cast<size_t>(p.M) * p.K, st) !=
+      if (cudaMemsetAsync(p.out, 0, sizeof(float) * static_cast<size_t>(p.M) * p.K, st) !=
           cudaSuccess)
         return NF4_ERR_CUDA;
       continue;
     }
-    const bool f16_in = p.go_dtype == NF4_F16;
     uint16_t* dst = nullptr;
-    if (!f16_in) {
+    if (needs_copy(p)) {
       dst = reinterpret_cast<uint16_t*>(copy);
       copy += round256(f16_bytes(p.M, p.N));
     }
-    if (!f16_in && p.M <= small_max) {
+    if (few_token(p, small_max)) {
       // Few tokens: the problem's own launch of the few-token kernel.
-      const int rc = small_m::run(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N,
-                                  p.K, st);
+      const int rc = small_m::run(p.part[0].src, p.part[0].dtype, p.scales, p.data, p.out, p.M,
+                                  p.N, p.K, st);
       if (rc != NF4_OK) return rc;
       continue;
     }
     descs.emplace_back();
-    job_of.push_back(f16_in ? -1 : static_cast<int>(jobs.size()));
-    const uint16_t* a = f16_in ? static_cast<const uint16_t*>(p.grad_out) : dst;
-    const int rc = fill_desc_pre(&descs.back(), a, p.scales, p.data, p.grad_A, p.M, p.N, p.K,
+    jobs_of.push_back(dst != nullptr ? static_cast<int>(jobs.size()) : -1);
+    jobs_n.push_back(dst != nullptr ? p.nparts : 0);
+    const uint16_t* a = dst != nullptr ? dst : static_cast<const uint16_t*>(p.part[0].src);
+    const int rc = fill_desc_pre(&descs.back(), a, p.scales, p.data, p.out, p.M, p.N, p.K,
                                  rows_per_tile);
     if (rc != NF4_OK) return rc;
-    if (!f16_in) {
-      F16Job j;
-      j.src = p.grad_out;
-      j.dst = dst;
-      j.mode = p.go_dtype == NF4_F32 ? kSrcF32 : kSrcBF16;
-      j.N = p.N;
-      j.ldh = f16_pitch(p.N);
-      j.pitch = j.ldh;
-      j.groups_per_row = (j.ldh + 15) >> 4;
-      j.begin = static_cast<int64_t>(p.M) * j.groups_per_row;  // size for now
-      jobs.push_back(j);
+    if (dst != nullptr) {
+      // Part j's grad_out goes into its columns of the copy (rows f16_pitch(N)
+      // apart; every part of a fused problem is a multiple of 8 columns wide).
+      int col = 0;
+      for (int q = 0; q < p.nparts; ++q) {
+        const GPart& pt = p.part[q];
+        F16Job j;
+        j.src = pt.src;
+        j.dst = dst + col;
+        j.mode = pt.dtype == NF4_F32 ? kSrcF32 : (pt.dtype == NF4_BF16 ? kSrcBF16 : kSrcF16);
+        j.N = pt.N;
+        j.ldh = f16_pitch(pt.N);
+        j.pitch = f16_pitch(p.N);
+        j.groups_per_row = (j.ldh + 15) >> 4;
+        j.begin = static_cast<int64_t>(p.M) * j.groups_per_row;  // size for now
+        jobs.push_back(j);
+        col += pt.N;
+      }
     }
   }
   if (descs.empty()) return NF4_OK;
-  // Longest tiles first (stable), as the grouped entry point orders them.
-  std::vector<int> order(descs.size());
-  for (size_t i = 0; i < order.size(); ++i) order[i] = static_cast<int>(i);
   // With the pass beside the GEMM, problems with more GEMM work per byte of the
   // pass come first (largest K: the pass writes M x N elements for 2 M N K
   // flops), so that the pass gets ahead while the GEMM works on them; then
-  // longest tiles first.
+  // longest tiles first (stable).
+  std::vector<int> order(descs.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = static_cast<int>(i);
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
     if (streamed && descs[a].K != descs[b].K) return descs[a].K > descs[b].K;
     return descs[a].n_stages > descs[b].n_stages;
   });
   {
     std::vector<ProblemDesc> sorted;
-    std::vector<int> sorted_job;
+    std::vector<int> sorted_of, sorted_n;
     sorted.reserve(descs.size());
     for (int i : order) {
       sorted.push_back(descs[i]);
-      sorted_job.push_back(job_of[i]);
+      sorted_of.push_back(jobs_of[i]);
+      sorted_n.push_back(jobs_n[i]);
     }
     descs.swap(sorted);
-    job_of.swap(sorted_job);
+    jobs_of.swap(sorted_of);
+    jobs_n.swap(sorted_n);
   }
   int64_t total = 0;
   for (ProblemDesc& d : descs) {
@@ -577,7 +599,8 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
     if (total > INT_MAX) return NF4_ERR_INVALID;
   }
   // Streamed pass: its jobs in the GEMM's order (the sorted descriptors), each
-  // problem's ready counters after the work counter and the claim flags.
+  // problem's ready counters after the work counter and the claim flags; the
+  // parts of a fused problem count into the same words.
   StreamJobs sjobs;
   if (streamed) {
     std::memset(&sjobs, 0, sizeof(sjobs));
@@ -586,21 +609,25 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
     unsigned int* ready = stream_area + 1 + kStreamClaimWords;
     int items = 0;
     for (size_t i = 0; i < descs.size(); ++i) {
-      if (job_of[i] < 0) continue;
-      const F16Job& f = jobs[job_of[i]];
-      StreamJob& j = sjobs.job[sjobs.n++];
-      j.src = f.src;
-      j.dst = f.dst;
-      j.ready = ready;
-      j.mode = f.mode;
-      j.M = descs[i].M;
-      j.N = f.N;
-      j.ldh = f.ldh;
-      j.item_begin = items;
-      j.groups_per_row = f.groups_per_row;
-      items += (j.M + kSlabRows - 1) / kSlabRows;
+      if (jobs_of[i] < 0) continue;
+      for (int q = 0; q < jobs_n[i]; ++q) {
+        const F16Job& f = jobs[jobs_of[i] + q];
+        StreamJob& j = sjobs.job[sjobs.n++];
+        j.src = f.src;
+        j.dst = f.dst;
+        j.ready = ready;
+        j.mode = f.mode;
+        j.M = descs[i].M;
+        j.N = f.N;
+        j.ldh = f.ldh;
+        j.pitch = f.pitch;
+        j.item_begin = items;
+        j.groups_per_row = f.groups_per_row;
+        items += (j.M + kSlabRows - 1) / kSlabRows;
+      }
       descs[i].ready = ready;
-      ready += (j.M + 255) / 256;
+      descs[i].ready_parts = jobs_n[i];
+      ready += (descs[i].M + 255) / 256;
     }
     sjobs.items = items;
   }
@@ -643,8 +670,8 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
     return launch_layout<LayoutPreA>(unused, ws, static_cast<int>(descs.size()),
                                      static_cast<int>(total), &sk, st, /*pdl=*/true);
   }
-  // The f16 copies, kF16JobsPerLaunch problems per launch; the GEMM follows
-  // the last of them as a programmatic dependent.
+  // The f16 copies, kF16JobsPerLaunch jobs per launch; the GEMM follows the
+  // last of them as a programmatic dependent.
   for (size_t i = 0; i < jobs.size(); i += kF16JobsPerLaunch) {
     F16Jobs batch;
     std::memset(&batch, 0, sizeof(batch));
@@ -667,6 +694,99 @@ extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count,
                                       static_cast<int>(total), nullptr, st, /*pdl=*/!jobs.empty());
   return launch_layout<LayoutPreA>(unused, ws, static_cast<int>(descs.size()),
                                    static_cast<int>(total), nullptr, st, /*pdl=*/!jobs.empty());
+}
+
+// nf4_problem -> one-part GProblem (its arguments not checked here).
+static GProblem from_plain(const nf4_problem& p) {
+  GProblem g;
+  std::memset(&g, 0, sizeof(g));
+  g.part[0].src = p.grad_out;
+  g.part[0].dtype = p.go_dtype;
+  g.part[0].N = p.N;
+  g.nparts = 1;
+  g.scales = p.scales;
+  g.data = p.data;
+  g.out = p.grad_A;
+  g.M = p.M;
+  g.N = p.N;
+  g.K = p.K;
+  return g;
+}
+
+// nf4_fused_problem -> GProblem, with the rules of nf4_backward_a_fused.
+static int from_fused(const nf4_fused_problem& f, GProblem* g) {
+  std::memset(g, 0, sizeof(*g));
+  if (f.count <= 0 || f.count > kMaxParts || f.parts == nullptr) return NF4_ERR_INVALID;
+  if (f.M < 0 || f.K <= 0 || f.K % 64 != 0) return NF4_ERR_INVALID;
+  int64_t ntot = 0;
+  for (int i = 0; i < f.count; ++i) {
+    const nf4_part& q = f.parts[i];
+    if (q.go_dtype != NF4_F32 && q.go_dtype != NF4_BF16 && q.go_dtype != NF4_F16)
+      return NF4_ERR_INVALID;
+    if (q.N <= 0 || q.N % 8 != 0) return NF4_ERR_INVALID;
+    g->part[i].src = q.grad_out;
+    g->part[i].dtype = q.go_dtype;
+    g->part[i].N = q.N;
+    ntot += q.N;
+  }
+  if (ntot > INT_MAX) return NF4_ERR_INVALID;
+  g->nparts = f.count;
+  g->scales = f.scales;
+  g->data = f.data;
+  g->out = f.grad_x;
+  g->M = f.M;
+  g->N = static_cast<int>(ntot);
+  g->K = f.K;
+  if (f.M == 0) return NF4_OK;
+  if (f.scales == nullptr || f.data == nullptr || f.grad_x == nullptr) return NF4_ERR_INVALID;
+  for (int i = 0; i < f.count; ++i) {
+    if (f.parts[i].grad_out == nullptr) return NF4_ERR_INVALID;
+    if (!aligned(f.parts[i].grad_out, 16)) return NF4_ERR_ALIGN;
+  }
+  if (!aligned(f.grad_x, 16) || !aligned(f.data, 16) || !aligned(f.scales, 4)) return NF4_ERR_ALIGN;
+  return NF4_OK;
+}
+}  // namespace nf4
+
+extern "C" size_t nf4_backward_a_batched_ws_bytes(const nf4_problem* problems, int count) {
+  if (count <= 0 || problems == nullptr) return 0;
+  std::vector<GProblem> g(count);
+  for (int i = 0; i < count; ++i) g[i] = from_plain(problems[i]);
+  return grouped_ws_bytes(g.data(), count);
+}
+
+extern "C" int nf4_backward_a_batched_ws(const nf4_problem* problems, int count, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  if (count < 0 || (count > 0 && problems == nullptr)) return NF4_ERR_INVALID;
+  std::vector<GProblem> g(count);
+  for (int i = 0; i < count; ++i) {
+    const nf4_problem& p = problems[i];
+    const int rc = check_problem(p.grad_out, p.go_dtype, p.scales, p.data, p.grad_A, p.M, p.N, p.K);
+    if (rc != NF4_OK) return rc;
+    g[i] = from_plain(p);
+  }
+  return grouped_ws(g.data(), count, workspace, workspace_bytes, as_stream(stream));
+}
+
+extern "C" size_t nf4_backward_a_fused_batched_ws_bytes(const nf4_fused_problem* problems,
+                                                        int count) {
+  if (count <= 0 || problems == nullptr) return 0;
+  std::vector<GProblem> g(count);
+  for (int i = 0; i < count; ++i)
+    if (from_fused(problems[i], &g[i]) != NF4_OK) return 0;
+  return grouped_ws_bytes(g.data(), count);
+}
+
+extern "C" int nf4_backward_a_fused_batched(const nf4_fused_problem* problems, int count,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* stream) {
+  if (count < 0 || (count > 0 && problems == nullptr)) return NF4_ERR_INVALID;
+  std::vector<GProblem> g(count);
+  for (int i = 0; i < count; ++i) {
+    const int rc = from_fused(problems[i], &g[i]);
+    if (rc != NF4_OK) return rc;
+  }
+  return grouped_ws(g.data(), count, workspace, workspace_bytes, as_stream(stream));
 }
 
 #ifdef NF4_PROGRESS

@@ -207,6 +207,9 @@ struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
   // writing; the A producer waits for a block's full count before its first
   // copy from it.  nullptr otherwise.
   const unsigned int* ready;
+  // Pass jobs counted into each ready word: the parts of a fused problem write
+  // their column slices of the same rows (1 for a plain problem).
+  int ready_parts;
   // Tile order: 1 = output-column tiles fastest over all row blocks; G > 1 =
   // groups of G row blocks, column tiles slowest within a group, so that the
   // pairs running at the same time share both a few row blocks of A and a few
@@ -790,7 +793,8 @@ __global__ void __launch_bounds__(L::kThreads, 1)
             const int rb = tl.mt * kMBlocks + b;
             const int rows = tl.M - rb * 256;
             if (rows <= 0) break;
-            const unsigned int need = static_cast<unsigned int>(((rows < 256 ? rows : 256) + 63) / 64);
+            const unsigned int need = static_cast<unsigned int>(tl.p->ready_parts) *
+                                      static_cast<unsigned int>(((rows < 256 ? rows : 256) + 63) / 64);
             ready = flag_wait_global_ge(cnt + rb, need, abort_flag);
           }
           fence_proxy_async_global();

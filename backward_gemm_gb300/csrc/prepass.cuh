@@ -175,9 +175,9 @@ constexpr int kStreamPrefetchAhead = 8;  // loop turns of source prefetched ahea
 
 struct StreamJob {
   const void* src;      // grad_out [M][N]
-  uint16_t* dst;        // f16 copy [M][ldh]
+  uint16_t* dst;        // f16 copy: ldh columns of rows `pitch` elements apart
   unsigned int* ready;  // [ceil(M / 256)] finished 64-row slabs per 256-row block
-  int mode, M, N, ldh;
+  int mode, M, N, ldh, pitch;
   int item_begin;       // first work item (slab) of this job
   int groups_per_row;   // (ldh + 15) / 16
 };
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kStreamThreads, 16)
           prefetch_l2_bulk(base + off, static_cast<uint32_t>(min(chunk, bytes - off)));
       }
       const int m = r0 + g / gpr;
-      convert_group(j.src, j.mode, j.dst, j.N, j.ldh, j.ldh, m, (g - (m - r0) * gpr) << 4);
+      convert_group(j.src, j.mode, j.dst, j.N, j.ldh, j.pitch, m, (g - (m - r0) * gpr) << 4);
     }
     // Every thread's stores are visible device-wide before the slab is counted.
     __threadfence();

@@ -406,6 +406,131 @@ def bench_forward(args, dev):
     }
 
 
+# The full step with the sibling projections fused (nf4_backward_a_fused_batched):
+# per layer q/k/v summed into one grad_x (three parts), o, gate/up summed (two
+# parts), down -- 112 problems for the 28 layers, the same 10.7 TFLOP as the
+# 196-projection step, each part with the full step's seeded inputs.
+FUSED_STEP_GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+
+
+def fused_step_groups(layers: int):
+    probs = full_step(layers=layers)
+    by_name = {p.name: p for p in probs}
+    out = []
+    for layer in range(layers):
+        for names in FUSED_STEP_GROUPS:
+            out.append([by_name[f"L{layer}.{n}"] for n in names])
+    return out
+
+
+def bench_fused_step(args, dev):
+    """nf4_backward_a_fused_batched over the fused full step on rotating input
+    sets beyond L2 (a CUDA graph of one step per set), the grouped GEMM alone
+    (the f16 operands the steps left in each set's workspace, read in place),
+    the tensor roofline, the clocks."""
+    import backward_gemm_gb300 as nb
+    from backward_gemm_gb300.build import build
+
+    build()
+    nb.lib()
+    groups = fused_step_groups(args.layers or 28)
+    flat = [p for g in groups for p in g]
+    flops = sum(p.flops for p in flat)
+    alg_bytes = sum(p.go_bytes + p.K * p.N // 2 + 4 * p.N * (p.K // 64) for p in flat) + \
+        sum(4 * g[0].M * g[0].K for g in groups)
+    base = {p.name: (make_grad_out(p), make_weight(p)) for p in flat}
+    per_set = sum(p.go_bytes + p.K * p.N // 2 + 2 * p.M * p.N for p in flat) + \
+        sum(4 * g[0].M * g[0].K for g in groups)
+    copies = max(2, min(16, -(-2 * L2_BYTES // per_set)))
+    sets = []
+    for _ in range(copies):
+        items = []
+        for g in groups:
+            gos = [torch.from_numpy(base[p.name][0]).to(dev) for p in g]
+            w = nb.stack_weights([nb.quantize(torch.from_numpy(base[p.name][1]).to(dev)) for p in g])
+            items.append((gos, w, torch.empty((g[0].M, g[0].K), device=dev)))
+        arr, keep, _ = nb._fused_array(items)
+        n = int(nb.lib().nf4_backward_a_fused_batched_ws_bytes(arr, len(items)))
+        sets.append((items, torch.empty(n, dtype=torch.uint8, device=dev)))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    steps = args.steps
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            nb.backward_a_fused_batched(*sets[i % copies])
+        nb.check_error()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for items, ws in sets:
+                nb.backward_a_fused_batched(items, ws)
+        graph.replay()
+        stream.synchronize()
+        full, rem = divmod(steps, copies)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index) as clocks:
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                nb.backward_a_fused_batched(*sets[i])
+            ev1.record(stream)
+            ev1.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        nb.check_error()
+        # The grouped GEMM alone: each problem's f16 operand [M][sum N] is in
+        # the workspace after the steps (descriptors first, then the copies in
+        # problem order); given as one f16 part it is read in place.
+        runs = []
+        desc = (640 * len(groups) + 255) // 256 * 256
+        for items, ws in sets:
+            at = desc
+            f16_items = []
+            for gos, w, out in items:
+                M, N = gos[0].shape[0], w.N
+                n = 2 * M * N
+                f16_items.append(([ws[at: at + n].view(torch.float16).view(M, N)], w, out))
+                at += (n + 255) // 256 * 256
+            runs.append((f16_items, ws))
+        kern_steps = min(steps, 200)
+        for i in range(3):
+            nb.backward_a_fused_batched(*runs[i % copies])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(kern_steps):
+            nb.backward_a_fused_batched(*runs[i % copies])
+        e1.record(stream)
+        e1.synchronize()
+        kern_ms = e0.elapsed_time(e1) / kern_steps
+        nb.check_error()
+    peaks, peak_kind = load_peaks()
+    peak_tf = peaks["bf16_tflops_sustained" if ms > 1000.0 else "bf16_tflops"]
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    return {
+        "metric": "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline",
+        "value": flops * steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 operands, f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"full_step_fused: {len(groups) // 4} layers x (q+k+v, o, gate+up, "
+                               f"down) = {len(groups)} grouped problems, M={groups[0][0].M}, "
+                               "grad_out f32",
+                   "gflop_per_step": flops / 1e9, "algorithmic_mb_per_step": alg_bytes / 1e6,
+                   "l2": f"rotating {copies} input sets, {copies * per_set / 2**20:.0f} MiB > L2",
+                   "timing": f"CUDA graph of {copies} steps, CUDA events",
+                   "entry": "nf4_backward_a_fused_batched", "parallelism": "dp1"},
+        "e2e": None,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": traffic_for("full_step_fused"),
+                     "peak_source": f"{peak_kind} bf16 (f16 nominal rate = bf16)",
+                     "kernel": "to_f16_stream_kernel (beside) + bwd_a_kernel", "kernel_ms": kern_ms,
+                     "timed": "grouped bwd_a_kernel launch alone (f16 operands read in place)"},
+        "gpu_launches": steps * (len(groups) // 48 + 3),
+        "clocks": clocks.summary(),
+    }
+
+
 # Fused input gradient of sibling projections (nf4_backward_a_fused): q/k/v and
 # gate/up of one layer at M = 4096, each part with its own seeded grad_out
 # (fp32) and weight; the weights stacked along N.
@@ -1040,7 +1165,37 @@ def bench_reference_extra(args, rank, world):
 
     build_oracle()
     per_step_s = 60.0 / max(args.steps + args.warmup, 1)
-    if args.workload in BWD_B_WORKLOADS:
+    if args.workload == "full_step_fused":
+        groups = fused_step_groups(1)  # one layer: the other 27 repeat its shapes
+        data = []
+        for g in groups:
+            qs = [oracle.quantize(make_weight(p)) for p in g]
+            data.append((g, [make_grad_out(p) for p in g], qs))
+        per_row = sum(2 * p.N * p.K for g in groups for p in g)
+
+        def run_rows(rows):
+            for g, gos, qs in data:
+                bts = [oracle.dequantize_f16(sc, d, p.K, p.N) for p, (d, sc) in zip(g, qs)]
+                oracle.backward_a_fused_rows([oracle.round_operand(x[:rows], p.go_dtype)
+                                              for p, x in zip(g, gos)], bts,
+                                             np.arange(rows, dtype=np.int32), want_bound=False)
+
+        probe = 8
+        t0 = time.perf_counter()
+        run_rows(probe)
+        rate = probe * per_row / max(time.perf_counter() - t0, 1e-6)
+        rows = max(1, min(groups[0][0].M, int(rate * per_step_s / per_row)))
+
+        def step():
+            run_rows(rows)
+
+        metric = "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline"
+        unit = "TFLOP/s"
+        workload = ("full_step_fused: 28 layers x (q+k+v, o, gate+up, down) = 112 grouped "
+                    f"problems, M={groups[0][0].M}, grad_out f32")
+        what = (f"of {groups[0][0].M} rows of each of the first layer's 4 fused problems per step "
+                "(dequantise + rounding + fp64 fused rows)")
+    elif args.workload in BWD_B_WORKLOADS:
         M, K, N = BWD_B_WORKLOADS[args.workload]
         g = torch.Generator().manual_seed(0)
         bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
@@ -1153,7 +1308,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="full_step",
                     choices=sorted(workloads()) + sorted(FWD_WORKLOADS) + sorted(RMSNORM_WORKLOADS)
-                    + sorted(FUSED) + sorted(BWD_B_WORKLOADS))
+                    + sorted(FUSED) + sorted(BWD_B_WORKLOADS) + ["full_step_fused"])
     ap.add_argument("--layers", type=int, default=None,
                     help="full_step only: run the first L of the 28 layers (a small case for a "
                          "profiler capture)")
@@ -1175,7 +1330,8 @@ def main():
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
 
     if args.workload in RMSNORM_WORKLOADS or args.workload in FWD_WORKLOADS or \
-            args.workload in FUSED or args.workload in BWD_B_WORKLOADS:
+            args.workload in FUSED or args.workload in BWD_B_WORKLOADS or \
+            args.workload == "full_step_fused":
         if args.impl == "reference":
             line = bench_reference_extra(args, rank, world)
         elif world > 1:
@@ -1184,6 +1340,7 @@ def main():
             dev = torch.device("cuda", local)
             torch.cuda.set_device(dev)
             line = (bench_rmsnorm if args.workload in RMSNORM_WORKLOADS else
+                    bench_fused_step if args.workload == "full_step_fused" else
                     bench_fused if args.workload in FUSED else
                     bench_backward_b if args.workload in BWD_B_WORKLOADS else
                     bench_forward)(args, dev)

@@ -213,6 +213,43 @@ int nf4_backward_a_fused(const nf4_part* parts, int count, const float* scales,
                          const uint8_t* data, float* grad_x, int M, int K, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* One problem of nf4_backward_a_fused_batched: the arguments of one
+ * nf4_backward_a_fused call. */
+typedef struct nf4_fused_problem {
+  const nf4_part* parts; /* HOST array of `count` parts (1..8), read before the call returns */
+  int count;
+  const float* scales;   /* the parts' weights stacked along N: [sum N_p][K/64] */
+  const uint8_t* data;   /* [sum N_p][K/2] */
+  float* grad_x;         /* [M][K], overwritten */
+  int M, K;
+} nf4_fused_problem;
+
+/* Bytes of workspace nf4_backward_a_fused_batched needs for these problems
+ * (descriptors, one f16 copy [M][sum N_p] per problem, and the bookkeeping of
+ * the pass beside the GEMM); 0 for count <= 0 or a problem outside the rules. */
+size_t nf4_backward_a_fused_batched_ws_bytes(const nf4_fused_problem* problems, int count);
+
+/*
+ * Many fused problems in one grouped launch: the pre-converted grouped path of
+ * nf4_backward_a_batched_ws over problems that are each a sibling-projection
+ * sum (nf4_backward_a_fused), e.g. the q/k/v and gate/up input gradients of
+ * every layer of a model plus its unfused o and down projections (one part
+ * each) in one call.  Every part's grad_out is rounded to f16 into its columns
+ * of its problem's copy in the workspace, by the pass that runs beside the GEMM
+ * (or before it, when the workspace has room for the descriptors and copies
+ * only); each problem's grad_x equals, bit for bit, what nf4_backward_a_fused
+ * gives for it without a split.  Every problem runs on the pair kernel,
+ * whatever its M.  No counterpart on the pages.
+ *   workspace  caller-owned device memory, 256-byte aligned,
+ *              nf4_backward_a_fused_batched_ws_bytes(problems, count) bytes;
+ *              smaller than the descriptors and copies, NULL or misaligned
+ *              returns NF4_ERR_WORKSPACE and enqueues nothing
+ * Returns NF4_ERR_INVALID or NF4_ERR_ALIGN (nothing enqueued) for a problem
+ * outside the rules of nf4_backward_a_fused or with more than 8 parts.
+ */
+int nf4_backward_a_fused_batched(const nf4_fused_problem* problems, int count, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /*
  * Tokens per pair tile, 256 or 512, that the pre-converted kernel uses for an
  * M x N x K problem run by `pairs` pairs of CTAs (pure host computation).  A

@@ -170,3 +170,68 @@ def test_fused_rejects_bad_arguments_without_launching(nb):
     assert bool((out == 0.0).all())  # zero grad_out, zero weight
     with pytest.raises(ValueError):
         nb.backward_a_fused([gos[0]], w)  # N sums to 64, the stacked weight has 128
+
+
+# ---------------------------------------------------------------- grouped
+def _layer_problems(nb, M, layer_seed, dtypes=None):
+    """A layer's backward as fused problems: q/k/v (3 parts), o (1), gate/up
+    (2), down (1), at reduced widths, with the oracle's f16 operands."""
+    shapes = [((192, 64, 64), 320), ((320,), 320), ((256, 256), 320), ((320,), 512)]
+    out = []
+    for i, (Ns, K) in enumerate(shapes):
+        probs = [Problem(M, N, K, F32, 1.0, 0.02, False, layer_seed + 10 * i + j)
+                 for j, N in enumerate(Ns)]
+        gos, ws, go16s, bts = _parts(nb, probs, dtypes)
+        out.append((gos, nb.stack_weights(ws), go16s, bts))
+    return out
+
+
+def test_fused_batched_matches_single_fused_calls_and_oracle(nb):
+    """Two layers' fused problems (8 problems, 14 parts) in one grouped call,
+    with the pass beside the GEMM and with the pass first: both equal single
+    nf4_backward_a_fused calls without a split bit for bit, and the oracle."""
+    probs = _layer_problems(nb, 700, 100) + _layer_problems(nb, 700, 200, [F32, BF16, F16])
+    items = [(gos, w, None) for gos, w, _, _ in probs]
+    streamed = nb.backward_a_fused_batched(items)
+    arr, keep, _ = nb._fused_array(items)
+    r = lambda x: (x + 255) // 256 * 256
+    seq_bytes = r(640 * len(items)) + sum(r(2 * gos[0].shape[0] * w.N) for gos, w, _ in items)
+    ws = torch.empty(seq_bytes, dtype=torch.uint8, device="cuda")
+    sequential = nb.backward_a_fused_batched(items, ws)
+    nb.check_error()
+    for i, ((gos, w, go16s, bts), a, b) in enumerate(zip(probs, streamed, sequential)):
+        M = gos[0].shape[0]
+        single = nb.backward_a_fused(gos, w, nb.ws_workspace(M, w.N, split=False))
+        nb.check_error()
+        assert torch.equal(a, b), f"problem {i}: streamed != sequential pass"
+        assert torch.equal(a, single), f"problem {i}: grouped != single fused call"
+        rows = sample_rows(M, 8, i)
+        ref, bound = oracle.backward_a_fused_rows(go16s, bts, rows)
+        assert_close(a.cpu().numpy()[rows], ref, bound, f"problem {i}")
+
+
+def test_fused_batched_rejects_bad_problems_without_launching(nb):
+    L = nb.lib()
+    M, K = 300, 128
+    gos = [torch.zeros((M, 64), device="cuda") for _ in range(3)]
+    w = nb.stack_weights([nb.quantize(torch.zeros((K, 64), device="cuda")) for _ in gos])
+    out = torch.full((M, K), 2.0, device="cuda")
+    items = [(gos, w, out)]
+    arr, keep, _ = nb._fused_array(items)
+    need = int(L.nf4_backward_a_fused_batched_ws_bytes(arr, 1))
+    assert need > 2 * M * 192
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert L.nf4_backward_a_fused_batched(arr, 1, None, 0, None) == nb.NF4_ERR_WORKSPACE
+    keep[0][1].N = 60  # a part not a multiple of 8 columns
+    assert L.nf4_backward_a_fused_batched(arr, 1, C.c_void_p(ws.data_ptr()), need, None) == \
+        nb.NF4_ERR_INVALID
+    keep[0][1].N = 64
+    arr[0].count = 9
+    assert L.nf4_backward_a_fused_batched(arr, 1, C.c_void_p(ws.data_ptr()), need, None) == \
+        nb.NF4_ERR_INVALID
+    torch.cuda.synchronize()
+    assert bool((out == 2.0).all())
+    arr[0].count = 3
+    assert L.nf4_backward_a_fused_batched(arr, 1, C.c_void_p(ws.data_ptr()), need, None) == nb.NF4_OK
+    nb.check_error()
+    assert bool((out == 0.0).all())
