@@ -352,11 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
           }
         }
       }
-      // The slot is refilled by TMA (async proxy) once released: order these
-      // generic-proxy reads before that write.
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_raw(rslot));
+      // The raw slot is refilled by TMA (async proxy) once released, so these
+      // generic-proxy reads must be ordered before that write: it is released
+      // after the stage's operand writes (below), where one proxy fence orders
+      // both (every configuration has at least two raw slots per group).
+      static_assert(RS >= 2 * kConvGroups, "a group keeps its raw slot through its stage");
 
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty_op(oslot), ((s / OS) & 1) ^ 1, abort_flag))) {
         ok = false;
@@ -400,7 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) small_m_kernel(const __grid_const
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(full_op(oslot));
+      if (lane == 0) {
+        mbar_arrive(empty_raw(rslot));
+        mbar_arrive(full_op(oslot));
+      }
       if (lead) NF4_PROBE(4, s);
       if (tail) NF4_PROBE(8, s);
     }

@@ -930,11 +930,18 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       const uint4 q = *reinterpret_cast<const uint4*>(
           raw + kGoBytes + (fwd ? static_cast<uint32_t>(fr * 32 + fh * 16) : bn * (BKC / 2) + qchunk));
       const float scale = stma ? *reinterpret_cast<const float*>(raw + scale_off) : scale_pre;
-      // The slot is refilled by TMA (async proxy) once released: order these
-      // generic-proxy reads before that write.
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_raw(rslot));
+      // The slot is refilled by TMA (async proxy) once released, so these
+      // generic-proxy reads must be ordered before that write by a proxy fence.
+      // With at least two raw slots per group the slot is released after the
+      // stage's operand writes, so that the one fence there orders both;
+      // otherwise here, with a fence of its own, so that the group's next
+      // stage does not wait for the refill.
+      constexpr bool kLateRawRelease = kRawStages >= 2 * kConvGroups;
+      if constexpr (!kLateRawRelease) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_raw(rslot));
+      }
 
       if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(empty_op(oslot),
                                                      ((it / kOpStages) & 1u) ^ 1u, abort_flag)))
@@ -983,6 +990,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       __syncwarp();
       if (probe) NF4_PROBE(64 + cw, it);
       if (lane == 0) {
+        if constexpr (kLateRawRelease) mbar_arrive(empty_raw(rslot));
         if (rank == 1) {
           // A 16-byte copy into CTA 0 that completes on CTA 0's operand barrier;
           // issued after this warp's operand writes were handed to the async
