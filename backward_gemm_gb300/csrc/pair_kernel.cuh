@@ -136,12 +136,15 @@ struct Layout {
   static constexpr int kEpiStageBytes = MB == 2 ? 0 : kEpiWarps * kEpiBufs * kEpiBufBytes;
   static constexpr int kBarOff = kEpiOff + kEpiStageBytes;
   // ... + one barrier per epilogue warp for reading other pairs' partial sums
-  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1 + 2 * RA + kEpiWarps + 1;
+  static constexpr int kNumBars = 2 * RS + 2 * OS + 2 + 2 + 1 + 2 * RA + kEpiWarps;
   // misc: TMEM address, abort flag, the ready counter (and spare words), then the
   // 16-byte signal words: in CTA 0 one destination per (operand slot,
   // converter warp of a group), and one source.
   static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
   static constexpr int kReadyOff = kMiscOff + 8;
+  // Two M-blocks: how many epilogue warps have handed their A-ring staging back
+  // (kEpiWarps per item, counted up in item order).
+  static constexpr int kRelOff = kMiscOff + 28;
   static constexpr int kSigOff = kMiscOff + 32;
   static constexpr uint32_t kSigSrcOff = kSigOff + OS * kGroupWarps * kSigBytes;
   static constexpr int kSmemBytes = kSigSrcOff + kSigBytes + 1024;  // + alignment slack
@@ -159,7 +162,14 @@ struct Layout {
   static constexpr bool kEpiInARing = MB == 2;
   static_assert(!kEpiInARing || kEpiWarps * (BK / EC) * kEpiBufBytes <= RA * MB * kABytes,
                 "the A ring holds every epilogue warp's M-block");
-  static_assert(kReadyOff + 4 * OS <= kSigOff, "ready counter fits before the signal area");
+  // A whole (unsplit) tile's epilogue stages half an M-block at a time in two A
+  // slots, half an M-block row band of two epilogue warps per slot, so that the
+  // other two slots take the next item's first stages meanwhile.
+  static constexpr int kHalfStageBytes = (BK / EC / 2) * kEpiBufBytes;
+  static_assert(!kEpiInARing || (RA == 4 && kEpiWarps == 4 && 2 * kHalfStageBytes == MB * kABytes),
+                "two epilogue warps' half M-blocks fill one A slot");
+  static_assert(kReadyOff + 4 * OS <= kRelOff && kRelOff + 4 <= kSigOff,
+                "ready and release counters fit before the signal area");
   static_assert(RS * kBoxes <= 32 && RA <= 32, "one producer lane per (ring slot, box)");
   // Each raw slot must always be consumed by the same converter group.  A group
   // waits for a slot's phase by parity only; if the slot alternated between the
@@ -273,6 +283,17 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc& single, const Problem
     if (batch[mid].tile_begin <= t) lo = mid; else hi = mid - 1;
   }
   return tile_fields(batch[lo], batch + lo, t);
+}
+
+// Two M-blocks: the A slots (bit i = slot i of RA) in which an item's epilogue
+// stages its result, given the global stage count `it_next` at which the next
+// item starts.  A part of a split tile stages whole M-blocks (every slot); a
+// whole tile half an M-block at a time in the two slots that the next item
+// fills third and fourth, so its first two stages load meanwhile.
+template <int RA>
+__device__ __forceinline__ uint32_t epi_stage_slots(bool split_part, uint32_t it_next) {
+  return split_part ? (1u << RA) - 1u
+                    : (1u << ((it_next + 2u) % RA)) | (1u << ((it_next + 3u) % RA));
 }
 
 // ------------------------------------------------------------------ work schedule
@@ -480,10 +501,10 @@ __global__ void __launch_bounds__(L::kThreads, 1)
   auto part_bar = [&](uint32_t w) {
     return bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + 2 * L::kAStages + w);
   };
-  // Two M-blocks: the epilogue warps hand the A ring back after each item (one
-  // phase per item, kEpiWarps arrivals).
-  const uint32_t epi_release =
-      bar0 + 8u * (2 * kRawStages + 2 * kOpStages + 5 + 2 * L::kAStages + kEpiWarps);
+  // Two M-blocks: the epilogue warps hand their A-ring staging back after each
+  // item by counting this word up (the A producer may be more than one item
+  // behind, so a counter, not the phases of a barrier).
+  const uint32_t epi_released = sbase + L::kRelOff;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -524,9 +545,9 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       mbar_init(empty_a(i), 1);
     }
     for (int i = 0; i < kEpiWarps; ++i) mbar_init(part_bar(i), 1);
-    mbar_init(epi_release, kEpiWarps);
     for (int i = 0; i < kOpStages; ++i)
       reinterpret_cast<volatile uint32_t*>(smem + kReadyOff)[i] = 0u;
+    *reinterpret_cast<volatile uint32_t*>(smem + L::kRelOff) = 0u;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -775,12 +796,39 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     if (!sk.streamed) griddep_wait();
     uint32_t it = 0;
     bool ok = true;
+    // Two M-blocks: item `held_item`'s epilogue stages its result in the A
+    // slots `held` until it counts them back (epi_stage_slots).  A copy into one
+    // of them waits for that, and so does the start of the item after next.
+    int held_item = -1;
+    uint32_t held = 0;
+    bool prev_split = false;
+    auto wait_released = [&](int j) -> bool {
+      bool got = true;
+      uint32_t seen = 0;
+      if (lane == 0)
+        got = flag_wait_ge(epi_released, static_cast<uint32_t>(j + 1) * kEpiWarps, abort_flag, &seen);
+      return __shfl_sync(0xFFFFFFFFu, got, 0);
+    };
     for (int k = 0; ok; ++k) {
       const Item w = item_at(sk, cluster, nclusters, k);
       if (w.t < 0) break;
       const Tile tl = tile_at(single, batch, count, w.t);
       const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
       const int row0 = tl.mt * kRowsPerTile + static_cast<int>(rank) * BM;
+      if constexpr (L::kEpiInARing) {
+        if (held_item >= 0 && held_item < k - 1) {
+          if (!wait_released(held_item)) {
+            ok = false;
+            break;
+          }
+          held_item = -1;
+        }
+        if (k > 0) {
+          held_item = k - 1;
+          held = epi_stage_slots<kAStages>(prev_split, it);
+        }
+        prev_split = w.s0 > 0 || s1 < tl.ns;
+      }
       const unsigned int* cnt = sk.streamed ? tl.p->ready : nullptr;
       if (cnt != nullptr) {
         // Each M-block of the tile is one 256-row block of A: wait until the
@@ -804,20 +852,17 @@ __global__ void __launch_bounds__(L::kThreads, 1)
           break;
         }
       }
-      if constexpr (L::kEpiInARing) {
-        // The previous item's epilogue stages its result in the A ring: wait
-        // until its stores have read it.
-        if (k > 0) {
-          bool released = true;
-          if (lane == 0) released = mbar_wait(epi_release, static_cast<uint32_t>(k - 1) & 1u, abort_flag);
-          if (!__shfl_sync(0xFFFFFFFFu, released, 0)) {
-            ok = false;
-            break;
-          }
-        }
-      }
       for (int s = w.s0; s < s1; ++s, ++it) {
         const uint32_t slot = it % kAStages;
+        if constexpr (L::kEpiInARing) {
+          if (held_item >= 0 && ((held >> slot) & 1u) != 0u) {
+            if (!wait_released(held_item)) {
+              ok = false;
+              break;
+            }
+            held_item = -1;
+          }
+        }
         bool free_slot = true;
         if (lane == 0)
           free_slot = mbar_wait_cluster(empty_a(slot), ((it / kAStages) & 1u) ^ 1u, abort_flag);
@@ -1025,6 +1070,7 @@ __global__ void __launch_bounds__(L::kThreads, 1)
     constexpr int kPieces = kEpiCols / 4;  // 16-byte pieces per staged row
     uint8_t* const buf0 = smem + kEpiOff + warp * kEpiBufs * kEpiBufBytes;
     uint32_t lt = 0;
+    uint32_t it_next = 0;  // global stage count at which the next item starts
     for (int k = 0;; ++k, ++lt) {
       const Item w = item_at(sk, cluster, nclusters, k);
       if (w.t < 0) break;
@@ -1032,11 +1078,14 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       const int s1 = w.s1 < tl.ns ? w.s1 : tl.ns;
       const bool partial = w.s0 > 0;                // later stages of a split tile
       const bool finish = !partial && s1 < tl.ns;  // first stages of a split tile
+      it_next += static_cast<uint32_t>(s1 - w.s0);
       // The pair's last item: once its accumulator is full every stage has been
       // consumed, so the operand rings are idle and serve as deep staging (a
       // warp's whole M-block of chunks, no wait for a staging buffer).
-      // With two M-blocks every item does so in the A ring, which the A producer
-      // refills for the next item only after the epilogue has released it.
+      // With two M-blocks every item stages in the A ring (epi_stage_slots): a
+      // whole tile in two of its slots, half an M-block at a time, a part of a
+      // split tile in all of it; the A producer refills those slots only after
+      // the epilogue has counted them back.
       const bool deep = L::kEpiInARing || item_at(sk, cluster, nclusters, k + 1).t < 0;
       // Pairs whose partial sums complete this tile: cluster+1 .. q_last.
       int q_last = cluster;
@@ -1114,7 +1163,62 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         }
         if (threadIdx.x == 0) NF4_PROBE(82, lt * 16 + c);
       };
-      if (!finish && deep) {
+      if (L::kEpiInARing && !finish && !partial) {
+        // A whole tile (two M-blocks): four rounds of half an M-block, staged in
+        // this warp's half of one of the two A slots named by epi_stage_slots
+        // (warps 0-1: the first, 2-3: the second); per round 8 chunks, one proxy
+        // fence and 8 stores, one bulk group each.  A chunk of the next round is
+        // loaded from TMEM while the stores drain, and staged once the store that
+        // read the same place in the previous round is done with it.
+        constexpr int kHalf = BK / kEpiCols / 2;
+        static_assert(kHalf % 2 == 0 && kHalf <= 8, "chunks go two at a time, one bulk group each");
+        const uint32_t hs = (it_next + 2u + static_cast<uint32_t>(warp >> 1)) % kAStages;
+        const uint32_t hoff = kAOff + hs * kASlotBytes + static_cast<uint32_t>(warp & 1) * L::kHalfStageBytes;
+#pragma unroll 1
+        for (int rnd = 0; rnd < 2 * kMBlocks; ++rnd) {
+          const int mb = rnd >> 1;
+          const int h = rnd & 1;
+#pragma unroll 1
+          for (int c = 0; c < kHalf; c += 2) {
+            uint32_t r[kEpiCols], r2[kEpiCols];
+            const int cc = h * kHalf + c;
+            tmem_ld_cols<kEpiCols>(taddr + mb * BK + cc * kEpiCols, r);
+            tmem_ld_cols<kEpiCols>(taddr + mb * BK + (cc + 1) * kEpiCols, r2);
+            tmem_wait_ld();
+            if (rnd > 0) {
+              // The previous round's stores of chunks c and c + 1 (its first
+              // c + 2 bulk groups) have read this staging.
+              if (lane == 0) bulk_wait_read_n(kHalf - 2 - c);
+              __syncwarp();
+            }
+            if (threadIdx.x == 0) NF4_PROBE(83, rnd * kHalf + c);
+            stage_chunk(smem + hoff + c * kEpiBufBytes, r);
+            stage_chunk(smem + hoff + (c + 1) * kEpiBufBytes, r2);
+          }
+          if (rnd == 2 * kMBlocks - 1) {
+            // Every accumulator column has been read: hand TMEM to the next
+            // tile's MMAs before the last stores go out.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (rank == 0) mbar_arrive(tmem_empty(acc));
+              else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (threadIdx.x == 0) NF4_PROBE(81, rnd);
+          if (lane == 0) {
+#pragma unroll 1
+            for (int c = 0; c < kHalf; ++c) {
+              tma_store_2d(&tl.p->tm_out, tl.kt * BK + (h * kHalf + c) * kEpiCols, row0 + mb * 256,
+                           sbase + hoff + c * kEpiBufBytes);
+              bulk_commit();
+            }
+          }
+          if (threadIdx.x == 0) NF4_PROBE(82, rnd);
+        }
+      } else if (!finish && deep) {
         // The pair's last item: the warp stages its whole M-block in the
         // region (chunk c at c x kEpiBufBytes, the staging layout), then
         // one proxy fence and all of the M-block's stores.
@@ -1230,11 +1334,13 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (rank == 0) mbar_arrive(tmem_empty(acc));
-        else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
+        if (!(L::kEpiInARing && !finish && !partial)) {  // (that path handed TMEM back already)
+          if (rank == 0) mbar_arrive(tmem_empty(acc));
+          else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
+        }
         if constexpr (L::kEpiInARing) {
           bulk_wait_read<0>();  // the stores have read the staged result
-          mbar_arrive(epi_release);
+          red_release_shared_add(epi_released, 1u);
         }
         if (partial) {
           // The warp's partial sums are in global memory once its copies have

@@ -246,6 +246,11 @@ __device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v) {
   asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// A shared-memory counter that several threads count up, polled like a flag.
+__device__ __forceinline__ void red_release_shared_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -390,6 +395,20 @@ __device__ __forceinline__ void bulk_commit() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// The same with a run-time count (0..7; larger counts wait for at most 7).
+__device__ __forceinline__ void bulk_wait_read_n(int n) {
+  switch (n) {
+    case 0: bulk_wait_read<0>(); break;
+    case 1: bulk_wait_read<1>(); break;
+    case 2: bulk_wait_read<2>(); break;
+    case 3: bulk_wait_read<3>(); break;
+    case 4: bulk_wait_read<4>(); break;
+    case 5: bulk_wait_read<5>(); break;
+    case 6: bulk_wait_read<6>(); break;
+    default: bulk_wait_read<7>(); break;
+  }
 }
 
 template <int N>
