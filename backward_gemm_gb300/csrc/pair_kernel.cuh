@@ -1164,38 +1164,30 @@ __global__ void __launch_bounds__(L::kThreads, 1)
         if (threadIdx.x == 0) NF4_PROBE(82, lt * 16 + c);
       };
       if (L::kEpiInARing && !finish && !partial) {
-        // A whole tile (two M-blocks): four rounds of half an M-block, staged in
-        // this warp's half of one of the two A slots named by epi_stage_slots
-        // (warps 0-1: the first, 2-3: the second); per round 8 chunks, one proxy
-        // fence and 8 stores, one bulk group each.  A chunk of the next round is
-        // loaded from TMEM while the stores drain, and staged once the store that
-        // read the same place in the previous round is done with it.
-        constexpr int kHalf = BK / kEpiCols / 2;
-        static_assert(kHalf % 2 == 0 && kHalf <= 8, "chunks go two at a time, one bulk group each");
+        // A whole tile (two M-blocks): this warp's 32 chunks go through a ring
+        // of 8 staging buffers, its half of one of the two A slots named by
+        // epi_stage_slots (warps 0-1: the first, 2-3: the second).  Two chunks
+        // per step: TMEM loads, then (once the stores of the chunks 8 earlier
+        // have read these buffers) staging, one proxy fence, two stores of one
+        // bulk group each.  TMEM drains as far ahead of the stores as the ring
+        // allows and goes back to the MMAs with the last loads.
+        constexpr int kChunks = BK / kEpiCols;  // per M-block
+        constexpr int kRing = L::kHalfStageBytes / kEpiBufBytes;
+        constexpr int kTotal = kMBlocks * kChunks;
+        static_assert(kRing % 2 == 0 && kRing >= 4 && kRing <= 9 && kChunks % 2 == 0,
+                      "two chunks per step; at most 7 bulk groups left pending");
         const uint32_t hs = (it_next + 2u + static_cast<uint32_t>(warp >> 1)) % kAStages;
         const uint32_t hoff = kAOff + hs * kASlotBytes + static_cast<uint32_t>(warp & 1) * L::kHalfStageBytes;
 #pragma unroll 1
-        for (int rnd = 0; rnd < 2 * kMBlocks; ++rnd) {
-          const int mb = rnd >> 1;
-          const int h = rnd & 1;
-#pragma unroll 1
-          for (int c = 0; c < kHalf; c += 2) {
-            uint32_t r[kEpiCols], r2[kEpiCols];
-            const int cc = h * kHalf + c;
-            tmem_ld_cols<kEpiCols>(taddr + mb * BK + cc * kEpiCols, r);
-            tmem_ld_cols<kEpiCols>(taddr + mb * BK + (cc + 1) * kEpiCols, r2);
-            tmem_wait_ld();
-            if (rnd > 0) {
-              // The previous round's stores of chunks c and c + 1 (its first
-              // c + 2 bulk groups) have read this staging.
-              if (lane == 0) bulk_wait_read_n(kHalf - 2 - c);
-              __syncwarp();
-            }
-            if (threadIdx.x == 0) NF4_PROBE(83, rnd * kHalf + c);
-            stage_chunk(smem + hoff + c * kEpiBufBytes, r);
-            stage_chunk(smem + hoff + (c + 1) * kEpiBufBytes, r2);
-          }
-          if (rnd == 2 * kMBlocks - 1) {
+        for (int i = 0; i < kTotal; i += 2) {
+          const int mb = i / kChunks;
+          const int cc = i % kChunks;
+          uint32_t r[kEpiCols], r2[kEpiCols];
+          tmem_ld_cols<kEpiCols>(taddr + mb * BK + cc * kEpiCols, r);
+          tmem_ld_cols<kEpiCols>(taddr + mb * BK + (cc + 1) * kEpiCols, r2);
+          tmem_wait_ld();
+          if (threadIdx.x == 0) NF4_PROBE(83, i);
+          if (i + 2 == kTotal) {
             // Every accumulator column has been read: hand TMEM to the next
             // tile's MMAs before the last stores go out.
             tc_fence_before();
@@ -1205,18 +1197,25 @@ __global__ void __launch_bounds__(L::kThreads, 1)
               else mbar_arrive_remote(tmem_empty_leader0 + 8u * acc);
             }
           }
+          if (i >= kRing) {
+            // Chunks i - kRing and i - kRing + 1 used these buffers: their
+            // stores are the oldest two of the last kRing bulk groups.
+            if (lane == 0) bulk_wait_read<kRing - 2>();
+            __syncwarp();
+          }
+          const uint32_t b0 = hoff + static_cast<uint32_t>(i % kRing) * kEpiBufBytes;
+          stage_chunk(smem + b0, r);
+          stage_chunk(smem + b0 + kEpiBufBytes, r2);
           fence_proxy_async_smem();
           __syncwarp();
-          if (threadIdx.x == 0) NF4_PROBE(81, rnd);
           if (lane == 0) {
-#pragma unroll 1
-            for (int c = 0; c < kHalf; ++c) {
-              tma_store_2d(&tl.p->tm_out, tl.kt * BK + (h * kHalf + c) * kEpiCols, row0 + mb * 256,
-                           sbase + hoff + c * kEpiBufBytes);
-              bulk_commit();
-            }
+            tma_store_2d(&tl.p->tm_out, tl.kt * BK + cc * kEpiCols, row0 + mb * 256, sbase + b0);
+            bulk_commit();
+            tma_store_2d(&tl.p->tm_out, tl.kt * BK + (cc + 1) * kEpiCols, row0 + mb * 256,
+                         sbase + b0 + kEpiBufBytes);
+            bulk_commit();
           }
-          if (threadIdx.x == 0) NF4_PROBE(82, rnd);
+          if (threadIdx.x == 0) NF4_PROBE(82, i);
         }
       } else if (!finish && deep) {
         // The pair's last item: the warp stages its whole M-block in the
