@@ -610,6 +610,14 @@ static int grouped_ws(const GProblem* problems, int count, void* workspace, size
     int items = 0;
     for (size_t i = 0; i < descs.size(); ++i) {
       if (jobs_of[i] < 0) continue;
+      // One slab height for all parts of a problem (their counts share the
+      // ready words), from the source bytes of a whole row.
+      size_t row_bytes = 0;
+      for (int q = 0; q < jobs_n[i]; ++q) {
+        const F16Job& f = jobs[jobs_of[i] + q];
+        row_bytes += static_cast<size_t>(f.N) * (f.mode == kSrcF32 ? 4u : 2u);
+      }
+      const int slab = slab_rows_for(row_bytes);
       for (int q = 0; q < jobs_n[i]; ++q) {
         const F16Job& f = jobs[jobs_of[i] + q];
         StreamJob& j = sjobs.job[sjobs.n++];
@@ -623,10 +631,12 @@ static int grouped_ws(const GProblem* problems, int count, void* workspace, size
         j.pitch = f.pitch;
         j.item_begin = items;
         j.groups_per_row = f.groups_per_row;
-        items += (j.M + kSlabRows - 1) / kSlabRows;
+        j.slab_rows = slab;
+        items += (j.M + slab - 1) / slab;
       }
       descs[i].ready = ready;
       descs[i].ready_parts = jobs_n[i];
+      descs[i].slab_rows = slab;
       ready += (descs[i].M + 255) / 256;
     }
     sjobs.items = items;

@@ -213,13 +213,15 @@ struct ProblemDesc {  // 128-byte aligned (CUtensorMap); copied as 16-byte words
   // the 64-wide stages of K.  Pre-converted variant only; scale_tma is 0.
   int fwd;
   // Streamed grouped launch (SkArgs::streamed): per 256-row block of the A
-  // operand, the count of 64-row slabs the concurrent f16 pass has finished
-  // writing; the A producer waits for a block's full count before its first
-  // copy from it.  nullptr otherwise.
+  // operand, the count of slabs (slab_rows rows each) the concurrent f16 pass
+  // has finished writing; the A producer waits for a block's full count before
+  // its first copy from it.  nullptr otherwise.
   const unsigned int* ready;
   // Pass jobs counted into each ready word: the parts of a fused problem write
   // their column slices of the same rows (1 for a plain problem).
   int ready_parts;
+  // Rows of one pass slab of this problem (8, 16, 32 or 64: divides 256).
+  int slab_rows;
   // Tile order: 1 = output-column tiles fastest over all row blocks; G > 1 =
   // groups of G row blocks, column tiles slowest within a group, so that the
   // pairs running at the same time share both a few row blocks of A and a few
@@ -832,8 +834,8 @@ __global__ void __launch_bounds__(L::kThreads, 1)
       const unsigned int* cnt = sk.streamed ? tl.p->ready : nullptr;
       if (cnt != nullptr) {
         // Each M-block of the tile is one 256-row block of A: wait until the
-        // pass has written all its 64-row slabs (fewer in a last, partial
-        // block), then order those generic-proxy writes before the copies.
+        // pass has written all its slabs (fewer in a last, partial block), then
+        // order those generic-proxy writes before the copies.
         // (A problem whose grad_out came in f16 has no pass and no counters.)
         bool ready = true;
         if (lane == 0) {
@@ -841,8 +843,9 @@ __global__ void __launch_bounds__(L::kThreads, 1)
             const int rb = tl.mt * kMBlocks + b;
             const int rows = tl.M - rb * 256;
             if (rows <= 0) break;
+            const int sr = tl.p->slab_rows;
             const unsigned int need = static_cast<unsigned int>(tl.p->ready_parts) *
-                                      static_cast<unsigned int>(((rows < 256 ? rows : 256) + 63) / 64);
+                                      static_cast<unsigned int>(((rows < 256 ? rows : 256) + sr - 1) / sr);
             ready = flag_wait_global_ge(cnt + rb, need, abort_flag);
           }
           fence_proxy_async_global();

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(256) to_f16_group_kernel(const __grid_constant
 // threads, at most 32 registers, no shared memory) fits on an SM next to a
 // GEMM CTA (768 threads x 80 registers, ~221 KB of shared memory).
 //
-// Work items are 64-row slabs of the problems, in the GEMM's order; blocks
+// Work items are slabs of rows of the problems, in the GEMM's order; blocks
 // take them through a global counter, so slabs finish roughly in order.  After
 // a slab, the block counts it into its 256-row block's `ready` word (release);
 // the GEMM's A producer waits for a block's full count (acquire) before its
@@ -168,7 +168,11 @@ __global__ void __launch_bounds__(256) to_f16_group_kernel(const __grid_constant
 // next rows is prefetched into L2 ahead of the loads, which gives the pass its
 // memory-level parallelism without registers or shared memory.
 constexpr int kStreamThreads = 128;
-constexpr int kSlabRows = 64;
+// Rows of a slab: at most 64, fewer for wide rows (slab_rows_for), so that a
+// 256-row block of a wide problem is spread over many blocks of the pass
+// instead of waiting for four long slabs.
+constexpr int kSlabMaxRows = 64;
+constexpr size_t kSlabTargetBytes = 256u << 10;  // source bytes of a slab, at most (above 8 rows)
 constexpr int kStreamMaxJobs = 256;
 constexpr int kStreamClaimWords = 256;  // per-SM claim flags (indexed by %smid)
 constexpr int kStreamPrefetchAhead = 8;  // loop turns of source prefetched ahead
@@ -176,11 +180,20 @@ constexpr int kStreamPrefetchAhead = 8;  // loop turns of source prefetched ahea
 struct StreamJob {
   const void* src;      // grad_out [M][N]
   uint16_t* dst;        // f16 copy: ldh columns of rows `pitch` elements apart
-  unsigned int* ready;  // [ceil(M / 256)] finished 64-row slabs per 256-row block
+  unsigned int* ready;  // [ceil(M / 256)] finished slabs per 256-row block
   int mode, M, N, ldh, pitch;
   int item_begin;       // first work item (slab) of this job
   int groups_per_row;   // (ldh + 15) / 16
+  int slab_rows;        // rows per slab (divides 256)
 };
+
+// Slab rows for a problem whose pass reads `row_bytes` source bytes per row (all
+// parts): the largest of 64, 32, 16, 8 whose slab stays within kSlabTargetBytes.
+inline int slab_rows_for(size_t row_bytes) {
+  int s = kSlabMaxRows;
+  while (s > 8 && static_cast<size_t>(s) * row_bytes > kSlabTargetBytes) s >>= 1;
+  return s;
+}
 struct StreamJobs {
   StreamJob job[kStreamMaxJobs];
   unsigned int* next;    // work-item counter, zero at launch
@@ -214,8 +227,8 @@ __global__ void __launch_bounds__(kStreamThreads, 16)
       if (jobs.job[mid].item_begin <= item) lo = mid; else hi = mid - 1;
     }
     const StreamJob& j = jobs.job[lo];
-    const int r0 = (item - j.item_begin) * kSlabRows;
-    const int rows = min(kSlabRows, j.M - r0);
+    const int r0 = (item - j.item_begin) * j.slab_rows;
+    const int rows = min(j.slab_rows, j.M - r0);
     const int gpr = j.groups_per_row;
     const int total = rows * gpr;
     // The slab's source is one contiguous run of rows; each loop turn reads

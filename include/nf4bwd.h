@@ -363,8 +363,9 @@ size_t nf4_backward_a_batched_ws_bytes(const nf4_problem* problems, int count);
  * fp32 or bf16 grad_out is rounded to f16 into the workspace, and one
  * persistent launch of the pair kernel with TMA-loaded A operands runs all
  * problems' tiles (longest first).  With the full workspace the rounding pass
- * runs BESIDE the GEMM: one block of it per SM converts 64-row slabs in the
- * GEMM's order and counts each finished slab into its 256-row block's ready
+ * runs BESIDE the GEMM: one block of it per SM converts slabs of rows (8 to 64
+ * rows, fewer for wide rows) in the GEMM's order and counts each finished slab
+ * into its 256-row block's ready
  * word; the GEMM (a programmatic dependent of the pass, so it starts as soon
  * as the pass has) waits for a block's count before its first copy from it.
  * With room for the descriptors and copies only, the passes run first and the
