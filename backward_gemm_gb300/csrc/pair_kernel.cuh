@@ -447,8 +447,11 @@ __device__ __forceinline__ float cc_scale_fwd(const ConvCursor& c, uint32_t rank
 // Progress slots (NF4_PROGRESS builds): 0 producer stages issued, 1 MMA stages
 // committed, 2 MMA tiles committed, 3 watcher stages published, 4-19 stages
 // finished by converter warp 0-15, 20-23 tiles stored by epilogue warp 0-3.
+// At most 72 registers a thread (the launch-bounds limit would be 85): the
+// CTA's 768 threads then leave 8,192 registers of the SM for a block of the
+// streamed f16 pass beside it.
 template <class L>
-__global__ void __launch_bounds__(L::kThreads, 1)
+__global__ void __maxnreg__(72)
     bwd_a_kernel(const __grid_constant__ ProblemDesc single, const ProblemDesc* __restrict__ batch,
                  int count, const __grid_constant__ SkArgs sk) {
   constexpr int kRawStages = L::kRawStages;

@@ -155,9 +155,10 @@ __global__ void __launch_bounds__(256) to_f16_group_kernel(const __grid_constant
 // The GEMM's tiles consume the problems' A operands in order, a few 256-row
 // blocks at a time, and is bound by the tensor pipe and its shared-memory
 // feed, while the pass is bound by HBM: run together, the pass's traffic fits
-// in the bandwidth the GEMM leaves unused.  A block of this kernel (128
+// in the bandwidth the GEMM leaves unused.  A block of this kernel (256
 // threads, at most 32 registers, no shared memory) fits on an SM next to a
-// GEMM CTA (768 threads x 80 registers, ~221 KB of shared memory).
+// GEMM CTA (768 threads x at most 72 registers, ~221 KB of shared memory):
+// 55,296 + 8,192 of the 65,536 registers.
 //
 // Work items are slabs of rows of the problems, in the GEMM's order; blocks
 // take them through a global counter, so slabs finish roughly in order.  After
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(256) to_f16_group_kernel(const __grid_constant
 // keep the GEMM's CTA off that SM, so it leaves at once.  The source of the
 // next rows is prefetched into L2 ahead of the loads, which gives the pass its
 // memory-level parallelism without registers or shared memory.
-constexpr int kStreamThreads = 128;
+constexpr int kStreamThreads = 256;
 // Rows of a slab: at most 64, fewer for wide rows (slab_rows_for), so that a
 // 256-row block of a wide problem is spread over many blocks of the pass
 // instead of waiting for four long slabs.
@@ -202,7 +203,7 @@ struct StreamJobs {
 };
 static_assert(sizeof(StreamJobs) <= 32000, "kernel parameter limit");
 
-__global__ void __launch_bounds__(kStreamThreads, 16)
+__global__ void __launch_bounds__(kStreamThreads, 8)
     to_f16_stream_kernel(const __grid_constant__ StreamJobs jobs) {
   // The GEMM may be scheduled now, beside this kernel's blocks.
   griddep_launch_dependents();
