@@ -229,6 +229,21 @@ def bench_ours(args, rank, world, dev):
         graph.replay()
         stream.synchronize()
 
+        # The dominant kernel alone: with the ws entry a step is the f16 pre-pass
+        # plus the GEMM; the GEMM is timed by itself by handing it the f16 copy
+        # that the warm-up steps left in each set's workspace (the f16 grad_out entry
+        # skips the pre-pass), over the same rotating sets.  It is timed before
+        # the steps: a step's pass adds HBM traffic that can hold the GPU at its
+        # power cap, and the lowered SM clock would carry over into a timing
+        # taken right after them.  Its clocks are sampled on their own.
+        kernel_ms = None
+        with ClockSampler(dev.index) as kclocks:
+            if entry == "ws" and len(probs) == 1 and probs[0].N % 8 == 0:
+                kernel_ms = time_gemm_only(sets, probs[0], stream, dev, min(args.steps, 200))
+            elif entry == "ws" and len(probs) > 1 and all(p.M > SMALL_M_MAX for p in probs):
+                kernel_ms = time_group_gemm_only(sets, probs, stream, dev, min(args.steps, 200))
+        kernel_clocks = kclocks.summary() if kernel_ms is not None else None
+
         K = args.steps
         full, rem = divmod(K, copies)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -261,16 +276,6 @@ def bench_ours(args, rank, world, dev):
     if not args.no_e2e:
         e2e = bench_e2e(args, probs, host_go, sets, stream, dev, flops, world)
 
-    # The dominant kernel alone: with the ws entry a step is the f16 pre-pass
-    # plus the GEMM; the GEMM is timed by itself by handing it the f16 copy that
-    # the steps left in each set's workspace (the f16 grad_out entry skips the
-    # pre-pass), over the same rotating sets.
-    kernel_ms = None
-    if entry == "ws" and len(probs) == 1 and probs[0].N % 8 == 0:
-        kernel_ms = time_gemm_only(sets, probs[0], stream, dev, min(K, 200))
-    elif entry == "ws" and len(probs) > 1 and all(p.M > SMALL_M_MAX for p in probs):
-        kernel_ms = time_group_gemm_only(sets, probs, stream, dev, min(K, 200))
-
     peaks, peak_kind = load_peaks()
     long_run = ms > 1000.0
     peak_tf = peaks["bf16_tflops_sustained" if long_run else "bf16_tflops"]
@@ -292,10 +297,14 @@ def bench_ours(args, rank, world, dev):
     roof["kernel"] = kernel_names(probs, entry)
     roof["kernel_ms"] = kern_ms
     roof["timed"] = ("whole step" if kernel_ms is None else
-                     "bwd_a_kernel alone (f16 grad_out entry, CUDA events, same rotating sets)"
+                     "bwd_a_kernel alone (f16 grad_out entry, CUDA events, same rotating sets, "
+                     "before the timed steps)"
                      if len(probs) == 1 else
                      "grouped bwd_a_kernel launch alone (f16 grad_out read in place, CUDA events, "
-                     "same rotating sets; its descriptor-upload kernels, ~2 us each, included)")
+                     "same rotating sets, before the timed steps; its descriptor-upload kernels, "
+                     "~2 us each, included)")
+    if kernel_clocks is not None:
+        roof["clocks"] = kernel_clocks
 
     line = {
         "metric": "NF4 backward-A GEMM TFLOP/s and % of GB300 dense FP16 tensor/HBM roofline",
@@ -465,22 +474,12 @@ def bench_fused_step(args, dev):
                 nb.backward_a_fused_batched(items, ws)
         graph.replay()
         stream.synchronize()
-        full, rem = divmod(steps, copies)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        with ClockSampler(dev.index) as clocks:
-            ev0.record(stream)
-            for _ in range(full):
-                graph.replay()
-            for i in range(rem):
-                nb.backward_a_fused_batched(*sets[i])
-            ev1.record(stream)
-            ev1.synchronize()
-        ms = ev0.elapsed_time(ev1)
-        nb.check_error()
         # The grouped GEMM alone: each problem's f16 operand [M][sum N] is in
-        # the workspace after the steps (descriptors first, then the copies in
-        # problem order); given as one f16 part it is read in place.
+        # the workspace after the warm-up steps (descriptors first, then the
+        # copies in problem order); given as one f16 part it is read in place.
+        # Timed before the steps, with its own clock samples: a step's pass adds
+        # HBM traffic that can hold the GPU at its power cap, and the lowered SM
+        # clock would carry over into a timing taken right after them.
         runs = []
         desc = (640 * len(groups) + 255) // 256 * 256
         for items, ws in sets:
@@ -497,12 +496,26 @@ def bench_fused_step(args, dev):
             nb.backward_a_fused_batched(*runs[i % copies])
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for i in range(kern_steps):
-            nb.backward_a_fused_batched(*runs[i % copies])
-        e1.record(stream)
-        e1.synchronize()
+        with ClockSampler(dev.index) as kclocks:
+            e0.record(stream)
+            for i in range(kern_steps):
+                nb.backward_a_fused_batched(*runs[i % copies])
+            e1.record(stream)
+            e1.synchronize()
         kern_ms = e0.elapsed_time(e1) / kern_steps
+        nb.check_error()
+        full, rem = divmod(steps, copies)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index) as clocks:
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                nb.backward_a_fused_batched(*sets[i])
+            ev1.record(stream)
+            ev1.synchronize()
+        ms = ev0.elapsed_time(ev1)
         nb.check_error()
     peaks, peak_kind = load_peaks()
     peak_tf = peaks["bf16_tflops_sustained" if ms > 1000.0 else "bf16_tflops"]
@@ -525,7 +538,9 @@ def bench_fused_step(args, dev):
                      "frac": achieved / peak_tf, "traffic": traffic_for("full_step_fused"),
                      "peak_source": f"{peak_kind} bf16 (f16 nominal rate = bf16)",
                      "kernel": "to_f16_stream_kernel (beside) + bwd_a_kernel", "kernel_ms": kern_ms,
-                     "timed": "grouped bwd_a_kernel launch alone (f16 operands read in place)"},
+                     "timed": "grouped bwd_a_kernel launch alone (f16 operands read in place, "
+                              "before the timed steps)",
+                     "clocks": kclocks.summary()},
         "gpu_launches": steps * (len(groups) // 48 + 3),
         "clocks": clocks.summary(),
     }
