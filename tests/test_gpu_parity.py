@@ -743,3 +743,40 @@ def test_batched_ws_streamed_and_sequential_passes_agree():
         assert torch.equal(a, c), f"problem {i}: not repeatable"
     for p, out, (rows, ref, bound) in zip(probs, streamed, refs):
         assert_close(out.cpu().numpy()[rows], ref, bound, str(p))
+
+
+def test_grouped_512_token_tiles_with_short_items():
+    """Forced 512-token tiles over many short problems (1 to 10 stages of 64),
+    so that every pair runs several short items back to back: a whole tile's
+    epilogue stages in the two A slots its successor fills third and fourth,
+    and the A producer must wait for an older item's hand-back at the start of
+    the item after next when the item between has fewer than three stages.
+    Every result equals the single call with the same tiles bit for bit and
+    the oracle on sampled rows; a second launch repeats the bits."""
+    rng = np.random.default_rng(97)
+    probs = []
+    for i in range(40):
+        N = int(rng.choice([64, 128, 192, 256, 640]))
+        M = int(rng.choice([512, 1000, 1536]))
+        K = int(rng.choice([256, 512]))
+        probs.append(Problem(M, N, K, F32, 1.0, 0.02, bool(i % 3 == 0), 3000 + i))
+    items, refs = [], []
+    for p in probs:
+        go = make_grad_out(p)
+        B = make_weight(p)
+        items.append((to_device_go(go, p.go_dtype), nb().quantize(torch.from_numpy(B).cuda()), None))
+        data_o, scales_o = oracle.quantize(B)
+        bt = oracle.dequantize_f16(scales_o, data_o, p.K, p.N)
+        rows = sample_rows(p.M, 4, p.seed)
+        refs.append((rows,) + oracle.backward_a_rows(oracle.round_operand(go, p.go_dtype), bt, rows))
+    with nb().tile_rows_forced(512), nb().small_m_max(0):
+        ws = nb().batched_ws_workspace(items)
+        outs = nb().backward_a_batched_ws(items, ws)
+        again = nb().backward_a_batched_ws(items, ws)
+        singles = [nb().backward_a_ws(go, w, nb().ws_workspace(p.M, p.N, split=False))
+                   for p, (go, w, _) in zip(probs, items)]
+    nb().check_error()
+    for p, out, out2, single, (rows, ref, bound) in zip(probs, outs, again, singles, refs):
+        assert torch.equal(out, out2), p
+        assert torch.equal(out, single), p
+        assert_close(out.cpu().numpy()[rows], ref, bound, str(p))
