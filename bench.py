@@ -44,6 +44,10 @@ from workloads import (BF16, CONFIGS, DTYPE_NAMES, F32, FUSED, Problem, full_ste
                        make_grad_out, make_weight)
 
 L2_BYTES = 129 * 2**20
+# Idle seconds before a kernel-alone timing that follows the timed steps: a
+# step whose f16 pass runs beside the GEMM can hold the GPU at its power cap,
+# and the lowered clock would otherwise carry over into the next timing.
+KERNEL_PAUSE_S = 2.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -229,21 +233,6 @@ def bench_ours(args, rank, world, dev):
         graph.replay()
         stream.synchronize()
 
-        # The dominant kernel alone: with the ws entry a step is the f16 pre-pass
-        # plus the GEMM; the GEMM is timed by itself by handing it the f16 copy
-        # that the warm-up steps left in each set's workspace (the f16 grad_out entry
-        # skips the pre-pass), over the same rotating sets.  It is timed before
-        # the steps: a step's pass adds HBM traffic that can hold the GPU at its
-        # power cap, and the lowered SM clock would carry over into a timing
-        # taken right after them.  Its clocks are sampled on their own.
-        kernel_ms = None
-        with ClockSampler(dev.index) as kclocks:
-            if entry == "ws" and len(probs) == 1 and probs[0].N % 8 == 0:
-                kernel_ms = time_gemm_only(sets, probs[0], stream, dev, min(args.steps, 200))
-            elif entry == "ws" and len(probs) > 1 and all(p.M > SMALL_M_MAX for p in probs):
-                kernel_ms = time_group_gemm_only(sets, probs, stream, dev, min(args.steps, 200))
-        kernel_clocks = kclocks.summary() if kernel_ms is not None else None
-
         K = args.steps
         full, rem = divmod(K, copies)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -276,6 +265,24 @@ def bench_ours(args, rank, world, dev):
     if not args.no_e2e:
         e2e = bench_e2e(args, probs, host_go, sets, stream, dev, flops, world)
 
+    # The dominant kernel alone: with the ws entry a step is the f16 pre-pass
+    # plus the GEMM; the GEMM is timed by itself by handing it the f16 copy that
+    # the steps left in each set's workspace (the f16 grad_out entry skips the
+    # pre-pass), over the same rotating sets, with its own clock samples.  A
+    # step's pass adds HBM traffic that can hold the GPU at its power cap; an
+    # idle pause first keeps the lowered clock from carrying over.
+    kernel_ms = None
+    kernel_clocks = None
+    if entry == "ws" and (len(probs) == 1 and probs[0].N % 8 == 0 or
+                          len(probs) > 1 and all(p.M > SMALL_M_MAX for p in probs)):
+        time.sleep(KERNEL_PAUSE_S)
+        with ClockSampler(dev.index) as kclocks:
+            if len(probs) == 1:
+                kernel_ms = time_gemm_only(sets, probs[0], stream, dev, min(K, 200))
+            else:
+                kernel_ms = time_group_gemm_only(sets, probs, stream, dev, min(K, 200))
+        kernel_clocks = kclocks.summary()
+
     peaks, peak_kind = load_peaks()
     long_run = ms > 1000.0
     peak_tf = peaks["bf16_tflops_sustained" if long_run else "bf16_tflops"]
@@ -298,11 +305,11 @@ def bench_ours(args, rank, world, dev):
     roof["kernel_ms"] = kern_ms
     roof["timed"] = ("whole step" if kernel_ms is None else
                      "bwd_a_kernel alone (f16 grad_out entry, CUDA events, same rotating sets, "
-                     "before the timed steps)"
+                     f"after the timed steps and a {KERNEL_PAUSE_S:g} s pause)"
                      if len(probs) == 1 else
                      "grouped bwd_a_kernel launch alone (f16 grad_out read in place, CUDA events, "
-                     "same rotating sets, before the timed steps; its descriptor-upload kernels, "
-                     "~2 us each, included)")
+                     f"same rotating sets, after the timed steps and a {KERNEL_PAUSE_S:g} s pause; "
+                     "its descriptor-upload kernels, ~2 us each, included)")
     if kernel_clocks is not None:
         roof["clocks"] = kernel_clocks
 
@@ -474,12 +481,23 @@ def bench_fused_step(args, dev):
                 nb.backward_a_fused_batched(items, ws)
         graph.replay()
         stream.synchronize()
+        full, rem = divmod(steps, copies)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(dev.index) as clocks:
+            ev0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            for i in range(rem):
+                nb.backward_a_fused_batched(*sets[i])
+            ev1.record(stream)
+            ev1.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        nb.check_error()
         # The grouped GEMM alone: each problem's f16 operand [M][sum N] is in
-        # the workspace after the warm-up steps (descriptors first, then the
-        # copies in problem order); given as one f16 part it is read in place.
-        # Timed before the steps, with its own clock samples: a step's pass adds
-        # HBM traffic that can hold the GPU at its power cap, and the lowered SM
-        # clock would carry over into a timing taken right after them.
+        # the workspace after the steps (descriptors first, then the copies in
+        # problem order); given as one f16 part it is read in place.  Timed
+        # after an idle pause (KERNEL_PAUSE_S), with its own clock samples.
         runs = []
         desc = (640 * len(groups) + 255) // 256 * 256
         for items, ws in sets:
@@ -496,6 +514,7 @@ def bench_fused_step(args, dev):
             nb.backward_a_fused_batched(*runs[i % copies])
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
+        time.sleep(KERNEL_PAUSE_S)
         with ClockSampler(dev.index) as kclocks:
             e0.record(stream)
             for i in range(kern_steps):
@@ -503,19 +522,6 @@ def bench_fused_step(args, dev):
             e1.record(stream)
             e1.synchronize()
         kern_ms = e0.elapsed_time(e1) / kern_steps
-        nb.check_error()
-        full, rem = divmod(steps, copies)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        with ClockSampler(dev.index) as clocks:
-            ev0.record(stream)
-            for _ in range(full):
-                graph.replay()
-            for i in range(rem):
-                nb.backward_a_fused_batched(*sets[i])
-            ev1.record(stream)
-            ev1.synchronize()
-        ms = ev0.elapsed_time(ev1)
         nb.check_error()
     peaks, peak_kind = load_peaks()
     peak_tf = peaks["bf16_tflops_sustained" if ms > 1000.0 else "bf16_tflops"]
@@ -539,7 +545,7 @@ def bench_fused_step(args, dev):
                      "peak_source": f"{peak_kind} bf16 (f16 nominal rate = bf16)",
                      "kernel": "to_f16_stream_kernel (beside) + bwd_a_kernel", "kernel_ms": kern_ms,
                      "timed": "grouped bwd_a_kernel launch alone (f16 operands read in place, "
-                              "before the timed steps)",
+                              f"after the timed steps and a {KERNEL_PAUSE_S:g} s pause)",
                      "clocks": kclocks.summary()},
         "gpu_launches": steps * (len(groups) // 48 + 3),
         "clocks": clocks.summary(),
