@@ -383,10 +383,12 @@ def bench_forward(args, dev):
             ev1.record(stream)
             ev1.synchronize()
         ms = ev0.elapsed_time(ev1)
-        # The GEMM alone: its f16 A is in each set's workspace after the steps.
+        # The GEMM alone: its f16 A is in each set's workspace after the steps
+        # (timed after an idle pause, KERNEL_PAUSE_S).
         runs = [(ws[: 2 * M * K].view(torch.float16).view(M, K), w, c, ws) for _, w, c, ws in sets]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
+        time.sleep(KERNEL_PAUSE_S)
         e0.record(stream)
         for i in range(steps):
             a16, w, c, ws = runs[i % copies]
@@ -609,6 +611,7 @@ def bench_fused(args, dev):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         kern_steps = min(steps, 200)
         torch.cuda.synchronize(dev)
+        time.sleep(KERNEL_PAUSE_S)  # after the steps: see KERNEL_PAUSE_S
         e0.record(stream)
         for i in range(kern_steps):
             a16, w, out, ws = runs[i % copies]
