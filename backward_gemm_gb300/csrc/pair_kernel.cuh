@@ -162,9 +162,9 @@ struct Layout {
   static constexpr bool kEpiInARing = MB == 2;
   static_assert(!kEpiInARing || kEpiWarps * (BK / EC) * kEpiBufBytes <= RA * MB * kABytes,
                 "the A ring holds every epilogue warp's M-block");
-  // A whole (unsplit) tile's epilogue stages half an M-block at a time in two A
-  // slots, half an M-block row band of two epilogue warps per slot, so that the
-  // other two slots take the next item's first stages meanwhile.
+  // A whole (unsplit) tile's epilogue stages in two A slots, a ring of 16 KB
+  // (eight 2 KB chunk buffers) per epilogue warp, two warps per slot, so that
+  // the other two slots take the next item's first stages meanwhile.
   static constexpr int kHalfStageBytes = (BK / EC / 2) * kEpiBufBytes;
   static_assert(!kEpiInARing || (RA == 4 && kEpiWarps == 4 && 2 * kHalfStageBytes == MB * kABytes),
                 "two epilogue warps' half M-blocks fill one A slot");
@@ -290,8 +290,8 @@ __device__ __forceinline__ Tile tile_at(const ProblemDesc& single, const Problem
 // Two M-blocks: the A slots (bit i = slot i of RA) in which an item's epilogue
 // stages its result, given the global stage count `it_next` at which the next
 // item starts.  A part of a split tile stages whole M-blocks (every slot); a
-// whole tile half an M-block at a time in the two slots that the next item
-// fills third and fourth, so its first two stages load meanwhile.
+// whole tile goes through a 16 KB chunk ring per warp in the two slots that
+// the next item fills third and fourth, so its first two stages load meanwhile.
 template <int RA>
 __device__ __forceinline__ uint32_t epi_stage_slots(bool split_part, uint32_t it_next) {
   return split_part ? (1u << RA) - 1u
@@ -1089,9 +1089,9 @@ __global__ void __maxnreg__(72)
       // consumed, so the operand rings are idle and serve as deep staging (a
       // warp's whole M-block of chunks, no wait for a staging buffer).
       // With two M-blocks every item stages in the A ring (epi_stage_slots): a
-      // whole tile in two of its slots, half an M-block at a time, a part of a
-      // split tile in all of it; the A producer refills those slots only after
-      // the epilogue has counted them back.
+      // whole tile in two of its slots (a 16 KB chunk ring per warp), a part of
+      // a split tile in all of it; the A producer refills those slots only
+      // after the epilogue has counted them back.
       const bool deep = L::kEpiInARing || item_at(sk, cluster, nclusters, k + 1).t < 0;
       // Pairs whose partial sums complete this tile: cluster+1 .. q_last.
       int q_last = cluster;
