@@ -93,6 +93,18 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------- clocks
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (every rank gets it), then a barrier; the time
+    itself with one rank.  `device` holds the reduction's tensor (a CUDA device
+    under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return float(t.item())
+
+
 class ClockSampler:
     """Samples SM clock and throttle reasons through NVML (ctypes) every ~2 ms."""
 
@@ -250,11 +262,7 @@ def bench_ours(args, rank, world, dev):
         torch.cuda.synchronize(dev)
         ms = ev0.elapsed_time(ev1)
         nb.check_error()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-        torch.distributed.barrier()
+    ms = max_over_ranks(ms, world, dev)
 
     ms_per_step = ms / K
     value = flops * K * world / (ms * 1e-3) / 1e12  # whole-job TFLOP/s
@@ -1024,7 +1032,7 @@ def bench_e2e(args, probs, host_go, sets, stream, dev, flops, world):
     ev1.record(s_out[0])
     ev1.synchronize()
     torch.cuda.synchronize(dev)
-    ms = ev0.elapsed_time(ev1) / steps
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps, world, dev)
     return {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
             "steps": steps,
