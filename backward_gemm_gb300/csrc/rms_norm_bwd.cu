@@ -154,25 +154,31 @@ __global__ void __launch_bounds__(T) rows_kernel(const float4* __restrict__ x,
 }
 
 // dL/dgamma_i = the sum of the CTAs' partial rows.  A CTA takes 32 columns;
-// warp w sums the partial rows w, w + 8, ... in order (lane = column, so each
-// load is one coalesced 128-byte row piece), then the 8 warp sums are added in
-// warp order: a fixed order, so the result does not depend on timing.
-__global__ void __launch_bounds__(256) gamma_kernel(const float* __restrict__ partial, int parts,
-                                                    int hidden, float* __restrict__ dgamma) {
-  __shared__ float sums[8][32];
+// warp w of its kGammaWarps sums the partial rows w, w + kGammaWarps, ... in
+// order (lane = column, so each load is one coalesced 128-byte row piece; up
+// to 8 of them in flight per warp), then the warp sums are added in warp
+// order: a fixed order, so the result does not depend on timing.  The partial
+// rows are few (4 per SM) and the sum is latency bound, so it is spread over
+// many warps.
+constexpr int kGammaWarps = 32;
+
+__global__ void __launch_bounds__(kGammaWarps * 32)
+    gamma_kernel(const float* __restrict__ partial, int parts, int hidden,
+                 float* __restrict__ dgamma) {
+  __shared__ float sums[kGammaWarps][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int i = blockIdx.x * 32 + lane;
   float s = 0.0f;
   if (i < hidden) {
-#pragma unroll 4
-    for (int b = warp; b < parts; b += 8) s += partial[static_cast<int64_t>(b) * hidden + i];
+#pragma unroll 8
+    for (int b = warp; b < parts; b += kGammaWarps) s += partial[static_cast<int64_t>(b) * hidden + i];
   }
   sums[warp][lane] = s;
   __syncthreads();
   if (warp == 0 && i < hidden) {
     float total = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) total += sums[w][lane];
+    for (int w = 0; w < kGammaWarps; ++w) total += sums[w][lane];
     dgamma[i] = total;
   }
 }
@@ -257,8 +263,8 @@ extern "C" int rms_norm_backward(const float* input, const float* gamma, const f
 #undef NF4_RMSB_LAUNCH
   if (cudaGetLastError() != cudaSuccess) return NF4_ERR_CUDA;
   if (grad_gamma != nullptr) {
-    rmsb::gamma_kernel<<<(hidden_dim + 31) / 32, 256, 0, st>>>(partial, grid, hidden_dim,
-                                                                grad_gamma);
+    rmsb::gamma_kernel<<<(hidden_dim + 31) / 32, rmsb::kGammaWarps * 32, 0, st>>>(
+        partial, grid, hidden_dim, grad_gamma);
     if (cudaGetLastError() != cudaSuccess) return NF4_ERR_CUDA;
   }
   return NF4_OK;
