@@ -557,7 +557,7 @@ def bench_fused_step(args, dev):
                      "timed": "grouped bwd_a_kernel launch alone (f16 operands read in place, "
                               f"after the timed steps and a {KERNEL_PAUSE_S:g} s pause)",
                      "clocks": kclocks.summary()},
-        "gpu_launches": steps * (len(groups) // 48 + 3),
+        "gpu_launches": steps * (-(-len(groups) // DESCS_PER_UPLOAD) + 2),  # uploads, pass, GEMM
         "clocks": clocks.summary(),
     }
 
@@ -869,6 +869,7 @@ def bench_rmsnorm(args, dev):
 
 
 SMALL_M_MAX = 64      # the library's default few-token limit (nf4_set_small_m_max)
+STREAM_MAX_JOBS = 256  # pass jobs the streamed f16 pass takes in one launch (kStreamMaxJobs)
 DESCS_PER_UPLOAD = 48  # descriptors per upload kernel of a grouped launch
 F16_JOBS_PER_LAUNCH = 64  # problems per grouped f16 pass (nf4_backward_a_batched_ws)
 
@@ -952,15 +953,20 @@ def launches_per_step(probs, entry="plain") -> int:
     """Kernel launches of one step through the C ABI: a single problem is one
     launch (two with the ws entry: the f16 pre-pass and the GEMM); a grouped
     call launches one few-token kernel per problem with M <= 64, then the
-    descriptor uploads and one grouped GEMM for the rest."""
+    descriptor uploads and one grouped GEMM for the rest, plus with the ws
+    entry the f16 pass: one launch beside the GEMM when the workspace has room
+    for its bookkeeping (the bench's always has) and at most STREAM_MAX_JOBS
+    problems need a copy, else F16_JOBS_PER_LAUNCH problems per launch before
+    it."""
     if len(probs) == 1:
         return 2 if entry == "ws" and probs[0].M > SMALL_M_MAX else 1
     few = sum(1 for p in probs if p.M <= SMALL_M_MAX)
     rest = len(probs) - few
     if not rest:
         return few
-    # grouped ws entry: + the f16 passes, F16_JOBS_PER_LAUNCH problems each
-    passes = -(-rest // F16_JOBS_PER_LAUNCH) if entry == "ws" else 0
+    passes = 0
+    if entry == "ws":
+        passes = 1 if rest <= STREAM_MAX_JOBS else -(-rest // F16_JOBS_PER_LAUNCH)
     return few + -(-rest // DESCS_PER_UPLOAD) + passes + 1
 
 
