@@ -105,3 +105,28 @@ def test_tile_rows_choice_for_the_workloads():
     assert nb.tile_rows(4096, 512, 4096, P) == 512           # 8 stages
     with pytest.raises(ValueError):
         nb.tile_rows(0, 64, 64, P)
+
+
+def test_backward_b_token_splits():
+    """GemmBackwardB cuts the token range (the contraction, 64 tokens a stage)
+    only when its (256 x 256) output tiles leave pairs idle, into at most
+    pairs // tiles runs of at least 8 stages each."""
+    L = nb.lib()
+    P = 76
+    for M, K, N in [(4096, 1536, 1536), (4096, 16, 8960), (4096, 16, 1536), (512, 16, 256),
+                    (511, 16, 256), (64, 8, 8), (100000, 16, 256), (4096, 4096, 14336)]:
+        tiles = -(-K // 256) * -(-N // 256)
+        stages = -(-M // 64)
+        s = int(L.nf4_gemm_backward_b_splits(M, K, N, P))
+        assert s >= 1
+        if tiles >= P:
+            assert s == 1, (M, K, N)
+        else:
+            assert s * tiles <= P and (s == 1 or 8 * s <= stages), (M, K, N, s)
+            assert s == max(1, min(P // tiles, stages // 8)), (M, K, N, s)
+    assert int(L.nf4_gemm_backward_b_splits(4096, 16, 8960, P)) == 2     # rank-16 adapter, 35 tiles
+    assert int(L.nf4_gemm_backward_b_splits(4096, 1536, 1536, P)) == 2   # 36 tiles
+    assert int(L.nf4_gemm_backward_b_splits(511, 16, 256, P)) == 1       # 8 stages: one run
+    assert int(L.nf4_gemm_backward_b_splits(0, 16, 256, P)) == 1         # no tokens
+    for bad in [(-1, 16, 256, P), (64, 0, 256, P), (64, 16, 0, P), (64, 16, 256, 0)]:
+        assert int(L.nf4_gemm_backward_b_splits(*bad)) == -1
